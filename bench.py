@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the absorbed MLA decode step on GB300.
+
+One step = one pass of the whole hot path over one batch of the full-step
+workload (batch 128, 128 heads, d_model 7168, q_lora 1536, cache of 8191
+tokens per sequence + 1 appended = 8192): mla_append_kv -> mla_absorb_q ->
+mla_decode_attention (+ split-KV combine) -> mla_out_absorb, all in libmla
+kernels. Inputs are synthetic (seeded), resident in HBM before the timed region,
+and larger than L2 (1.21 GB latent cache + 374 MB of weights), so no L2 flush is
+needed between steps.
+
+`value` is the step's algorithmic bytes (latent cache rows read once, weights read
+once, q/out/new-row traffic) per second, summed over all ranks. `e2e` is the same
+metric through the public Python API with the step's per-token inputs (hidden
+states, positions, lengths) copied from pinned host memory and the output y copied
+back inside the timed region; the cache and weights are device-resident state.
+
+--impl reference times the fp64 CPU oracle (the only other implementation) on a
+bounded sample of the same workload on this machine's host cores.
+
+Multi-GPU: the decode step shards by sequence with no exchange, so N ranks run N
+independent replicas of the batch (weak scaling) and rank 0 reports the total.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import threading
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+WORKLOAD = "step"
+
+
+def _measured_peaks():
+    path = os.path.join(HERE, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def step_costs(d):
+    """Algorithmic bytes and flops of one full step (see the design doc for the derivation)."""
+    B, H, dm, ql = d["B"], d["H"], d["d_model"], d["q_lora"]
+    L = d["seqlens_after"].astype(np.int64)
+    weights = 2 * (576 * dm + ql * dm + H * 128 * ql + H * 64 * ql + H * 128 * 512 * 2 +
+                   dm * H * 128)
+    cache = int(L.sum()) * 576 * 2
+    act = B * dm * 2 * 2 + B * 576 * 2 + B * H * (576 * 2 + 512 * 2 + 4)
+    attn_flops = int(L.sum()) * 2 * H * (576 + 512)
+    proj_flops = 2 * B * (weights // 2)
+    return {"bytes": weights + cache + act, "flops": attn_flops + proj_flops,
+            "attn_bytes": cache + B * H * (576 * 2 + 512 * 2 + 4), "attn_flops": attn_flops,
+            "weight_bytes": weights, "cache_bytes": cache}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("MLA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- CPU oracle leg
+
+def time_oracle(d, n_seq: int):
+    """The fp64 oracle's full step on the first n_seq sequences; returns (seconds, info)."""
+    import oracle
+    rows = list(range(n_seq))
+    cache = d["kv_cache"]
+    t0 = time.perf_counter()
+    oracle.append_kv(d["h"][rows], d["w_dkr"], d["pos"][rows], d["block_table"][rows], cache)
+    q_lat, q_rope = oracle.absorb_q(d["h"][rows], d["w_dq"], d["w_uq"], d["w_qr"], d["w_uk"],
+                                    d["pos"][rows], d["rope_theta"])
+    o_lat, _ = oracle.decode_absorbed(q_lat, q_rope, cache, d["block_table"][rows],
+                                      d["seqlens_after"][rows], d["scale"])
+    oracle.out_absorb(o_lat, d["w_uv"], d["w_o"])
+    return time.perf_counter() - t0
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, d, costs, metric, unit):
+    world, rank, _ = _dist_init()
+    if rank != 0:
+        return
+    n_seq = args.ref_sample
+    B = d["B"]
+    for _ in range(args.warmup):
+        time_oracle(d, 1)
+    ts = [time_oracle(d, n_seq) for _ in range(args.steps)]
+    t_step = statistics.median(ts) * B / n_seq
+    value = costs["bytes"] / t_step / 1e9
+    sample = f"{n_seq} of {B} sequences of the full step (all 128 heads, 8192 tokens), " \
+             f"scaled linearly to the batch"
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": dict(d["_cfg"], impl="fp64 CPU oracle"),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": _host_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU leg
+
+def run_gpu(args, d, costs, metric, unit):
+    import torch
+    world, rank, local = _dist_init()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_kv_13_gb300 import mla
+
+    def dbf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def di(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    names = ["w_dkr", "w_dq", "w_uq", "w_qr", "w_uk", "w_uv", "w_o"]
+    wt = {k: dbf(d[k]) for k in names}
+    cache = dbf(d["kv_cache"])
+    bt = di(d["block_table"])
+    h, pos, L = dbf(d["h"]), di(d["pos"]), di(d["seqlens_after"])
+    B, H = d["B"], d["H"]
+    max_len = int(d["seqlens_after"].max())
+    step = mla.DecodeStep(wt, B, H, max_len, num_splits=args.num_splits)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- device-resident timing, with the decode kernel timed inside each step
+    for _ in range(args.warmup):
+        step(h, pos, L, bt, cache)
+    torch.cuda.synchronize(dev)
+    if step.check() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    start.record(stream)
+    w = step.w
+    for i in range(args.steps):
+        mla.append_kv(h, w["w_dkr"], pos, bt, cache, step.theta, step.ws_append)
+        mla.absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, step.theta,
+                     step.q_lat, step.q_rope, step.ws_q)
+        ev[i][0].record(stream)
+        mla.decode_attention(step.q_lat, step.q_rope, cache, bt, L, max_len, step.scale,
+                             step.num_splits, step.o_lat, step.lse, step.ws_att)
+        ev[i][1].record(stream)
+        mla.out_absorb(step.o_lat, w["w_uv"], w["w_o"], step.y, step.ws_out)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop() if clocks else None
+    _barrier(world)
+    t_ms = start.elapsed_time(end)
+    t_ms = _max_over_ranks(t_ms, world, dev)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if step.check() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    # ---- end-to-end through the public API with host buffers
+    h_host = torch.from_numpy(d["h"].view(np.int16)).pin_memory()
+    pos_host = torch.from_numpy(d["pos"]).pin_memory()
+    L_host = torch.from_numpy(d["seqlens_after"]).pin_memory()
+    y_host = torch.empty((B, d["d_model"]), dtype=torch.int16).pin_memory()
+    h_dev = torch.empty_like(h).view(torch.int16)
+    pos_dev, L_dev = torch.empty_like(pos), torch.empty_like(L)
+    for _ in range(2):
+        h_dev.copy_(h_host, non_blocking=True)
+        step(h_dev.view(torch.bfloat16), pos, L, bt, cache)
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        pos_dev.copy_(pos_host, non_blocking=True)
+        L_dev.copy_(L_host, non_blocking=True)
+        y = step(h_dev.view(torch.bfloat16), pos_dev, L_dev, bt, cache)
+        y_host.copy_(y.view(torch.int16), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = h_host.numel() * 2 + pos_host.numel() * 4 + L_host.numel() * 4
+    d2h = y_host.numel() * 2
+
+    if rank != 0:
+        return
+    peaks = _measured_peaks()
+    ms_step = t_ms / args.steps
+    value = costs["bytes"] * world * args.steps / (t_ms * 1e-3) / 1e9
+    tflops = costs["flops"] * world * args.steps / (t_ms * 1e-3) / 1e12
+    roof_s = max(costs["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                 costs["flops"] / (peaks["bf16_tflops"] * 1e12))
+    attn_gbs = costs["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+    traffic = None
+    tr_path = os.path.join(HERE, "profiles", "decode_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            tj = json.load(open(tr_path))
+            if tj.get("kernel_source_hash") == _kernel_hash():
+                traffic = tj.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    launches_per_step = step_launches(step)
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(d["_cfg"], parallelism=f"replicas{world}" if world > 1 else "single",
+                       l2="inputs larger than L2 (1.21 GB cache + 374 MB weights); no flush",
+                       num_splits=args.num_splits or "auto"),
+        "tflops": tflops,
+        "tokens_per_s": B * world * args.steps / (t_ms * 1e-3),
+        "roofline_frac_step": roof_s / (ms_step * 1e-3),
+        "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": attn_gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": attn_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"] + " (burst copy)",
+                     "launch_ms": attn_ms,
+                     "algorithmic_bytes_per_launch": costs["attn_bytes"]},
+        "e2e": {"value": costs["bytes"] * world * args.steps / (e2e_ms * 1e-3) / 1e9,
+                "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        t_s = time_oracle(d, args.cpu_sample)
+        t_step = t_s * B / args.cpu_sample
+        line["cpu_baseline"] = {
+            "value": costs["bytes"] / t_step / 1e9, "unit": unit, "cores": _host_cores(),
+            "kind": "oracle",
+            "sample": f"{args.cpu_sample} of {B} sequences of the full step, scaled linearly"}
+    print(json.dumps(line), flush=True)
+
+
+def step_launches(step) -> int:
+    """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1 (+1 combine), out 3."""
+    from mla_latent_kv_13_gb300 import mla
+    ws_bytes = mla.decode_workspace_size(step.B, step.H, step.max_seqlen, step.num_splits)
+    decode = 1 if ws_bytes <= mla.WS_HEADER_BYTES else 2
+    return 2 + 6 + decode + 3
+
+
+def _kernel_hash() -> str:
+    import hashlib
+    hsh = hashlib.sha256()
+    csrc = os.path.join(HERE, "mla_latent_kv_13_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            hsh.update(f.read())
+    return hsh.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-sample", type=int, default=32)
+    ap.add_argument("--ref-sample", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    import sys
+    sys.path.insert(0, HERE)
+    from mla_latent_kv_13_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    d = synth.make_step_inputs(w, seed=0)
+    d["_cfg"] = dict(w.describe(), seqlen=int(d["seqlens_after"].max()), prefilled=int(d["pos"][0]))
+    costs = step_costs(d)
+    metric = "MLA decode attn: latent-KV GB/s, TFLOP/s and % roofline on 1 GB300"
+    if args.impl == "reference":
+        run_reference(args, d, costs, metric, "GB/s")
+    else:
+        run_gpu(args, d, costs, metric, "GB/s")
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) decode over a
+ * paged, compressed latent KV cache, with the up-projections absorbed.
+ *
+ * Sources (web pages, cited by address and section):
+ *   [V2] sheratonhq.com/news/191949 "DeepSeek-V2 teardown: how MLA and MoE cut
+ *        the KV cache by 93.3%", section 2.1 -- only the low-rank latent c_t is
+ *        cached; W_UK is absorbed into the query projection and W_UV into the
+ *        output projection; queries are low-rank compressed too; a separate
+ *        decoupled-RoPE branch carries position.
+ *   [MW] zskr.cn/news/1409628 "from the memory wall to the compute wall",
+ *        section 2.1 (hidden 7168 -> latent 512; scores = (Q W_DK^T) CKV^T;
+ *        decoupled RoPE), 2.2 (reorder the products by associativity), 2.3 (all
+ *        heads share the compressed cache), 4.2 (fuse Q generation with W_DK).
+ *   [V3] fsdata.site/2026/11/deepseek-v3-mla-optimization, section 1 (paged
+ *        storage of the latent; on-the-fly back projection).
+ *
+ * Conventions shared by every call:
+ *   - bf16 values are passed as uint16_t bit patterns (mla_bf16_t).
+ *   - Every tensor argument is a DEVICE pointer to caller-owned, contiguous,
+ *     row-major memory, unless stated otherwise. The library never allocates,
+ *     frees or retains device memory; it keeps no state between calls.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream), on the device current for the calling thread.
+ *   - Arguments are validated on the host first: a bad argument returns an error
+ *     code and launches nothing.
+ *   - Conditions only the GPU can see (a block-table entry outside the pool for
+ *     a token that is read or written, a position beyond the block table) set a
+ *     sticky error word in the caller's workspace; the affected token is skipped
+ *     (reads are treated as masked, writes are dropped), nothing traps. Read the
+ *     word with mla_check_device_status().
+ *   - A workspace is caller-owned device memory of at least the size the
+ *     matching *_workspace_size() call reports, aligned to 256 bytes. Its first
+ *     256 bytes hold the error word; clear it once with mla_clear_device_status()
+ *     before first use. One workspace may serve consecutive calls on one stream;
+ *     calls that overlap on the GPU must not share one.
+ *
+ * Fixed dimensions (the only ones the kernels are built for):
+ *   d_c = 512 latent, d_rope = 64 decoupled-RoPE key, 576 cached values per
+ *   token, 64 tokens per cache block, d_nope = d_v = 128 per head.
+ * Cache layout: kv_cache[num_blocks][64][576] bf16; row = [c_kv (512) | k_rope (64)],
+ *   k_rope stored already rotated to the token's position.
+ * Block table: block_table[B][max_blocks] int32; token t of sequence b lives in
+ *   block block_table[b][t / 64], slot t % 64. Entries past a sequence's last
+ *   block are never read and may hold any value.
+ * RoPE: pairs (2i, 2i+1) of a 64-vector turn by pos * rope_theta^(-2i/64)
+ *   radians; pos is the 0-based token index within its sequence.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16_t;
+typedef void *mla_stream_t; /* cudaStream_t */
+
+#define MLA_D_C 512
+#define MLA_D_ROPE 64
+#define MLA_D_QK 576
+#define MLA_BLOCK 64
+#define MLA_D_NOPE 128
+#define MLA_D_V 128
+#define MLA_WS_HEADER_BYTES 256
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer         */
+    MLA_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels are built for       */
+    MLA_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_size figure */
+    MLA_ERR_OUT_OF_RANGE = 4, /* device-detected: block id or position out of range */
+    MLA_ERR_TIMEOUT = 5,      /* device-detected: a bounded wait gave up            */
+    MLA_ERR_CUDA = 6          /* a CUDA runtime call failed (launch, sync)          */
+} mla_status_t;
+
+/* Human-readable name of a status code (static storage). */
+const char *mla_status_string(mla_status_t status);
+
+/* ---------------------------------------------------------------- append */
+
+/*
+ * [V2] 2.1, [MW] 2.1: write one new token per sequence into the latent cache.
+ *   x = h[b] . W_DKR^T                (d_model -> 576, fp32 accumulation)
+ *   c_kv = x[0:512]; k_rope = RoPE(x[512:576], pos[b])
+ *   kv_cache[block_table[b][pos[b]/64]][pos[b]%64] = bf16([c_kv | k_rope])  (nearest-even)
+ *
+ * h       [B][d_model] bf16            w_dkr [576][d_model] bf16 (rows 0..511 = W_DKV,
+ * pos     [B] int32 (slot to write)                                rows 512..575 = W_KR)
+ * The caller advances its own sequence lengths after the append (pos is usually
+ * the length before it). Requires 1 <= B <= 4096, d_model a multiple of 64.
+ * Workspace: mla_append_kv_workspace_size(B, d_model).
+ */
+mla_status_t mla_append_kv_workspace_size(int B, int d_model, size_t *bytes);
+mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                           const int32_t *pos, const int32_t *block_table, int max_blocks,
+                           mla_bf16_t *kv_cache, int num_blocks, float rope_theta,
+                           void *workspace, size_t ws_bytes, mla_stream_t stream);
+
+/* ------------------------------------------------------- decode attention */
+
+/*
+ * [V2] 2.1, [MW] 2.1-2.3: absorbed decode attention. For every sequence b and
+ * head h, over the tokens j < seqlens[b] of the paged cache:
+ *   s_j   = scale * (q_lat[b][h] . c_kv_j + q_rope[b][h] . k_rope_j)
+ *   out   = sum_j softmax(s)_j c_kv_j     (the latent output; W_UV is applied later)
+ *   lse   = ln sum_j exp(s_j)             (natural log, fp32)
+ * seqlens[b] = 0 gives out = 0 and lse = -inf.
+ *
+ * q_lat [B][H][512] bf16, q_rope [B][H][64] bf16 (already rotated),
+ * seqlens [B] int32 (0 <= seqlens[b] <= 64 * max_blocks; checked on the device),
+ * out [B][H][512] bf16, lse [B][H] fp32.
+ * H must be 16, 32, 64 or 128. num_splits: 0 = chosen by the library, else the
+ * number of token ranges each sequence is cut into (1..256); the ranges are
+ * merged exactly by their log-sum-exp (split-KV combine).
+ * Workspace: mla_decode_workspace_size(B, H, max_seqlen, num_splits) with the
+ * same B, H and num_splits; max_seqlen is an upper bound of seqlens.
+ */
+mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_splits,
+                                       size_t *bytes);
+mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                  const mla_bf16_t *kv_cache, int num_blocks,
+                                  const int32_t *block_table, int max_blocks,
+                                  const int32_t *seqlens, int B, int H, int max_seqlen,
+                                  float scale, int num_splits, void *workspace,
+                                  size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                  mla_stream_t stream);
+
+/*
+ * The split-KV merge on its own (the last step of mla_decode_attention):
+ *   lse[b][h] = ln sum_s exp(lse_part[b][s][h]);
+ *   out[b][h] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h]
+ * Parts with lse_part = -inf weigh zero; all-empty gives out = 0, lse = -inf.
+ * o_part [B][S][H][512] fp32 (each part already normalised), lse_part [B][S][H] fp32,
+ * out [B][H][512] bf16, lse [B][H] fp32. Needs no workspace.
+ */
+mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S, int H,
+                                mla_bf16_t *out, float *lse, mla_stream_t stream);
+
+/* ------------------------------------------------- absorbed projections */
+
+/*
+ * [V2] 2.1 (query compression, decoupled RoPE, W_UK absorbed into the query),
+ * [MW] 2.2 and 4.2 (Q times W_DK first; fuse query generation with W_DK):
+ *   c_q       = h . W_DQ^T                      (d_model -> q_lora)
+ *   q_nope_i  = c_q . W_UQ_i^T                  (q_lora -> 128, head i)
+ *   q_rope_i  = RoPE(c_q . W_QR_i^T, pos[b])    (q_lora -> 64, head i)
+ *   q_lat_i   = q_nope_i . W_UK_i               (128 -> 512, head i)
+ * Intermediates (c_q, q_nope) are kept as bf16 between the products.
+ *
+ * h [B][d_model]; w_dq [q_lora][d_model]; w_uq [H*128][q_lora]; w_qr [H*64][q_lora];
+ * w_uk [H][128][512] (W_UK_i maps a latent to head i's key: k = W_UK_i c);
+ * pos [B] int32 -> q_lat [B][H][512] bf16, q_rope [B][H][64] bf16.
+ * Requires d_model and q_lora multiples of 64, H in {16, 32, 64, 128}, 1 <= B <= 4096.
+ */
+mla_status_t mla_absorb_q_workspace_size(int B, int d_model, int q_lora, int H, size_t *bytes);
+mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dq,
+                          int q_lora, const mla_bf16_t *w_uq, const mla_bf16_t *w_qr,
+                          const mla_bf16_t *w_uk, int H, const int32_t *pos, float rope_theta,
+                          void *workspace, size_t ws_bytes, mla_bf16_t *q_lat,
+                          mla_bf16_t *q_rope, mla_stream_t stream);
+
+/*
+ * [V2] 2.1 (W_UV absorbed into the output projection):
+ *   o_v_i = W_UV_i . o_lat_i    (512 -> 128, head i)
+ *   y     = [o_v_1 | ... | o_v_H] . W_O^T        (H*128 -> d_model)
+ * o_lat [B][H][512] bf16; w_uv [H][128][512]; w_o [d_model][H*128] -> y [B][d_model] bf16.
+ * o_v is kept as bf16 between the products. Requires d_model a multiple of 64.
+ */
+mla_status_t mla_out_absorb_workspace_size(int B, int H, int d_model, size_t *bytes);
+mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf16_t *w_uv,
+                            const mla_bf16_t *w_o, int d_model, void *workspace, size_t ws_bytes,
+                            mla_bf16_t *y, mla_stream_t stream);
+
+/* ------------------------------------------------------- device status */
+
+/* Zero the workspace's error word (asynchronous on `stream`). */
+mla_status_t mla_clear_device_status(void *workspace, mla_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return the first device-detected error recorded in
+ * the workspace (MLA_OK if none) and clear it. Returns MLA_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+mla_status_t mla_check_device_status(void *workspace, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

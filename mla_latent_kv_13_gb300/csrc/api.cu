@@ -1,0 +1,363 @@
+// api.cu -- the C ABI of libmla (declared in include/mla.h): host-side validation,
+// workspace layout, split planning and kernel launches.
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mla;
+
+namespace {
+
+constexpr size_t HDR = MLA_WS_HEADER_BYTES;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t S(mla_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+uint32_t *err_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+bool heads_ok(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+
+// K cut into ranges (multiples of 64) so that n-tiles x m-tiles x splits covers
+// about two waves of the SMs.
+void plan_ksplit(int M, int N, int K, int &splits, int &per) {
+    int tiles = ((N + 63) / 64) * ((M + 63) / 64);
+    int target = 2 * device_sm_count();
+    int kblocks = K / 64;
+    int s = (target + tiles - 1) / tiles;
+    if (s < 1) s = 1;
+    if (s > kblocks) s = kblocks;
+    per = ((kblocks + s - 1) / s) * 64;
+    splits = (K + per - 1) / per;
+}
+
+// Token ranges per sequence for decode: minimise waves x tiles-per-range.
+int plan_decode_splits(int B, int H, int max_seqlen, int requested) {
+    int T = (max_seqlen + BLOCK - 1) / BLOCK;
+    if (T < 1) T = 1;
+    if (requested > 0) return requested;
+    int ctas = B * ((H + 63) / 64);
+    int sms = device_sm_count();
+    int best = 1;
+    long best_cost = -1;
+    for (int s = 1; s <= 64 && s <= T; ++s) {
+        long waves = (ctas * (long)s + sms - 1) / sms;
+        long cost = waves * ((T + s - 1) / s) * 16 + (s > 1 ? 1 : 0);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+size_t decode_ws_bytes(int B, int H, int splits) {
+    if (splits <= 1) return HDR;
+    size_t o = align256((size_t)B * splits * H * D_C * sizeof(float));
+    size_t l = align256((size_t)B * splits * H * sizeof(float));
+    return HDR + o + l;
+}
+
+}  // namespace
+
+namespace mla {
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+}  // namespace mla
+
+extern "C" {
+
+const char *mla_status_string(mla_status_t s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+        case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+        case MLA_ERR_OUT_OF_RANGE: return "MLA_ERR_OUT_OF_RANGE";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    }
+    return "MLA_ERR_UNKNOWN";
+}
+
+// ------------------------------------------------------------------ append
+
+mla_status_t mla_append_kv_workspace_size(int B, int d_model, size_t *bytes) {
+    if (!bytes || B < 1 || B > 4096 || d_model < 64 || d_model % 64) return MLA_ERR_INVALID_ARG;
+    int splits, per;
+    plan_ksplit(B, D_QK, d_model, splits, per);
+    *bytes = HDR + align256((size_t)splits * B * D_QK * sizeof(float));
+    return MLA_OK;
+}
+
+mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                           const int32_t *pos, const int32_t *block_table, int max_blocks,
+                           mla_bf16_t *kv_cache, int num_blocks, float rope_theta,
+                           void *workspace, size_t ws_bytes, mla_stream_t stream) {
+    if (!h || !w_dkr || !pos || !block_table || !kv_cache || !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || max_blocks < 1 || num_blocks < 1 ||
+        !(rope_theta > 0.f) || !isfinite(rope_theta))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_dkr, 16) || !aligned(kv_cache, 16) ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    size_t need;
+    mla_append_kv_workspace_size(B, d_model, &need);
+    if (ws_bytes < need) return MLA_ERR_WORKSPACE;
+
+    int splits, per;
+    plan_ksplit(B, D_QK, d_model, splits, per);
+    float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + HDR);
+    GemmParams g{};
+    g.A = h; g.lda = d_model; g.a_bstride = 0;
+    g.B = w_dkr; g.ldb = d_model; g.b_bstride = 0;
+    g.M = B; g.N = D_QK; g.K = d_model; g.batch = 1;
+    g.k_splits = splits; g.k_per_split = per;
+    g.c_part = part;
+    cudaError_t e = launch_gemm(g, false, S(stream));
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_append_finalize(part, splits, B, pos, block_table, max_blocks, kv_cache, num_blocks,
+                               rope_theta, err_word(workspace), S(stream));
+    return cuda_status(e);
+}
+
+// ---------------------------------------------------------------- decode
+
+mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_splits,
+                                       size_t *bytes) {
+    if (!bytes || B < 1 || max_seqlen < 0 || num_splits < 0 || num_splits > 256)
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    *bytes = decode_ws_bytes(B, H, plan_decode_splits(B, H, max_seqlen, num_splits));
+    return MLA_OK;
+}
+
+mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                  const mla_bf16_t *kv_cache, int num_blocks,
+                                  const int32_t *block_table, int max_blocks,
+                                  const int32_t *seqlens, int B, int H, int max_seqlen,
+                                  float scale, int num_splits, void *workspace,
+                                  size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                  mla_stream_t stream) {
+    if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !workspace || !out || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
+        max_seqlen > max_blocks * BLOCK || num_splits < 0 || num_splits > 256 ||
+        !isfinite(scale))
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||
+        !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    const int splits = plan_decode_splits(B, H, max_seqlen, num_splits);
+    if (ws_bytes < decode_ws_bytes(B, H, splits)) return MLA_ERR_WORKSPACE;
+
+    const int T = (max_seqlen + BLOCK - 1) / BLOCK;
+    DecodeParams p{};
+    p.q_lat = q_lat; p.q_rope = q_rope; p.cache = kv_cache;
+    p.block_table = block_table; p.seqlens = seqlens;
+    p.num_blocks = num_blocks; p.max_blocks = max_blocks; p.B = B; p.H = H;
+    p.num_splits = splits;
+    p.tiles_per_split = T > 0 ? (T + splits - 1) / splits : 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out; p.lse = lse;
+    p.err = err_word(workspace);
+    if (splits > 1) {
+        char *w = static_cast<char *>(workspace) + HDR;
+        p.o_part = reinterpret_cast<float *>(w);
+        p.lse_part = reinterpret_cast<float *>(
+            w + align256((size_t)B * splits * H * D_C * sizeof(float)));
+    }
+    cudaError_t e = launch_decode_mma(p, S(stream));
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    if (splits > 1) e = launch_combine(p.o_part, p.lse_part, B, splits, H, out, lse, S(stream));
+    return cuda_status(e);
+}
+
+mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S_, int H,
+                                mla_bf16_t *out, float *lse, mla_stream_t stream) {
+    if (!o_part || !lse_part || !out || !lse || B < 1 || S_ < 1 || H < 1 || H > 65535)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(o_part, 16) || !aligned(out, 8) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(o_part, lse_part, B, S_, H, out, lse, S(stream)));
+}
+
+// ------------------------------------------------------------ absorb_q
+
+namespace {
+struct AbsorbQLayout {
+    int s1, per1;     // split of c_q = h W_DQ^T
+    size_t part, cq, qn, total;
+};
+AbsorbQLayout absorb_q_layout(int B, int d_model, int q_lora, int H) {
+    AbsorbQLayout L{};
+    plan_ksplit(B, q_lora, d_model, L.s1, L.per1);
+    size_t part1 = (size_t)L.s1 * B * q_lora * sizeof(float);
+    size_t part2 = (size_t)B * H * D_ROPE * sizeof(float);
+    L.part = HDR;
+    L.cq = L.part + align256(part1 > part2 ? part1 : part2);
+    L.qn = L.cq + align256((size_t)B * q_lora * 2);
+    L.total = L.qn + align256((size_t)B * H * D_NOPE * 2);
+    return L;
+}
+}  // namespace
+
+mla_status_t mla_absorb_q_workspace_size(int B, int d_model, int q_lora, int H, size_t *bytes) {
+    if (!bytes || B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 ||
+        q_lora % 64)
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    *bytes = absorb_q_layout(B, d_model, q_lora, H).total;
+    return MLA_OK;
+}
+
+mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dq,
+                          int q_lora, const mla_bf16_t *w_uq, const mla_bf16_t *w_qr,
+                          const mla_bf16_t *w_uk, int H, const int32_t *pos, float rope_theta,
+                          void *workspace, size_t ws_bytes, mla_bf16_t *q_lat,
+                          mla_bf16_t *q_rope, mla_stream_t stream) {
+    if (!h || !w_dq || !w_uq || !w_qr || !w_uk || !pos || !workspace || !q_lat || !q_rope)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 || q_lora % 64 ||
+        !(rope_theta > 0.f) || !isfinite(rope_theta))
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(w_dq, 16) || !aligned(w_uq, 16) || !aligned(w_qr, 16) ||
+        !aligned(w_uk, 16) || !aligned(q_lat, 16) || !aligned(q_rope, 16) ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    AbsorbQLayout L = absorb_q_layout(B, d_model, q_lora, H);
+    if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+    char *w = static_cast<char *>(workspace);
+    float *part = reinterpret_cast<float *>(w + L.part);
+    uint16_t *cq = reinterpret_cast<uint16_t *>(w + L.cq);
+    uint16_t *qn = reinterpret_cast<uint16_t *>(w + L.qn);
+    cudaStream_t st = S(stream);
+
+    // c_q = h W_DQ^T (bf16 intermediate)
+    GemmParams g{};
+    g.A = h; g.lda = d_model; g.B = w_dq; g.ldb = d_model;
+    g.M = B; g.N = q_lora; g.K = d_model; g.batch = 1;
+    g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
+    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_reduce_bf16(part, L.s1, 1, B, q_lora, cq, q_lora, 0, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+
+    // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128])
+    g = GemmParams{};
+    g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
+    g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
+    g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
+    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+
+    // q_rope = RoPE(c_q W_QR^T)
+    g = GemmParams{};
+    g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
+    g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
+    g.k_splits = 1; g.k_per_split = q_lora; g.c_part = part;
+    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_qrope_finalize(part, 1, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+
+    // q_lat[b, i] = q_nope[b, i] W_UK_i  (per-head product, W_UK_i stored [128][512])
+    g = GemmParams{};
+    g.A = qn; g.lda = H * D_NOPE; g.a_bstride = D_NOPE;
+    g.B = w_uk; g.ldb = D_C; g.b_bstride = (long)D_NOPE * D_C;
+    g.M = B; g.N = D_C; g.K = D_NOPE; g.batch = H;
+    g.k_splits = 1; g.k_per_split = D_NOPE;
+    g.c_bf16 = q_lat; g.ldc = (long)H * D_C; g.c_bstride = D_C;
+    return cuda_status(launch_gemm(g, true, st));
+}
+
+// ---------------------------------------------------------- out_absorb
+
+namespace {
+struct OutLayout {
+    int s2, per2;
+    size_t ov, part, total;
+};
+OutLayout out_layout(int B, int H, int d_model) {
+    OutLayout L{};
+    plan_ksplit(B, d_model, H * D_V, L.s2, L.per2);
+    L.ov = HDR;
+    L.part = L.ov + align256((size_t)B * H * D_V * 2);
+    L.total = L.part + align256((size_t)L.s2 * B * d_model * sizeof(float));
+    return L;
+}
+}  // namespace
+
+mla_status_t mla_out_absorb_workspace_size(int B, int H, int d_model, size_t *bytes) {
+    if (!bytes || B < 1 || B > 4096 || d_model < 64 || d_model % 64) return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    *bytes = out_layout(B, H, d_model).total;
+    return MLA_OK;
+}
+
+mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf16_t *w_uv,
+                            const mla_bf16_t *w_o, int d_model, void *workspace, size_t ws_bytes,
+                            mla_bf16_t *y, mla_stream_t stream) {
+    if (!o_lat || !w_uv || !w_o || !workspace || !y) return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64) return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(o_lat, 16) || !aligned(w_uv, 16) || !aligned(w_o, 16) || !aligned(y, 16) ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    OutLayout L = out_layout(B, H, d_model);
+    if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+    char *w = static_cast<char *>(workspace);
+    uint16_t *ov = reinterpret_cast<uint16_t *>(w + L.ov);
+    float *part = reinterpret_cast<float *>(w + L.part);
+    cudaStream_t st = S(stream);
+
+    // o_v[b, i] = W_UV_i o_lat[b, i]   (per head: A = o_lat [B][512], B = W_UV_i [128][512])
+    GemmParams g{};
+    g.A = o_lat; g.lda = (long)H * D_C; g.a_bstride = D_C;
+    g.B = w_uv; g.ldb = D_C; g.b_bstride = (long)D_V * D_C;
+    g.M = B; g.N = D_V; g.K = D_C; g.batch = H;
+    g.k_splits = 1; g.k_per_split = D_C;
+    g.c_bf16 = ov; g.ldc = (long)H * D_V; g.c_bstride = D_V;
+    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+
+    // y = o_v W_O^T
+    g = GemmParams{};
+    g.A = ov; g.lda = (long)H * D_V; g.B = w_o; g.ldb = (long)H * D_V;
+    g.M = B; g.N = d_model; g.K = H * D_V; g.batch = 1;
+    g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
+    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_status(launch_reduce_bf16(part, L.s2, 1, B, d_model, y, d_model, 0, st));
+}
+
+// -------------------------------------------------------------- status
+
+mla_status_t mla_clear_device_status(void *workspace, mla_stream_t stream) {
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, 8, S(stream)));
+}
+
+mla_status_t mla_check_device_status(void *workspace, mla_stream_t stream) {
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    uint32_t word[2] = {0, 0};
+    if (cudaMemcpyAsync(word, workspace, sizeof word, cudaMemcpyDeviceToHost, S(stream)) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+    if (word[0] != 0) {
+        if (cudaMemsetAsync(workspace, 0, 8, S(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+        if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    return static_cast<mla_status_t>(word[0]);
+}
+
+}  // extern "C"

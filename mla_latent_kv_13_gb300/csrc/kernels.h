@@ -1,0 +1,57 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct GemmParams {
+    const uint16_t *A;  // [batch][M][K] via a_bstride / lda
+    long lda, a_bstride;
+    const uint16_t *B;  // TN: [N][K]; NN: [K][N]
+    long ldb, b_bstride;
+    int M, N, K, batch;
+    int k_splits, k_per_split;  // k_per_split a multiple of 64
+    float *c_part;              // if non-null: fp32 partials [k_splits][batch][M][N]
+    uint16_t *c_bf16;           // else: bf16 C with ldc / c_bstride
+    long ldc, c_bstride;
+};
+
+cudaError_t launch_gemm(const GemmParams &p, bool nn, cudaStream_t stream);
+cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
+                               long ldc, long c_bstride, cudaStream_t stream);
+
+// Append: reduce split partials of x = h W_DKR^T, RoPE the last 64, round, scatter.
+cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_t *pos,
+                                   const int32_t *block_table, int max_blocks, uint16_t *cache,
+                                   int num_blocks, float theta, uint32_t *err,
+                                   cudaStream_t stream);
+
+// Query side: reduce partials of c_q W_QR^T, RoPE per head, write bf16 q_rope.
+cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const int32_t *pos,
+                                  float theta, uint16_t *q_rope, cudaStream_t stream);
+
+struct DecodeParams {
+    const uint16_t *q_lat;     // [B][H][512]
+    const uint16_t *q_rope;    // [B][H][64]
+    const uint16_t *cache;     // [num_blocks][64][576]
+    const int32_t *block_table;
+    const int32_t *seqlens;
+    int num_blocks, max_blocks, B, H;
+    int num_splits, tiles_per_split;
+    float scale_log2;          // scale * log2(e)
+    uint16_t *out;             // [B][H][512]  (written when num_splits == 1)
+    float *lse;                // [B][H]       (written when num_splits == 1)
+    float *o_part;             // [B][S][H][512] (num_splits > 1)
+    float *lse_part;           // [B][S][H]      (num_splits > 1)
+    uint32_t *err;
+};
+
+cudaError_t launch_decode_mma(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
+                           uint16_t *out, float *lse, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace mla

@@ -1,0 +1,265 @@
+"""Thin Python binding of libmla (include/mla.h): argument marshalling only.
+
+Every function takes torch tensors that live on the current CUDA device, passes
+their data pointers and the current stream to the C ABI, and raises MLAError on a
+non-zero status. Importing this module loads libmla.so and raises if it is
+missing: there is no other implementation behind these names.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libmla.so not found at {LIB_PATH}; build it with "
+        "`python -m mla_latent_kv_13_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+D_C, D_ROPE, D_QK, BLOCK, D_NOPE, D_V = 512, 64, 576, 64, 128, 128
+WS_HEADER_BYTES = 256
+
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+          3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_OUT_OF_RANGE", 5: "MLA_ERR_TIMEOUT",
+          6: "MLA_ERR_CUDA"}
+
+
+class MLAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+_szp = ctypes.POINTER(ctypes.c_size_t)
+
+_SIGS = {
+    "mla_status_string": ([_i], ctypes.c_char_p),
+    "mla_append_kv_workspace_size": ([_i, _i, _szp], _i),
+    "mla_append_kv": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _f, _vp, _sz, _vp], _i),
+    "mla_decode_workspace_size": ([_i, _i, _i, _i, _szp], _i),
+    "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
+                              _vp, _vp, _vp], _i),
+    "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "mla_absorb_q_workspace_size": ([_i, _i, _i, _i, _szp], _i),
+    "mla_absorb_q": ([_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _f, _vp, _sz, _vp, _vp,
+                      _vp], _i),
+    "mla_out_absorb_workspace_size": ([_i, _i, _i, _szp], _i),
+    "mla_out_absorb": ([_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
+    "mla_clear_device_status": ([_vp, _vp], _i),
+    "mla_check_device_status": ([_vp, _vp], _i),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+def lib():
+    return _lib
+
+
+def _ok(rc: int, where: str):
+    if rc != 0:
+        raise MLAError(rc, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensors pass as their 16-bit patterns; uint16/int16 views pass through."""
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"expected bf16 storage, got {t.dtype}")
+    return t
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _size(fn, *args) -> int:
+    out = ctypes.c_size_t(0)
+    _ok(getattr(_lib, fn)(*args, ctypes.byref(out)), fn)
+    return int(out.value)
+
+
+def alloc_workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
+    """Caller-owned workspace (256-byte aligned by the caching allocator), error word cleared."""
+    ws = torch.empty(max(nbytes, WS_HEADER_BYTES), dtype=torch.uint8,
+                     device=device or torch.cuda.current_device())
+    assert ws.data_ptr() % 256 == 0
+    _ok(_lib.mla_clear_device_status(_ptr(ws), _stream(stream)), "mla_clear_device_status")
+    return ws
+
+
+# ------------------------------------------------------------------ sizes
+
+def append_kv_workspace_size(B, d_model):
+    return _size("mla_append_kv_workspace_size", B, d_model)
+
+
+def decode_workspace_size(B, H, max_seqlen, num_splits=0):
+    return _size("mla_decode_workspace_size", B, H, max_seqlen, num_splits)
+
+
+def absorb_q_workspace_size(B, d_model, q_lora, H):
+    return _size("mla_absorb_q_workspace_size", B, d_model, q_lora, H)
+
+
+def out_absorb_workspace_size(B, H, d_model):
+    return _size("mla_out_absorb_workspace_size", B, H, d_model)
+
+
+# ------------------------------------------------------------------ calls
+
+def append_kv(h, w_dkr, pos, block_table, kv_cache, rope_theta=10000.0, workspace=None,
+              stream=None):
+    B, dm = h.shape
+    nb = kv_cache.shape[0]
+    if workspace is None:
+        workspace = alloc_workspace(append_kv_workspace_size(B, dm), stream=stream)
+    rc = _lib.mla_append_kv(_ptr(_bits(h)), B, dm, _ptr(_bits(w_dkr)), _ptr(pos),
+                            _ptr(block_table), block_table.shape[1], _ptr(_bits(kv_cache)), nb,
+                            float(rope_theta), _ptr(workspace), workspace.numel(),
+                            _stream(stream))
+    _ok(rc, "mla_append_kv")
+    return workspace
+
+
+def decode_attention(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, scale,
+                     num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """Returns (out [B,H,512] bf16, lse [B,H] fp32, workspace)."""
+    B, H, _ = q_lat.shape
+    dev = q_lat.device
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(decode_workspace_size(B, H, max_seqlen, num_splits),
+                                    stream=stream)
+    rc = _lib.mla_decode_attention(_ptr(_bits(q_lat)), _ptr(_bits(q_rope)),
+                                   _ptr(_bits(kv_cache)), kv_cache.shape[0], _ptr(block_table),
+                                   block_table.shape[1], _ptr(seqlens), B, H, int(max_seqlen),
+                                   float(scale), int(num_splits), _ptr(workspace),
+                                   workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
+    _ok(rc, "mla_decode_attention")
+    return out, lse, workspace
+
+
+def decode_combine(o_part, lse_part, out=None, lse=None, stream=None):
+    B, S, H, _ = o_part.shape
+    dev = o_part.device
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    rc = _lib.mla_decode_combine(_ptr(o_part), _ptr(lse_part), B, S, H, _ptr(out), _ptr(lse),
+                                 _stream(stream))
+    _ok(rc, "mla_decode_combine")
+    return out, lse
+
+
+def absorb_q(h, w_dq, w_uq, w_qr, w_uk, pos, rope_theta=10000.0, q_lat=None, q_rope=None,
+             workspace=None, stream=None):
+    B, dm = h.shape
+    ql = w_dq.shape[0]
+    H = w_uk.shape[0]
+    dev = h.device
+    if q_lat is None:
+        q_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if q_rope is None:
+        q_rope = torch.empty((B, H, D_ROPE), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(absorb_q_workspace_size(B, dm, ql, H), stream=stream)
+    rc = _lib.mla_absorb_q(_ptr(_bits(h)), B, dm, _ptr(_bits(w_dq)), ql, _ptr(_bits(w_uq)),
+                           _ptr(_bits(w_qr)), _ptr(_bits(w_uk)), H, _ptr(pos), float(rope_theta),
+                           _ptr(workspace), workspace.numel(), _ptr(q_lat), _ptr(q_rope),
+                           _stream(stream))
+    _ok(rc, "mla_absorb_q")
+    return q_lat, q_rope, workspace
+
+
+def out_absorb(o_lat, w_uv, w_o, y=None, workspace=None, stream=None):
+    B, H, _ = o_lat.shape
+    dm = w_o.shape[0]
+    if y is None:
+        y = torch.empty((B, dm), dtype=torch.bfloat16, device=o_lat.device)
+    if workspace is None:
+        workspace = alloc_workspace(out_absorb_workspace_size(B, H, dm), stream=stream)
+    rc = _lib.mla_out_absorb(_ptr(_bits(o_lat)), B, H, _ptr(_bits(w_uv)), _ptr(_bits(w_o)), dm,
+                             _ptr(workspace), workspace.numel(), _ptr(y), _stream(stream))
+    _ok(rc, "mla_out_absorb")
+    return y, workspace
+
+
+def check_device_status(workspace, stream=None) -> int:
+    """Synchronise and return (and clear) the workspace's device error word."""
+    return int(_lib.mla_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def clear_device_status(workspace, stream=None):
+    _ok(_lib.mla_clear_device_status(_ptr(workspace), _stream(stream)), "mla_clear_device_status")
+
+
+class DecodeStep:
+    """The absorbed MLA decode step for one layer: append the new token's latent,
+    build the absorbed query, attend over the paged cache, project the latent
+    output back. Holds caller-owned workspaces; every step runs in libmla kernels."""
+
+    def __init__(self, weights: dict, B: int, H: int, max_seqlen: int, num_splits: int = 0,
+                 rope_theta: float = 10000.0, scale: float | None = None):
+        self.w = weights
+        self.B, self.H = B, H
+        self.dm = weights["w_dkr"].shape[1]
+        self.ql = weights["w_dq"].shape[0]
+        self.max_seqlen = max_seqlen
+        self.num_splits = num_splits
+        self.theta = rope_theta
+        self.scale = (1.0 / (D_NOPE + D_ROPE) ** 0.5) if scale is None else scale
+        dev = weights["w_dkr"].device
+        self.ws_append = alloc_workspace(append_kv_workspace_size(B, self.dm))
+        self.ws_q = alloc_workspace(absorb_q_workspace_size(B, self.dm, self.ql, H))
+        self.ws_att = alloc_workspace(decode_workspace_size(B, H, max_seqlen, num_splits))
+        self.ws_out = alloc_workspace(out_absorb_workspace_size(B, H, self.dm))
+        self.q_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+        self.q_rope = torch.empty((B, H, D_ROPE), dtype=torch.bfloat16, device=dev)
+        self.o_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        self.y = torch.empty((B, self.dm), dtype=torch.bfloat16, device=dev)
+
+    def __call__(self, h, pos, seqlens_after, block_table, kv_cache, stream=None):
+        w = self.w
+        append_kv(h, w["w_dkr"], pos, block_table, kv_cache, self.theta, self.ws_append, stream)
+        absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, self.theta, self.q_lat,
+                 self.q_rope, self.ws_q, stream)
+        decode_attention(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
+                         self.max_seqlen, self.scale, self.num_splits, self.o_lat, self.lse,
+                         self.ws_att, stream)
+        out_absorb(self.o_lat, w["w_uv"], w["w_o"], self.y, self.ws_out, stream)
+        return self.y
+
+    def check(self, stream=None) -> int:
+        codes = [check_device_status(ws, stream) for ws in
+                 (self.ws_append, self.ws_q, self.ws_att, self.ws_out)]
+        return next((c for c in codes if c), 0)

@@ -1,0 +1,70 @@
+"""The C-ABI library loads and exports every symbol include/mla.h declares, and
+host-side validation rejects bad arguments before anything is launched. CPU only:
+no call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_latent_kv_13_gb300 import build
+    build.build()
+    return ctypes.CDLL(build.LIB)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["mla_append_kv", "mla_decode_attention", "mla_decode_combine", "mla_absorb_q",
+              "mla_out_absorb", "mla_decode_workspace_size", "mla_check_device_status",
+              "mla_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_binding_declares_every_symbol(lib):
+    from mla_latent_kv_13_gb300 import mla
+    assert sorted(mla.EXPORTED) == _declared()
+
+
+def test_status_strings(lib):
+    lib.mla_status_string.restype = ctypes.c_char_p
+    assert lib.mla_status_string(0) == b"MLA_OK"
+    assert lib.mla_status_string(4) == b"MLA_ERR_OUT_OF_RANGE"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    lib.mla_decode_attention.restype = ctypes.c_int
+    null = vp(0)
+    # null pointers
+    rc = lib.mla_decode_attention(null, null, null, 1, null, 1, null, 1, 128, 64,
+                                  ctypes.c_float(0.07), 0, null, ctypes.c_size_t(0), null, null,
+                                  null)
+    assert rc == 1
+    # workspace sizes and unsupported head counts (pure host arithmetic)
+    sz = ctypes.c_size_t(0)
+    assert lib.mla_decode_workspace_size(16, 128, 4096, 0, ctypes.byref(sz)) == 0
+    assert sz.value >= 256
+    assert lib.mla_decode_workspace_size(16, 48, 4096, 0, ctypes.byref(sz)) == 2
+    assert lib.mla_decode_workspace_size(16, 128, 4096, 4, ctypes.byref(sz)) == 0
+    assert sz.value >= 256 + 16 * 4 * 128 * 512 * 4
+    assert lib.mla_append_kv_workspace_size(128, 7168, ctypes.byref(sz)) == 0
+    assert lib.mla_append_kv_workspace_size(128, 7000, ctypes.byref(sz)) == 1
+    assert lib.mla_absorb_q_workspace_size(128, 7168, 1536, 128, ctypes.byref(sz)) == 0
+    assert lib.mla_out_absorb_workspace_size(128, 128, 7168, ctypes.byref(sz)) == 0

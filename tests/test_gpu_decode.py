@@ -1,0 +1,185 @@
+"""GPU parity of mla_decode_attention (and its split-KV combine) against the fp64
+oracle, through the C ABI, on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_13_gb300 import synth
+from tests.helpers import (assert_close_rows, assert_lse, dev_bf16, dev_i32, host_bits,
+                           host_f64_from_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_13_gb300 import mla as m
+    return m
+
+
+def _to_dev(d):
+    return dict(q_lat=dev_bf16(d["q_lat"]), q_rope=dev_bf16(d["q_rope"]),
+                cache=dev_bf16(d["kv_cache"]), bt=dev_i32(d["block_table"]),
+                seqlens=dev_i32(d["seqlens"]))
+
+
+def _run(mla, d, num_splits=0, cache=None, bt=None):
+    t = _to_dev(d)
+    if cache is not None:
+        t["cache"] = cache
+    if bt is not None:
+        t["bt"] = dev_i32(bt)
+    max_len = int(np.max(d["seqlens"])) if len(d["seqlens"]) else 0
+    out, lse, ws = mla.decode_attention(t["q_lat"], t["q_rope"], t["cache"], t["bt"],
+                                        t["seqlens"], max_len, d["scale"], num_splits)
+    status = mla.check_device_status(ws)
+    return host_f64_from_bf16(out), lse.cpu().numpy().astype(np.float64), status
+
+
+def _oracle(d, rows=None, bt=None, cache=None):
+    """Oracle on all sequences, or only on the listed rows (b indices)."""
+    bt = d["block_table"] if bt is None else bt
+    cache = d["kv_cache"] if cache is None else cache
+    ql = synth.bf16_bits_to_f64(d["q_lat"])
+    qr = synth.bf16_bits_to_f64(d["q_rope"])
+    L = d["seqlens"]
+    if rows is not None:
+        ql, qr, bt, L = ql[rows], qr[rows], bt[rows], L[rows]
+    return oracle.decode_absorbed(ql, qr, cache, bt, L, d["scale"])
+
+
+def _case(B, H, seqlens, seed=0, shuffled=True):
+    w = synth.Workload("case", B, H, tuple(seqlens), None, shuffled)
+    return synth.make_attention_inputs(w, seed=seed)
+
+
+def test_tiny_workload_full_parity(mla):
+    d = synth.make_attention_inputs(synth.WORKLOADS["tiny"], seed=0)
+    out, lse, st = _run(mla, d)
+    assert st == 0
+    ref, lref = _oracle(d)
+    assert_close_rows(out, ref)
+    assert_lse(lse, lref)
+
+
+@pytest.mark.parametrize("H", [16, 32, 64, 128])
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+def test_ragged_lengths_and_splits(mla, H, splits):
+    d = _case(5, H, (100, 63, 65, 1, 300), seed=1)
+    out, lse, st = _run(mla, d, num_splits=splits)
+    assert st == 0
+    ref, lref = _oracle(d)
+    assert_close_rows(out, ref)
+    assert_lse(lse, lref)
+
+
+def test_empty_sequence_gives_zero_and_neg_inf(mla):
+    d = _case(3, 64, (0, 70, 0), seed=2)
+    for splits in (1, 3):
+        out, lse, st = _run(mla, d, num_splits=splits)
+        assert st == 0
+        assert np.all(out[0] == 0) and np.all(out[2] == 0)
+        assert np.all(np.isneginf(lse[0])) and np.all(np.isneginf(lse[2]))
+        ref, lref = _oracle(d)
+        assert_close_rows(out[1], ref[1])
+        assert_lse(lse, lref)
+
+
+def test_split_invariance(mla):
+    d = _case(2, 128, (1000, 777), seed=3)
+    outs = [_run(mla, d, num_splits=s)[:2] for s in (1, 2, 7, 0)]
+    for o, l in outs[1:]:
+        np.testing.assert_allclose(o, outs[0][0], rtol=1e-2, atol=2e-3)
+        np.testing.assert_allclose(l, outs[0][1], atol=1e-4)
+
+
+def test_poison_outside_sequences_is_never_read(mla):
+    d = _case(3, 128, (100, 64, 130), seed=4)
+    cache = d["kv_cache"].copy()
+    bt = d["block_table"]
+    nb = d["num_blocks"]
+    used = {}
+    for b, L in enumerate(d["seqlens"]):
+        for t in range((L + 63) // 64):
+            used.setdefault(int(bt[b, t]), 0)
+            used[int(bt[b, t])] = max(used[int(bt[b, t])], min(64, L - 64 * t))
+    for blk in range(nb):
+        n = used.get(blk, 0)
+        cache[blk, n:, :] = 0x7FC0 if blk % 2 else 0x7F80   # NaN / +inf
+    bt2 = bt.copy()
+    bt2[bt2 < 0] = 2 ** 30   # unused table entries: far out of range, must not be read
+    out, lse, st = _run(mla, d, cache=dev_bf16(cache), bt=bt2)
+    assert st == 0
+    ref, lref = _oracle(d)
+    assert_close_rows(out, ref)
+    assert_lse(lse, lref)
+
+
+def test_block_permutation_is_bit_identical(mla):
+    d = _case(2, 64, (200, 129), seed=5, shuffled=False)
+    out1, lse1, _ = _run(mla, d, num_splits=1)
+    nb = d["num_blocks"]
+    perm = np.random.default_rng(6).permutation(nb)
+    cache2 = np.empty_like(d["kv_cache"])
+    cache2[perm] = d["kv_cache"]
+    bt2 = np.where(d["block_table"] >= 0, perm[np.maximum(d["block_table"], 0)], -1)
+    out2, lse2, _ = _run(mla, d, num_splits=1, cache=dev_bf16(cache2), bt=bt2)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+def test_constant_rows_return_the_row(mla):
+    d = _case(2, 128, (333, 64), seed=7)
+    c = synth.f32_to_bf16_bits(np.random.default_rng(8).standard_normal(576).astype(np.float32))
+    cache = np.broadcast_to(c, d["kv_cache"].shape).copy()
+    out, lse, st = _run(mla, d, cache=dev_bf16(cache))
+    assert st == 0
+    want = synth.bf16_bits_to_f64(c[:512])
+    assert np.array_equal(out, np.broadcast_to(want, out.shape))
+
+
+def test_out_of_range_block_sets_error_word(mla):
+    d = _case(2, 64, (130, 64), seed=9)
+    bt = d["block_table"].copy()
+    bt[0, 1] = d["num_blocks"] + 1000
+    out, lse, st = _run(mla, d, bt=bt)
+    assert st == 4   # MLA_ERR_OUT_OF_RANGE
+    assert np.all(np.isfinite(out))
+    # the bad block is skipped: result equals the oracle that also skips it
+    ref, lref = oracle.decode_absorbed(synth.bf16_bits_to_f64(d["q_lat"]),
+                                       synth.bf16_bits_to_f64(d["q_rope"]), d["kv_cache"], bt,
+                                       d["seqlens"], d["scale"], allow_range=True)
+    assert_close_rows(out, ref)
+    # the word was cleared by the read
+    from mla_latent_kv_13_gb300 import mla as m
+    assert m.check_device_status(m.alloc_workspace(256)) == 0
+
+
+def test_combine_matches_oracle(mla):
+    rng = np.random.default_rng(10)
+    B, S, H = 3, 5, 16
+    o = rng.standard_normal((B, S, H, 512)).astype(np.float32)
+    l = (rng.standard_normal((B, S, H)) * 3).astype(np.float32)
+    l[0, 1:, :] = -np.inf
+    l[1, :, 3] = -np.inf
+    out, lse = mla.decode_combine(torch.from_numpy(o).cuda(), torch.from_numpy(l).cuda())
+    ref, lref = oracle.combine(o.astype(np.float64), l.astype(np.float64))
+    assert_close_rows(host_f64_from_bf16(out), ref, norm_rtol=1e-2)
+    assert_lse(lse.cpu().numpy(), lref, atol=1e-5)
+
+
+@pytest.mark.parametrize("name,rows", [("v3", [0, 9]), ("mixed", [3, 77]), ("long", [5])])
+def test_full_size_workloads_sampled(mla, name, rows):
+    """Full-size workloads in the library's own split choice; the oracle checks the
+    sampled sequences in full (every head, every latent column)."""
+    w = synth.WORKLOADS[name]
+    d = synth.make_attention_inputs(w, seed=0)
+    out, lse, st = _run(mla, d)
+    assert st == 0
+    ref, lref = _oracle(d, rows=rows)
+    assert_close_rows(out[rows], ref)
+    assert_lse(lse[rows], lref)
+    # property that holds at any size: every row is finite and lse >= max possible floor
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))

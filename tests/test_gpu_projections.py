@@ -1,0 +1,112 @@
+"""GPU parity of mla_append_kv, mla_absorb_q and mla_out_absorb against the fp64
+oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_13_gb300 import synth
+from tests.helpers import assert_close_rows, dev_bf16, dev_i32, host_bits, host_f64_from_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mla():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_13_gb300 import mla as m
+    return m
+
+
+def bf16(x):
+    return synth.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _append_both(mla, h, w, pos, bt, cache):
+    c_gpu = dev_bf16(cache)
+    ws = mla.append_kv(dev_bf16(h), dev_bf16(w), dev_i32(pos), dev_i32(bt), c_gpu)
+    st = mla.check_device_status(ws)
+    c_ref = cache.copy()
+    oracle.append_kv(h, w, pos, bt, c_ref, allow_range=True)
+    return host_bits(c_gpu), c_ref, st
+
+
+def test_append_exact_on_integer_inputs(mla):
+    rng = np.random.default_rng(0)
+    B, dm = 7, 128
+    h = bf16(rng.integers(-1, 2, (B, dm)))
+    w = bf16(rng.integers(-1, 2, (576, dm)))
+    bt = np.arange(B * 2, dtype=np.int32).reshape(B, 2)[:, ::-1].copy()
+    cache = bf16(rng.standard_normal((B * 2, 64, 576)))
+    got, ref, st = _append_both(mla, h, w, np.zeros(B, np.int32), bt, cache)
+    assert st == 0
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("B,dm", [(5, 256), (128, 7168)])
+def test_append_real_inputs_within_one_ulp(mla, B, dm):
+    rng = np.random.default_rng(1)
+    h = bf16(rng.standard_normal((B, dm)))
+    w = bf16(rng.standard_normal((576, dm)) * 0.02)
+    nb = 3 * B
+    bt = rng.permutation(nb).astype(np.int32).reshape(B, 3)
+    pos = rng.integers(0, 192, B).astype(np.int32)
+    cache = np.zeros((nb, 64, 576), np.uint16)
+    got, ref, st = _append_both(mla, h, w, pos, bt, cache)
+    assert st == 0
+    diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
+    # bf16 bit patterns of same-sign values differ by the number of ulps between them
+    assert diff.max() <= 1
+    assert (diff > 0).mean() < 0.01
+
+
+def test_append_out_of_range_is_flagged_and_dropped(mla):
+    rng = np.random.default_rng(2)
+    B, dm = 3, 64
+    h = bf16(rng.standard_normal((B, dm)))
+    w = bf16(rng.standard_normal((576, dm)))
+    bt = np.array([[0], [1], [99]], np.int32)      # sequence 2 points outside the pool
+    pos = np.array([3, 64, 0], np.int32)           # sequence 1 writes past its table
+    cache = np.zeros((3, 64, 576), np.uint16)
+    got, ref, st = _append_both(mla, h, w, pos, bt, cache)
+    assert st == 4
+    assert np.array_equal(got, ref)                # only sequence 0 was written
+
+
+def _proj(B, dm, ql, H, seed):
+    rng = np.random.default_rng(seed)
+    s = 0.02
+    return dict(h=bf16(rng.standard_normal((B, dm))),
+                w_dq=bf16(rng.standard_normal((ql, dm)) * s),
+                w_uq=bf16(rng.standard_normal((H * 128, ql)) * s),
+                w_qr=bf16(rng.standard_normal((H * 64, ql)) * s),
+                w_uk=bf16(rng.standard_normal((H, 128, 512)) * s),
+                w_uv=bf16(rng.standard_normal((H, 128, 512)) * s),
+                w_o=bf16(rng.standard_normal((dm, H * 128)) * s),
+                pos=rng.integers(0, 9000, B).astype(np.int32))
+
+
+@pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
+                                           (128, 7168, 1536, 128, [0, 61, 127])])
+def test_absorb_q(mla, B, dm, ql, H, rows):
+    p = _proj(B, dm, ql, H, 3)
+    q_lat, q_rope, ws = mla.absorb_q(dev_bf16(p["h"]), dev_bf16(p["w_dq"]), dev_bf16(p["w_uq"]),
+                                     dev_bf16(p["w_qr"]), dev_bf16(p["w_uk"]), dev_i32(p["pos"]))
+    assert mla.check_device_status(ws) == 0
+    rows = list(range(B)) if rows is None else rows
+    rl, rr = oracle.absorb_q(p["h"][rows], p["w_dq"], p["w_uq"], p["w_qr"], p["w_uk"],
+                             p["pos"][rows])
+    assert_close_rows(host_f64_from_bf16(q_lat)[rows], rl, "q_lat")
+    assert_close_rows(host_f64_from_bf16(q_rope)[rows], rr, "q_rope")
+
+
+@pytest.mark.parametrize("B,dm,H,rows", [(3, 256, 16, None), (128, 7168, 128, [1, 64, 100])])
+def test_out_absorb(mla, B, dm, H, rows):
+    p = _proj(B, dm, 64, H, 4)
+    o_lat = bf16(np.random.default_rng(5).standard_normal((B, H, 512)) * 0.05)
+    y, ws = mla.out_absorb(dev_bf16(o_lat), dev_bf16(p["w_uv"]), dev_bf16(p["w_o"]))
+    assert mla.check_device_status(ws) == 0
+    rows = list(range(B)) if rows is None else rows
+    ref = oracle.out_absorb(synth.bf16_bits_to_f64(o_lat)[rows], p["w_uv"], p["w_o"])
+    assert_close_rows(host_f64_from_bf16(y)[rows], ref, "y")
