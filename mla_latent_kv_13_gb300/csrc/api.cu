@@ -42,13 +42,17 @@ int plan_decode_splits(int B, int H, int max_seqlen, int requested) {
     int T = (max_seqlen + BLOCK - 1) / BLOCK;
     if (T < 1) T = 1;
     if (requested > 0) return requested;
-    int ctas = B * ((H + 63) / 64);
-    int sms = device_sm_count();
+    // one 2-CTA cluster per (sequence, range); a range's partial output costs about
+    // H * 512 * 4 * 2 bytes of extra traffic, i.e. H / 18 cache tiles of 64 tokens
+    const int slots = decode_tc_cluster_slots();
+    const double part_cost = (double)H * D_C * 4 * 2 / (BLOCK * D_QK * 2);
     int best = 1;
-    long best_cost = -1;
+    double best_cost = -1;
     for (int s = 1; s <= 64 && s <= T; ++s) {
-        long waves = (ctas * (long)s + sms - 1) / sms;
-        long cost = waves * ((T + s - 1) / s) * 16 + (s > 1 ? 1 : 0);
+        long items = (long)B * s;
+        long waves = (items + slots - 1) / slots;
+        double cost = (double)waves * ((T + s - 1) / s) +
+                      (s > 1 ? (double)items * part_cost / slots : 0.0);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = s;
@@ -180,7 +184,7 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
         p.lse_part = reinterpret_cast<float *>(
             w + align256((size_t)B * splits * H * D_C * sizeof(float)));
     }
-    cudaError_t e = launch_decode_mma(p, S(stream));
+    cudaError_t e = launch_decode_tc(p, S(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (splits > 1) e = launch_combine(p.o_part, p.lse_part, B, splits, H, out, lse, S(stream));
     return cuda_status(e);

@@ -24,7 +24,7 @@ constexpr int SEG_BYTES = 64 * 128;
 constexpr int Q_BYTES = SEG * SEG_BYTES;   // 72 KB
 constexpr int KV_BYTES = SEG * SEG_BYTES;  // 72 KB per stage
 constexpr int P_BYTES = SEG_BYTES;         // 64 heads x 64 tokens bf16
-constexpr int SMEM_BYTES = Q_BYTES + 2 * KV_BYTES + P_BYTES + 4 * 64 * 4 + 64 * 4;
+constexpr int SMEM_BYTES = Q_BYTES + 2 * KV_BYTES + P_BYTES + 6 * 64 * 4 + 64 * 4;
 
 __device__ __forceinline__ uint32_t seg_addr(uint32_t base, int row, int col_chunk) {
     // col_chunk counts 16-byte chunks across the 576-wide row (0..71)
@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
     uint8_t *sP = sKV + 2 * KV_BYTES;
     float *sRed = reinterpret_cast<float *>(sP + P_BYTES);  // [2][64] tile row max halves
     float *sL = sRed + 128;                                  // [2][64] row sums halves
-    float *sAlpha = sL + 128;                                // [64]
+    float *sLe = sL + 128;                                   // [2][64] exact sums halves
+    float *sAlpha = sLe + 128;                               // [64]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, b = blockIdx.y, h0 = blockIdx.z * HPC;
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
             for (int e = 0; e < 4; ++e) o[i][j][e] = 0.f;
 
     float m_run[2] = {-INFINITY, -INFINITY};  // rows g and g+8 of the S-role head tile
-    float l_run[2] = {0.f, 0.f};              // sums over this warp's token half
+    float l_run[2] = {0.f, 0.f};   // sums of the bf16-rounded p this warp feeds to P.V
+    float le_run[2] = {0.f, 0.f};  // sums of the unrounded p (for lse)
 
     for (int tile = t_begin; tile < t_end; ++tile) {
         const int stage = (tile - t_begin) & 1;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
             m_new[r] = fmaxf(m_run[r], mt);
             alpha[r] = (m_new[r] == -INFINITY) ? 1.f : fast_exp2(m_run[r] - m_new[r]);
         }
-        float rsum[2] = {0.f, 0.f};
+        float rsum[2] = {0.f, 0.f}, esum[2] = {0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -178,8 +180,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
                 float p0 = (m_new[r] == -INFINITY) ? 0.f : fast_exp2(s[j][2 * r] - m_new[r]);
                 float p1 = (m_new[r] == -INFINITY) ? 0.f : fast_exp2(s[j][2 * r + 1] - m_new[r]);
                 uint32_t pk = pack_bf16x2(p0, p1);
-                // sum the values the PV product will actually use (bf16-rounded)
+                // the output is normalised by the sum of the values the P.V product
+                // actually uses (bf16-rounded); lse uses the unrounded sum
                 rsum[r] += bf16_to_f32(pk & 0xffff) + bf16_to_f32(pk >> 16);
+                esum[r] += p0 + p1;
                 int row = hm * 16 + (lane >> 2) + r * 8;
                 int col = th * 32 + j * 8 + (lane & 3) * 2;  // token within tile
                 uint32_t addr = pBase + swz128(row, col >> 3) + (col & 7) * 2;
@@ -190,7 +194,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
         for (int r = 0; r < 2; ++r) {
             rsum[r] += __shfl_xor_sync(0xffffffffu, rsum[r], 1);
             rsum[r] += __shfl_xor_sync(0xffffffffu, rsum[r], 2);
+            esum[r] += __shfl_xor_sync(0xffffffffu, esum[r], 1);
+            esum[r] += __shfl_xor_sync(0xffffffffu, esum[r], 2);
             l_run[r] = l_run[r] * alpha[r] + rsum[r];
+            le_run[r] = le_run[r] * alpha[r] + esum[r];
             m_run[r] = m_new[r];
         }
         if (th == 0 && (lane & 3) == 0) {
@@ -240,6 +247,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
     if ((lane & 3) == 0) {
         sL[th * 64 + hm * 16 + (lane >> 2)] = l_run[0];
         sL[th * 64 + hm * 16 + (lane >> 2) + 8] = l_run[1];
+        sLe[th * 64 + hm * 16 + (lane >> 2)] = le_run[0];
+        sLe[th * 64 + hm * 16 + (lane >> 2) + 8] = le_run[1];
         if (th == 0) {
             sRed[hm * 16 + (lane >> 2)] = m_run[0];
             sRed[hm * 16 + (lane >> 2) + 8] = m_run[1];
@@ -270,7 +279,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_mma_kernel(DecodeParams p) {
             }
             if (lq == 0 && (lane & 3) == 0) {
                 float m2 = sRed[row];
-                float lse = l > 0.f ? (m2 + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                float le = sLe[row] + sLe[64 + row];
+                float lse = le > 0.f ? (m2 + log2f(le)) * 0.69314718055994531f : -INFINITY;
                 if (direct)
                     p.lse[(size_t)b * H + h] = lse;
                 else

@@ -1,0 +1,510 @@
+// decode_tc.cu -- absorbed MLA decode attention on the sm_100-family tensor cores
+// (tcgen05 + TMEM), fed by TMA, one 2-CTA thread-block cluster per work item.
+//
+// Work item = (sequence b, token range s). All heads of a sequence score the same
+// latent cache rows [c_kv (512) | k_rope (64)], so the 128 head rows form the M=128
+// side of both products and a 64-token cache tile the N (scores) or K (output) side:
+//   S   = Q [128 x 576] . K^T [576 x 64]      (scores)
+//   O  += P [128 x 64]  . V   [64 x 512]      (latent output, V = c_kv part)
+// The fp32 accumulator O [128 x 512] alone fills a whole SM's tensor memory, so the
+// two CTAs of a cluster split the latent columns: CTA r stages only its columns of
+// each tile -- r = 0: c_kv[0:256); r = 1: c_kv[256:512) and k_rope -- computes the
+// partial scores over them, swaps the 128 x 64 fp32 partial with its peer through
+// distributed shared memory (st.async), and both CTAs then run the same softmax on
+// the same full scores (bit-identical, since fp32 addition commutes) and accumulate
+// their own 256 output columns. No cache byte is read twice and no product is
+// computed twice; the only duplicated work is the (cheap) softmax.
+//
+// Roles per CTA (192 threads): warp 0 issues TMA loads (one elected lane); warp 1
+// allocates TMEM and issues tcgen05.mma / tcgen05.commit (one elected lane); warps
+// 2-5 (thread = head row = TMEM lane) exchange scores, run the online softmax in the
+// exp2 domain, write P to shared memory and finish the output. The running maximum
+// is only raised (and O rescaled in TMEM) when a score exceeds it by more than 2^8,
+// so after the first tile of a sequence O is almost never touched between MMAs.
+// Every mbarrier wait is bounded (about one second); a wait that gives up records
+// MLA_ERR_TIMEOUT in the error word and the CTA drains and exits.
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int TOK = 64;
+constexpr int NS = 2;                        // cache-tile stages
+constexpr int QCH = 128 * 128;               // one Q chunk: 128 rows x 64 bf16 (16 KB)
+constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
+constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
+constexpr int Q_OFF = 0;
+constexpr int KV_OFF = Q_OFF + MAXCH * QCH;  // 81920
+constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
+constexpr int P_OFF = KV_OFF + NS * KV_STAGE;
+constexpr int P_BYTES = 128 * 128;           // 128 rows x 64 bf16
+constexpr int RECV_STRIDE = 272;             // 64 fp32 + 16 B pad: conflict-free v4 rows
+constexpr int RECV_OFF = P_OFF + P_BYTES;
+constexpr int BAR_OFF = RECV_OFF + 128 * RECV_STRIDE;
+constexpr int NBAR = 16;
+constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+constexpr int SMEM_USED = MISC_OFF + 64;
+constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
+
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_O = 0;                 // O: columns [0, 256)
+constexpr uint32_t TM_S = 256;               // S: columns [256, 320)
+constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
+constexpr uint64_t DRAIN_NS = 200000000ull;
+constexpr float TAU = 8.0f;                  // lazy-rescale threshold (log2 units)
+
+constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
+
+static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+static_assert((BAR_OFF % 8) == 0, "mbarrier alignment");
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Wait that ignores the abort flag: used only to drain copies before exit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return;
+    uint64_t t0 = globaltimer_ns();
+    while (!mbar_test(bar, parity))
+        if (globaltimer_ns() - t0 > DRAIN_NS) return;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv,
+                     const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_qr, DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const int item = blockIdx.x >> 1;
+    const int b = item / p.num_splits, split = item % p.num_splits;
+    const int H = p.H;
+    const int nch = rank == 0 ? 4 : 5;  // chunks of Q / of each tile staged by this CTA
+
+    const uint32_t bar = sb + BAR_OFF;
+    const uint32_t q_full = bar;
+    const uint32_t s_full = bar + 8 * (1 + 2 * NS);
+    const uint32_t s_free = s_full + 8;
+    const uint32_t p_full = s_full + 16;
+    const uint32_t pv_done = s_full + 24;
+    const uint32_t recv_full = s_full + 32;
+    const uint32_t send_ok = s_full + 40;
+    const uint32_t mma_drain = s_full + 48;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
+    auto kv_full = [&](int s) { return bar + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bar + 8u * (1 + NS + s); };
+
+    int L = p.seqlens[b];
+    if (L < 0 || L > p.max_blocks * TOK) {
+        if (tid == 0 && rank == 0 && split == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
+        L = L < 0 ? 0 : p.max_blocks * TOK;
+    }
+    const int ntiles = (L + TOK - 1) / TOK;
+    const int t_begin = split * p.tiles_per_split;
+    const int t_end = min(ntiles, t_begin + p.tiles_per_split);
+    const int n = max(0, t_end - t_begin);
+    const int32_t *btab = p.block_table + (size_t)b * p.max_blocks;
+
+    if (tid == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(recv_full, 1);
+        mbar_init(send_ok, 4);
+        mbar_init(mma_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_kv);
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_qr);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before any remote operation
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n > 0) {
+            const int row0 = b * H;
+            mbar_arrive_expect_tx(q_full, nch * QCH);
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t dst = sb + Q_OFF + c * QCH;
+                if (c < 4)
+                    tma_load_2d(dst, &map_q, q_full, 256 * rank + 64 * c, row0);
+                else
+                    tma_load_2d(dst, &map_qr, q_full, 0, row0);
+            }
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % NS;
+                if (!mbar_wait(kv_empty(s), ((i / NS) & 1) ^ 1, abort_flag, WAIT_NS)) break;
+                const int blk = btab[t_begin + i];
+                if (blk >= 0 && blk < p.num_blocks) {
+                    mbar_arrive_expect_tx(kv_full(s), nch * KVCH);
+                    for (int c = 0; c < nch; ++c)
+                        tma_load_2d(sb + KV_OFF + s * KV_STAGE + c * KVCH, &map_kv, kv_full(s),
+                                    64 * (4 * rank + c), blk * TOK);
+                } else {
+                    if (rank == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
+                    mbar_arrive(kv_full(s));  // no data: the consumers mask the tile
+                }
+                issued = i + 1;
+            }
+            // copies still in flight must land before this CTA may exit
+            for (int i = max(0, issued - NS); i < issued; ++i) drain_wait(kv_full(i % NS), (i / NS) & 1);
+            drain_wait(q_full, 0);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA
+        if (lane == 0 && n > 0) {
+            const uint32_t qa = sb + Q_OFF;
+            auto issue_s = [&](int i) {
+                const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
+                for (int c = 0; c < nch; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma(tmem + TM_S, sdesc_sw128(qa + c * QCH + kk * 32, 16, 1024),
+                               sdesc_sw128(kv + c * KVCH + kk * 32, 16, 1024), IDESC_S,
+                               (c | kk) != 0);
+                tc_commit(s_full);
+            };
+            bool ok = mbar_wait(q_full, 0, abort_flag, WAIT_NS) &&
+                      mbar_wait(kv_full(0), 0, abort_flag, WAIT_NS);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int i = 0; ok && i < n; ++i) {
+                if (i + 1 < n) {
+                    ok = mbar_wait(kv_full((i + 1) % NS), ((i + 1) / NS) & 1, abort_flag,
+                                   WAIT_NS) &&
+                         mbar_wait(s_free, i & 1, abort_flag, WAIT_NS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(i + 1);
+                }
+                if (!(ok = mbar_wait(p_full, i & 1, abort_flag, WAIT_NS))) break;
+                tc_fence_after();
+                const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma(tmem + TM_O, sdesc_sw128(sb + P_OFF + kk * 32, 16, 1024),
+                           sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV, (i > 0 || kk > 0));
+                tc_commit(kv_empty(i % NS));
+                tc_commit(pv_done);
+            }
+            // every MMA this thread issued has finished before TMEM is released
+            tc_commit(mma_drain);
+            drain_wait(mma_drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- softmax / exchange / output
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;  // head row == TMEM lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t recv_local = sb + RECV_OFF + row * RECV_STRIDE;
+        const uint32_t recv_remote = mapa(recv_local, peer);
+        const uint32_t recv_full_remote = mapa(recv_full, peer);
+        const uint32_t send_ok_remote = mapa(send_ok, peer);
+        const uint32_t prow = sb + P_OFF + (row >> 3) * 1024 + (row & 7) * 128;
+        float m = -INFINITY, l = 0.f, le = 0.f;
+        bool ok = true;
+        // waits are warp-uniform: a lane that gives up takes its whole warp with it
+        auto wait_w = [&](uint32_t bar_, uint32_t par) {
+            return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
+        };
+        auto wait_wc = [&](uint32_t bar_, uint32_t par) {
+            return __all_sync(0xffffffffu, mbar_wait<true>(bar_, par, abort_flag, WAIT_NS));
+        };
+        for (int i = 0; i < n; ++i) {
+            const int tile = t_begin + i;
+            if (!(ok = wait_w(s_full, i & 1))) break;
+            tc_fence_after();
+            uint32_t sa[32], sc[32];
+            tmem_ld32(tl + TM_S, sa);
+            tmem_ld32(tl + TM_S + 32, sc);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+
+            // swap partial scores with the peer CTA
+            if (i > 0 && !(ok = wait_w(send_ok, (i - 1) & 1))) break;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                st_async_v4(recv_remote + 16 * k, sa[4 * k], sa[4 * k + 1], sa[4 * k + 2],
+                            sa[4 * k + 3], recv_full_remote);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                st_async_v4(recv_remote + 128 + 16 * k, sc[4 * k], sc[4 * k + 1], sc[4 * k + 2],
+                            sc[4 * k + 3], recv_full_remote);
+            if (row == 0) mbar_arrive_expect_tx(recv_full, 128 * 64 * 4);
+            if (!(ok = wait_wc(recv_full, i & 1))) break;
+            float s[64];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                float4 v = ld_shared_v4f(recv_local + 16 * k);
+                const uint32_t *mine = k < 8 ? &sa[4 * k] : &sc[4 * (k - 8)];
+                s[4 * k + 0] = __uint_as_float(mine[0]) + v.x;
+                s[4 * k + 1] = __uint_as_float(mine[1]) + v.y;
+                s[4 * k + 2] = __uint_as_float(mine[2]) + v.z;
+                s[4 * k + 3] = __uint_as_float(mine[3]) + v.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(send_ok_remote);
+
+            // online softmax on this head row
+            const int blk = btab[tile];
+            const bool blk_ok = blk >= 0 && blk < p.num_blocks;
+            const int valid = blk_ok ? min(TOK, L - tile * TOK) : 0;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                s[j] = j < valid ? s[j] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[j]);
+            }
+            const bool raise = mx > m + TAU;
+            if (__any_sync(0xffffffffu, raise)) {
+                const float m_new = raise ? mx : m;
+                const float alpha = raise ? exp2f(m - m_new) : 1.f;
+                if (i > 0) {
+                    // O holds tiles < i: wait until P.V of tile i-1 has landed, then rescale
+                    if (!(ok = wait_w(pv_done, (i - 1) & 1))) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tl + TM_O + 32 * c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                        tmem_st32(tl + TM_O + 32 * c, r);
+                    }
+                    tmem_st_wait();
+                }
+                l *= alpha;
+                le *= alpha;
+                m = m_new;
+            }
+            // P (bf16) for the P.V product; sums of the rounded and of the exact values
+            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;
+            uint32_t pk[32];
+            float rs = 0.f, es = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = (m == -INFINITY) ? 0.f : exp2f(s[2 * j] - m);
+                const float p1 = (m == -INFINITY) ? 0.f : exp2f(s[2 * j + 1] - m);
+                pk[j] = pack_bf16x2(p0, p1);
+                rs += bf16_to_f32(pk[j] & 0xffffu) + bf16_to_f32(pk[j] >> 16);
+                es += p0 + p1;
+            }
+            l += rs;
+            le += es;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(prow + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1],
+                             pk[4 * c + 2], pk[4 * c + 3]);
+            // rows past the valid tokens (the whole tile if its block is bad) may hold
+            // stale or poisoned data: zero them in the four chunks P.V reads, since
+            // 0 * NaN would still poison the product
+            if (valid < TOK) {
+                const uint32_t st = sb + KV_OFF + (i % NS) * KV_STAGE;
+                const int nchunks = (TOK - valid) * 32;  // 16-byte chunks: rows x 4 x 8
+                for (int e = row; e < nchunks; e += 128) {
+                    const int r = valid + (e >> 5), c = (e >> 3) & 3, k = e & 7;
+                    st_shared_v4(st + c * KVCH + r * 128 + k * 16, 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+
+        // ------------------------------------------------------------- output
+        const bool direct = p.num_splits == 1;
+        const int col0 = 256 * rank;
+        if (n > 0 && ok && wait_w(pv_done, (n - 1) & 1)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tl + TM_O + 32 * c, r);
+                tmem_ld_wait();
+                if (row < H) {
+                    if (direct) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            p.out + ((size_t)b * H + row) * D_C + col0 + 32 * c);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * k + 0]) * inv,
+                                            __uint_as_float(r[8 * k + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv,
+                                            __uint_as_float(r[8 * k + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv,
+                                            __uint_as_float(r[8 * k + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv,
+                                            __uint_as_float(r[8 * k + 7]) * inv));
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            p.o_part + (((size_t)b * p.num_splits + split) * H + row) * D_C +
+                            col0 + 32 * c);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv,
+                                                 __uint_as_float(r[4 * k + 1]) * inv,
+                                                 __uint_as_float(r[4 * k + 2]) * inv,
+                                                 __uint_as_float(r[4 * k + 3]) * inv);
+                    }
+                }
+            }
+        } else if (row < H) {
+            // empty range (or aborted): zero output, lse = -inf
+            if (direct) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)b * H + row) * D_C + col0);
+                for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.o_part + (((size_t)b * p.num_splits + split) * H + row) * D_C + col0);
+                for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            le = 0.f;
+        }
+        if (rank == 0 && row < H) {
+            const float lse = le > 0.f ? (m + log2f(le)) * 0.69314718055994531f : -INFINITY;
+            if (direct)
+                p.lse[(size_t)b * H + row] = lse;
+            else
+                p.lse_part[((size_t)b * p.num_splits + split) * H + row] = lse;
+        }
+    }
+
+    if (tid == 0 && *abort_flag) flag_error(p.err, MLA_ERR_TIMEOUT, b);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no remote access into this CTA after this point
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] (row pitch = cols) as a 2-D tensor map with
+// 128-byte swizzled boxes of box_rows x 64 columns.
+bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                    uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int decode_tc_cluster_slots() {
+    static int slots = 0;
+    if (slots > 0) return slots;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_TOTAL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_TOTAL) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) == cudaSuccess && n > 0)
+        slots = n;
+    else
+        slots = device_sm_count() / 2;
+    return slots;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
+    CUtensorMap mkv, mq, mqr;
+    if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, TOK) ||
+        !encode_bf16_2d(&mq, p.q_lat, D_C, (uint64_t)p.B * p.H, 128) ||
+        !encode_bf16_2d(&mqr, p.q_rope, D_ROPE, (uint64_t)p.B * p.H, 128))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    dim3 grid(2 * p.B * p.num_splits);
+    decode_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mkv, mq, mqr, p);
+    return cudaGetLastError();
+}
+
+}  // namespace mla

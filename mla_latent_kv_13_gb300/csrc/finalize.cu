@@ -35,25 +35,36 @@ __global__ void __launch_bounds__(288) append_finalize_kernel(
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(x0, x1);
 }
 
-// Grid-stride over (b, h, pair): sum the partials of c_q W_QR^T, rotate, store bf16.
-__global__ void qrope_finalize_kernel(const float *part, int S, int B, int H, const int32_t *pos,
-                                      float theta, uint16_t *q_rope) {
-    const long n = (long)B * H * (D_ROPE / 2);
+// One CTA per sequence: the 32 rotation angles of its position are formed once
+// (in double, so large positions keep their fractional part), then every head's
+// 32 pairs of c_q W_QR^T are reduced over the k-splits, rotated and stored as bf16.
+__global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, int S, int B,
+                                                             int H, const int32_t *pos,
+                                                             float theta, uint16_t *q_rope) {
+    __shared__ float cs[D_ROPE / 2], sn[D_ROPE / 2];
+    const int b = blockIdx.x;
+    if (threadIdx.x < D_ROPE / 2) {
+        const int i = threadIdx.x;
+        double freq = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(D_ROPE));
+        double sv, cv;
+        sincos(static_cast<double>(pos[b]) * freq, &sv, &cv);
+        cs[i] = static_cast<float>(cv);
+        sn[i] = static_cast<float>(sv);
+    }
+    __syncthreads();
     const long row_len = (long)H * D_ROPE;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n;
-         i += (long)gridDim.x * blockDim.x) {
-        int pair = i % (D_ROPE / 2);
-        long bh = i / (D_ROPE / 2);
-        int b = bh / H;
-        long off = (long)b * row_len + (bh % H) * D_ROPE + 2 * pair;
+    for (int e = threadIdx.x; e < H * (D_ROPE / 2); e += blockDim.x) {
+        const int h = e / (D_ROPE / 2), pair = e % (D_ROPE / 2);
+        const long off = (long)b * row_len + (long)h * D_ROPE + 2 * pair;
         float x0 = 0.f, x1 = 0.f;
         for (int s = 0; s < S; ++s) {
             float2 v = *reinterpret_cast<const float2 *>(part + (long)s * B * row_len + off);
             x0 += v.x;
             x1 += v.y;
         }
-        rope_pair(x0, x1, pair, pos[b], theta);
-        *reinterpret_cast<uint32_t *>(q_rope + bh * D_ROPE + 2 * pair) = pack_bf16x2(x0, x1);
+        const float y0 = x0 * cs[pair] - x1 * sn[pair];
+        const float y1 = x0 * sn[pair] + x1 * cs[pair];
+        *reinterpret_cast<uint32_t *>(q_rope + off) = pack_bf16x2(y0, y1);
     }
 }
 
@@ -70,10 +81,7 @@ cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_
 
 cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const int32_t *pos,
                                   float theta, uint16_t *q_rope, cudaStream_t stream) {
-    long n = (long)B * H * (D_ROPE / 2);
-    long nb = (n + 255) / 256;
-    int blocks = (int)(nb < 4096 ? nb : 4096);
-    qrope_finalize_kernel<<<blocks, 256, 0, stream>>>(part, S, B, H, pos, theta, q_rope);
+    qrope_finalize_kernel<<<B, 256, 0, stream>>>(part, S, B, H, pos, theta, q_rope);
     return cudaGetLastError();
 }
 

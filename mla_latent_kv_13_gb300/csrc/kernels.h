@@ -49,6 +49,8 @@ struct DecodeParams {
 };
 
 cudaError_t launch_decode_mma(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
+int decode_tc_cluster_slots();
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                            uint16_t *out, float *lse, cudaStream_t stream);
 
