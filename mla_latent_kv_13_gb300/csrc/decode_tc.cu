@@ -34,27 +34,26 @@ namespace {
 using namespace sm100;
 
 constexpr int TOK = 64;
-constexpr int NS = 2;                        // cache-tile stages
-constexpr int QCH = 128 * 128;               // one Q chunk: 128 rows x 64 bf16 (16 KB)
+constexpr int NS = 4;                        // cache-tile stages
 constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
 constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
-constexpr int Q_OFF = 0;
-constexpr int KV_OFF = Q_OFF + MAXCH * QCH;  // 81920
+constexpr int KV_OFF = 0;
 constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
 constexpr int P_OFF = KV_OFF + NS * KV_STAGE;
 constexpr int P_BYTES = 128 * 128;           // 128 rows x 64 bf16
 constexpr int RECV_STRIDE = 272;             // 64 fp32 + 16 B pad: conflict-free v4 rows
 constexpr int RECV_OFF = P_OFF + P_BYTES;
 constexpr int BAR_OFF = RECV_OFF + 128 * RECV_STRIDE;
-constexpr int NBAR = 16;
+constexpr int NBAR = 24;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0;                 // O: columns [0, 256)
-constexpr uint32_t TM_S = 256;               // S: columns [256, 320)
+constexpr uint32_t TM_O = 0;                 // O: fp32 columns [0, 256)
+constexpr uint32_t TM_S = 256;               // S: fp32 columns [256, 320)
+constexpr uint32_t TM_Q = 320;               // Q: bf16 pairs, columns [320, 480)
 constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                  // lazy-rescale threshold (log2 units)
@@ -89,9 +88,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv,
-                     const __grid_constant__ CUtensorMap map_q,
-                     const __grid_constant__ CUtensorMap map_qr, DecodeParams p) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv, DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -103,21 +100,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int item = blockIdx.x >> 1;
     const int b = item / p.num_splits, split = item % p.num_splits;
     const int H = p.H;
-    const int nch = rank == 0 ? 4 : 5;  // chunks of Q / of each tile staged by this CTA
+    const int nch = rank == 0 ? 4 : 5;  // 64-column chunks of Q and of each tile owned here
 
     const uint32_t bar = sb + BAR_OFF;
-    const uint32_t q_full = bar;
-    const uint32_t s_full = bar + 8 * (1 + 2 * NS);
-    const uint32_t s_free = s_full + 8;
-    const uint32_t p_full = s_full + 16;
-    const uint32_t pv_done = s_full + 24;
-    const uint32_t recv_full = s_full + 32;
-    const uint32_t send_ok = s_full + 40;
-    const uint32_t mma_drain = s_full + 48;
+    auto kv_full = [&](int s) { return bar + 8u * s; };
+    auto kv_empty = [&](int s) { return bar + 8u * (NS + s); };
+    const uint32_t q_ready = bar + 8u * (2 * NS);
+    const uint32_t s_full = q_ready + 8;
+    const uint32_t s_free = q_ready + 16;
+    const uint32_t p_full = q_ready + 24;
+    const uint32_t pv_done = q_ready + 32;
+    const uint32_t recv_full = q_ready + 40;
+    const uint32_t send_ok = q_ready + 48;
+    const uint32_t mma_drain = q_ready + 56;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
-    auto kv_full = [&](int s) { return bar + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bar + 8u * (1 + NS + s); };
 
     int L = p.seqlens[b];
     if (L < 0 || L > p.max_blocks * TOK) {
@@ -131,11 +128,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int32_t *btab = p.block_table + (size_t)b * p.max_blocks;
 
     if (tid == 0) {
-        mbar_init(q_full, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
         }
+        mbar_init(q_ready, 4);
         mbar_init(s_full, 1);
         mbar_init(s_free, 4);
         mbar_init(p_full, 4);
@@ -146,11 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&map_kv);
-        tma_prefetch_map(&map_q);
-        tma_prefetch_map(&map_qr);
-    }
+    if (warp == 0 && lane == 0) tma_prefetch_map(&map_kv);
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
@@ -164,15 +157,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
-            const int row0 = b * H;
-            mbar_arrive_expect_tx(q_full, nch * QCH);
-            for (int c = 0; c < nch; ++c) {
-                const uint32_t dst = sb + Q_OFF + c * QCH;
-                if (c < 4)
-                    tma_load_2d(dst, &map_q, q_full, 256 * rank + 64 * c, row0);
-                else
-                    tma_load_2d(dst, &map_qr, q_full, 0, row0);
-            }
             int issued = 0;
             for (int i = 0; i < n; ++i) {
                 const int s = i % NS;
@@ -190,24 +174,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 issued = i + 1;
             }
             // copies still in flight must land before this CTA may exit
-            for (int i = max(0, issued - NS); i < issued; ++i) drain_wait(kv_full(i % NS), (i / NS) & 1);
-            drain_wait(q_full, 0);
+            for (int i = max(0, issued - NS); i < issued; ++i)
+                drain_wait(kv_full(i % NS), (i / NS) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA
         if (lane == 0 && n > 0) {
-            const uint32_t qa = sb + Q_OFF;
             auto issue_s = [&](int i) {
                 const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
                 for (int c = 0; c < nch; ++c)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem + TM_S, sdesc_sw128(qa + c * QCH + kk * 32, 16, 1024),
-                               sdesc_sw128(kv + c * KVCH + kk * 32, 16, 1024), IDESC_S,
-                               (c | kk) != 0);
+                        tc_mma_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * kk,
+                                  sdesc_sw128(kv + c * KVCH + kk * 32, 16, 1024), IDESC_S,
+                                  (c | kk) != 0);
                 tc_commit(s_full);
             };
-            bool ok = mbar_wait(q_full, 0, abort_flag, WAIT_NS) &&
+            bool ok = mbar_wait(q_ready, 0, abort_flag, WAIT_NS) &&
                       mbar_wait(kv_full(0), 0, abort_flag, WAIT_NS);
             if (ok) {
                 tc_fence_after();
@@ -256,44 +239,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         auto wait_wc = [&](uint32_t bar_, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait<true>(bar_, par, abort_flag, WAIT_NS));
         };
-        for (int i = 0; i < n; ++i) {
-            const int tile = t_begin + i;
-            if (!(ok = wait_w(s_full, i & 1))) break;
+
+        if (n > 0) {
+            // Q rows of this CTA's columns into TMEM (A operand of the score product):
+            // rank 0: q_lat[0:256); rank 1: q_lat[256:512) and q_rope. Rows >= H are 0.
+            const uint4 *qsrc =
+                reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + row) * D_C + 256 * rank);
+            const uint4 *rsrc =
+                reinterpret_cast<const uint4 *>(p.q_rope + ((size_t)b * H + row) * D_ROPE);
+            for (int c = 0; c < nch; ++c) {
+                uint32_t r[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (row < H) v = c < 4 ? qsrc[8 * c + k] : rsrc[k];
+                    r[4 * k] = v.x;
+                    r[4 * k + 1] = v.y;
+                    r[4 * k + 2] = v.z;
+                    r[4 * k + 3] = v.w;
+                }
+                tmem_st32(tl + TM_Q + 32 * c, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_ready);
+        }
+
+        // Own partial scores of the next tile: read from TMEM, release the S buffer,
+        // and send them to the peer (whose copy of the previous tile was consumed).
+        uint32_t own[64];
+        auto load_and_send = [&](int i) -> bool {
+            if (!wait_w(s_full, i & 1)) return false;
             tc_fence_after();
-            uint32_t sa[32], sc[32];
-            tmem_ld32(tl + TM_S, sa);
-            tmem_ld32(tl + TM_S + 32, sc);
+            tmem_ld32(tl + TM_S, *reinterpret_cast<uint32_t(*)[32]>(&own[0]));
+            tmem_ld32(tl + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&own[32]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
+            if (i > 0 && !wait_w(send_ok, (i - 1) & 1)) return false;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                st_async_v4(recv_remote + 16 * k, own[4 * k], own[4 * k + 1], own[4 * k + 2],
+                            own[4 * k + 3], recv_full_remote);
+            return true;
+        };
 
-            // swap partial scores with the peer CTA
-            if (i > 0 && !(ok = wait_w(send_ok, (i - 1) & 1))) break;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                st_async_v4(recv_remote + 16 * k, sa[4 * k], sa[4 * k + 1], sa[4 * k + 2],
-                            sa[4 * k + 3], recv_full_remote);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                st_async_v4(recv_remote + 128 + 16 * k, sc[4 * k], sc[4 * k + 1], sc[4 * k + 2],
-                            sc[4 * k + 3], recv_full_remote);
+        if (n > 0) ok = load_and_send(0);
+        for (int i = 0; ok && i < n; ++i) {
+            const int tile = t_begin + i;
+            // (a) the peer's partial of tile i -> full scores
             if (row == 0) mbar_arrive_expect_tx(recv_full, 128 * 64 * 4);
             if (!(ok = wait_wc(recv_full, i & 1))) break;
             float s[64];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 float4 v = ld_shared_v4f(recv_local + 16 * k);
-                const uint32_t *mine = k < 8 ? &sa[4 * k] : &sc[4 * (k - 8)];
-                s[4 * k + 0] = __uint_as_float(mine[0]) + v.x;
-                s[4 * k + 1] = __uint_as_float(mine[1]) + v.y;
-                s[4 * k + 2] = __uint_as_float(mine[2]) + v.z;
-                s[4 * k + 3] = __uint_as_float(mine[3]) + v.w;
+                s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
+                s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
+                s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
+                s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(send_ok_remote);
+            // (b) start the exchange of tile i+1 so that it overlaps this tile's softmax
+            if (i + 1 < n && !(ok = load_and_send(i + 1))) break;
 
-            // online softmax on this head row
+            // (c) online softmax of tile i on this head row
             const int blk = btab[tile];
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int valid = blk_ok ? min(TOK, L - tile * TOK) : 0;
@@ -306,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const bool raise = mx > m + TAU;
             if (__any_sync(0xffffffffu, raise)) {
                 const float m_new = raise ? mx : m;
-                const float alpha = raise ? exp2f(m - m_new) : 1.f;
+                const float alpha = raise ? fast_exp2(m - m_new) : 1.f;
                 if (i > 0) {
                     // O holds tiles < i: wait until P.V of tile i-1 has landed, then rescale
                     if (!(ok = wait_w(pv_done, (i - 1) & 1))) break;
@@ -328,19 +341,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 m = m_new;
             }
             // P (bf16) for the P.V product; sums of the rounded and of the exact values
-            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;
             uint32_t pk[32];
             float rs = 0.f, es = 0.f;
+            const bool live = m != -INFINITY;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = (m == -INFINITY) ? 0.f : exp2f(s[2 * j] - m);
-                const float p1 = (m == -INFINITY) ? 0.f : exp2f(s[2 * j + 1] - m);
+                const float p0 = live ? fast_exp2(s[2 * j] - m) : 0.f;
+                const float p1 = live ? fast_exp2(s[2 * j + 1] - m) : 0.f;
                 pk[j] = pack_bf16x2(p0, p1);
-                rs += bf16_to_f32(pk[j] & 0xffffu) + bf16_to_f32(pk[j] >> 16);
+                rs += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
                 es += p0 + p1;
             }
             l += rs;
             le += es;
+            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;  // P buffer free
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 st_shared_v4(prow + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1],
@@ -494,16 +508,14 @@ int decode_tc_cluster_slots() {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
-    CUtensorMap mkv, mq, mqr;
-    if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, TOK) ||
-        !encode_bf16_2d(&mq, p.q_lat, D_C, (uint64_t)p.B * p.H, 128) ||
-        !encode_bf16_2d(&mqr, p.q_rope, D_ROPE, (uint64_t)p.B * p.H, 128))
+    CUtensorMap mkv;
+    if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, TOK))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.B * p.num_splits);
-    decode_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mkv, mq, mqr, p);
+    decode_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mkv, p);
     return cudaGetLastError();
 }
 
