@@ -113,6 +113,7 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  * q_lat [B][H][512] bf16, q_rope [B][H][64] bf16 (already rotated),
  * seqlens [B] int32 (0 <= seqlens[b] <= 64 * max_blocks; checked on the device),
  * out [B][H][512] bf16, lse [B][H] fp32.
+ * scale must be finite and > 0 (1/sqrt(d_nope + d_rope) for DeepSeek-shaped heads).
  * H must be 16, 32, 64 or 128. num_splits: 0 = chosen by the library, else the
  * number of token ranges each sequence is cut into (1..256); the ranges are
  * merged exactly by their log-sum-exp (split-KV combine).

@@ -159,7 +159,7 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
         return MLA_ERR_INVALID_ARG;
     if (B < 1 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
         max_seqlen > max_blocks * BLOCK || num_splits < 0 || num_splits > 256 ||
-        !isfinite(scale))
+        !(scale > 0.f) || !isfinite(scale))
         return MLA_ERR_INVALID_ARG;
     if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||

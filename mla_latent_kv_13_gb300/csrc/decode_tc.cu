@@ -17,8 +17,10 @@
 //
 // Roles per CTA (192 threads): warp 0 issues TMA loads (one elected lane); warp 1
 // allocates TMEM and issues tcgen05.mma / tcgen05.commit (one elected lane); warps
-// 2-5 (thread = head row = TMEM lane) exchange scores, run the online softmax in the
-// exp2 domain, write P to shared memory and finish the output. The running maximum
+// 2-5 (thread = head row = TMEM lane) load Q into TMEM, exchange scores, run the
+// online softmax in the exp2 domain, write P (bf16) into TMEM and finish the output.
+// Both products read their A operand (Q, P) from TMEM and their B operand (the
+// cache tile, 128-byte swizzled as TMA wrote it) from shared memory. The running maximum
 // is only raised (and O rescaled in TMEM) when a score exceeds it by more than 2^8,
 // so after the first tile of a sequence O is almost never touched between MMAs.
 // Every mbarrier wait is bounded (about one second); a wait that gives up records
@@ -39,10 +41,8 @@ constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 b
 constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
 constexpr int KV_OFF = 0;
 constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
-constexpr int P_OFF = KV_OFF + NS * KV_STAGE;
-constexpr int P_BYTES = 128 * 128;           // 128 rows x 64 bf16
 constexpr int RECV_STRIDE = 272;             // 64 fp32 + 16 B pad: conflict-free v4 rows
-constexpr int RECV_OFF = P_OFF + P_BYTES;
+constexpr int RECV_OFF = KV_OFF + NS * KV_STAGE;
 constexpr int BAR_OFF = RECV_OFF + 128 * RECV_STRIDE;
 constexpr int NBAR = 24;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
@@ -54,6 +54,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                 // O: fp32 columns [0, 256)
 constexpr uint32_t TM_S = 256;               // S: fp32 columns [256, 320)
 constexpr uint32_t TM_Q = 320;               // Q: bf16 pairs, columns [320, 480)
+constexpr uint32_t TM_P = 480;               // P: bf16 pairs, columns [480, 512)
 constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                  // lazy-rescale threshold (log2 units)
@@ -190,28 +191,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                   (c | kk) != 0);
                 tc_commit(s_full);
             };
+            // Order: S(0), S(1), then per tile i: S(i+2) as soon as the softmax has read
+            // S(i+1) out of TMEM, then P.V(i) once P(i) is in TMEM. Scores thus run two
+            // tiles ahead of the output product and are ready when the softmax wants them.
             bool ok = mbar_wait(q_ready, 0, abort_flag, WAIT_NS) &&
                       mbar_wait(kv_full(0), 0, abort_flag, WAIT_NS);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
             }
+            if (ok && n > 1) {
+                ok = mbar_wait(kv_full(1), 0, abort_flag, WAIT_NS) &&
+                     mbar_wait(s_free, 0, abort_flag, WAIT_NS);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(1);
+                }
+            }
             for (int i = 0; ok && i < n; ++i) {
-                if (i + 1 < n) {
-                    ok = mbar_wait(kv_full((i + 1) % NS), ((i + 1) / NS) & 1, abort_flag,
+                if (i + 2 < n) {
+                    ok = mbar_wait(kv_full((i + 2) % NS), ((i + 2) / NS) & 1, abort_flag,
                                    WAIT_NS) &&
-                         mbar_wait(s_free, i & 1, abort_flag, WAIT_NS);
+                         mbar_wait(s_free, (i + 1) & 1, abort_flag, WAIT_NS);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(i + 1);
+                    issue_s(i + 2);
                 }
                 if (!(ok = mbar_wait(p_full, i & 1, abort_flag, WAIT_NS))) break;
                 tc_fence_after();
                 const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc_mma(tmem + TM_O, sdesc_sw128(sb + P_OFF + kk * 32, 16, 1024),
-                           sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV, (i > 0 || kk > 0));
+                    tc_mma_ts(tmem + TM_O, tmem + TM_P + 8 * kk,
+                              sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV,
+                              (i > 0 || kk > 0));
                 tc_commit(kv_empty(i % NS));
                 tc_commit(pv_done);
             }
@@ -229,8 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t recv_remote = mapa(recv_local, peer);
         const uint32_t recv_full_remote = mapa(recv_full, peer);
         const uint32_t send_ok_remote = mapa(send_ok, peer);
-        const uint32_t prow = sb + P_OFF + (row >> 3) * 1024 + (row & 7) * 128;
-        float m = -INFINITY, l = 0.f, le = 0.f;
+        float m = -INFINITY, l = 0.f;
         bool ok = true;
         // waits are warp-uniform: a lane that gives up takes its whole warp with it
         auto wait_w = [&](uint32_t bar_, uint32_t par) {
@@ -287,8 +299,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         };
 
         if (n > 0) ok = load_and_send(0);
+        int blk_next = n > 0 ? btab[t_begin] : 0;  // block ids are fetched one tile ahead
         for (int i = 0; ok && i < n; ++i) {
             const int tile = t_begin + i;
+            const int blk = blk_next;
+            if (i + 1 < n) blk_next = btab[tile + 1];
             // (a) the peer's partial of tile i -> full scores
             if (row == 0) mbar_arrive_expect_tx(recv_full, 128 * 64 * 4);
             if (!(ok = wait_wc(recv_full, i & 1))) break;
@@ -302,20 +317,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(send_ok_remote);
+            if (lane == 0) mbar_arrive_remote_relaxed(send_ok_remote);
             // (b) start the exchange of tile i+1 so that it overlaps this tile's softmax
             if (i + 1 < n && !(ok = load_and_send(i + 1))) break;
 
             // (c) online softmax of tile i on this head row
-            const int blk = btab[tile];
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int valid = blk_ok ? min(TOK, L - tile * TOK) : 0;
-            float mx = -INFINITY;
+            if (valid < TOK) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = j < valid ? s[j] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[j]);
+                for (int j = 0; j < 64; ++j)
+                    if (j >= valid) s[j] = -INFINITY;
             }
+            float mx = s[0];
+#pragma unroll
+            for (int j = 1; j < 64; ++j) mx = fmaxf(mx, s[j]);
+            mx *= p.scale_log2;  // scale > 0: the max of the scaled scores
             const bool raise = mx > m + TAU;
             if (__any_sync(0xffffffffu, raise)) {
                 const float m_new = raise ? mx : m;
@@ -337,28 +354,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     tmem_st_wait();
                 }
                 l *= alpha;
-                le *= alpha;
                 m = m_new;
             }
-            // P (bf16) for the P.V product; sums of the rounded and of the exact values
+            // P = exp2(scale * s - m) as bf16 pairs for the P.V product
             uint32_t pk[32];
-            float rs = 0.f, es = 0.f;
             const bool live = m != -INFINITY;
+            const float nm = live ? -m : 0.f;
+            float es = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = live ? fast_exp2(s[2 * j] - m) : 0.f;
-                const float p1 = live ? fast_exp2(s[2 * j + 1] - m) : 0.f;
+                const float p0 = fast_exp2(fmaf(s[2 * j], p.scale_log2, nm));
+                const float p1 = fast_exp2(fmaf(s[2 * j + 1], p.scale_log2, nm));
                 pk[j] = pack_bf16x2(p0, p1);
-                rs += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
                 es += p0 + p1;
             }
-            l += rs;
-            le += es;
-            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;  // P buffer free
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_shared_v4(prow + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1],
-                             pk[4 * c + 2], pk[4 * c + 3]);
+            l += live ? es : 0.f;
+            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;  // P columns free
+            tmem_st32(tl + TM_P, pk);
             // rows past the valid tokens (the whole tile if its block is bad) may hold
             // stale or poisoned data: zero them in the four chunks P.V reads, since
             // 0 * NaN would still poison the product
@@ -369,8 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const int r = valid + (e >> 5), c = (e >> 3) & 3, k = e & 7;
                     st_shared_v4(st + c * KVCH + r * 128 + k * 16, 0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
@@ -424,10 +438,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     p.o_part + (((size_t)b * p.num_splits + split) * H + row) * D_C + col0);
                 for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            le = 0.f;
+            l = 0.f;
         }
         if (rank == 0 && row < H) {
-            const float lse = le > 0.f ? (m + log2f(le)) * 0.69314718055994531f : -INFINITY;
+            const float lse = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
             if (direct)
                 p.lse[(size_t)b * H + row] = lse;
             else
