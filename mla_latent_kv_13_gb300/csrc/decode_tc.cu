@@ -15,10 +15,15 @@
 // their own 256 output columns. No cache byte is read twice and no product is
 // computed twice; the only duplicated work is the (cheap) softmax.
 //
-// Roles per CTA (192 threads): warp 0 issues TMA loads (one elected lane); warp 1
+// Roles per CTA (224 threads): warp 0 issues TMA loads (one elected lane); warp 1
 // allocates TMEM and issues tcgen05.mma / tcgen05.commit (one elected lane); warps
-// 2-5 (thread = head row = TMEM lane) load Q into TMEM, exchange scores, run the
-// online softmax in the exp2 domain, write P (bf16) into TMEM and finish the output.
+// 2-5 (thread = head row = TMEM lane) load Q into TMEM, combine the two partial
+// scores, run the online softmax in the exp2 domain, write P (bf16) into TMEM and
+// finish the output; they also stage this CTA's partial scores of the next tile in
+// shared memory, from where one thread of warp 6 bulk-copies them to the peer. The
+// exchange (64 fp32 per head row per tile) is bounded by distributed-shared-memory
+// bandwidth (~14 B/clk per SM measured), so it runs one tile ahead on the copy
+// engine, overlapping the softmax of the current tile.
 // Both products read their A operand (Q, P) from TMEM and their B operand (the
 // cache tile, 128-byte swizzled as TMA wrote it) from shared memory. The running maximum
 // is only raised (and O rescaled in TMEM) when a score exceeds it by more than 2^8,
@@ -36,20 +41,22 @@ namespace {
 using namespace sm100;
 
 constexpr int TOK = 64;
-constexpr int NS = 4;                        // cache-tile stages
+constexpr int NS = 3;                        // cache-tile stages
 constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
 constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
 constexpr int KV_OFF = 0;
 constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
-constexpr int RECV_STRIDE = 272;             // 64 fp32 + 16 B pad: conflict-free v4 rows
-constexpr int RECV_OFF = KV_OFF + NS * KV_STAGE;
-constexpr int BAR_OFF = RECV_OFF + 128 * RECV_STRIDE;
+constexpr int XROW = 256;                    // exchange row: 64 fp32, 16-byte chunks XOR-swizzled
+constexpr int XBUF = 128 * XROW;             // 32768
+constexpr int SEND_OFF = KV_OFF + NS * KV_STAGE;   // one send buffer
+constexpr int RECV_OFF = SEND_OFF + XBUF;          // two receive buffers
+constexpr int BAR_OFF = RECV_OFF + 2 * XBUF;
 constexpr int NBAR = 24;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;                // 7 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                 // O: fp32 columns [0, 256)
 constexpr uint32_t TM_S = 256;               // S: fp32 columns [256, 320)
@@ -63,6 +70,11 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+static_assert(SEND_OFF >= KV_OFF + NS * KV_STAGE && RECV_OFF >= SEND_OFF + XBUF &&
+                  BAR_OFF >= RECV_OFF + 2 * XBUF && MISC_OFF >= BAR_OFF + NBAR * 8,
+              "shared-memory regions must not overlap");
+static_assert(SEND_OFF % 1024 == 0 && RECV_OFF % 16 == 0 && XBUF % 16 == 0,
+              "bulk-copy and swizzle alignment");
 static_assert((BAR_OFF % 8) == 0, "mbarrier alignment");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -111,9 +123,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t s_free = q_ready + 16;
     const uint32_t p_full = q_ready + 24;
     const uint32_t pv_done = q_ready + 32;
-    const uint32_t recv_full = q_ready + 40;
-    const uint32_t send_ok = q_ready + 48;
-    const uint32_t mma_drain = q_ready + 56;
+    const uint32_t mma_drain = q_ready + 40;
+    const uint32_t send_ready = q_ready + 48;  // our partial of the next tile is staged
+    const uint32_t send_free = q_ready + 56;   // the send buffer may be rewritten
+    auto recv_full = [&](int k) { return q_ready + 64 + 8u * k; };  // peer's partial in slot k
+    auto send_ok = [&](int k) { return q_ready + 80 + 8u * k; };    // peer drained its slot k
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
@@ -138,9 +152,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mbar_init(s_free, 4);
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
-        mbar_init(recv_full, 1);
-        mbar_init(send_ok, 4);
         mbar_init(mma_drain, 1);
+        mbar_init(send_ready, 4);
+        mbar_init(send_free, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(recv_full(k), 1);
+            mbar_init(send_ok(k), 4);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -191,57 +209,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                   (c | kk) != 0);
                 tc_commit(s_full);
             };
-            // Order: S(0), S(1), then per tile i: S(i+2) as soon as the softmax has read
-            // S(i+1) out of TMEM, then P.V(i) once P(i) is in TMEM. Scores thus run two
-            // tiles ahead of the output product and are ready when the softmax wants them.
-            bool ok = mbar_wait(q_ready, 0, abort_flag, WAIT_NS) &&
-                      mbar_wait(kv_full(0), 0, abort_flag, WAIT_NS);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
-            if (ok && n > 1) {
-                ok = mbar_wait(kv_full(1), 0, abort_flag, WAIT_NS) &&
-                     mbar_wait(s_free, 0, abort_flag, WAIT_NS);
-                if (ok) {
+            // Scores of tile k need its cache tile (kv_full) and the S columns back from
+            // the softmax (s_free of tile k-1); the output product of tile i needs P(i)
+            // (p_full). Issue whichever is ready first, so that a tile still in flight
+            // from HBM never holds up the output product of an earlier tile.
+            bool ok = mbar_wait(q_ready, 0, abort_flag, WAIT_NS);
+            if (ok) tc_fence_after();
+            int s_next = 0, pv_next = 0;
+            uint64_t t_last = globaltimer_ns();
+            uint32_t spins = 0;
+            while (ok && pv_next < n) {
+                if (s_next < n && mbar_test(kv_full(s_next % NS), (s_next / NS) & 1) &&
+                    (s_next == 0 || mbar_test(s_free, (s_next - 1) & 1))) {
                     tc_fence_after();
-                    issue_s(1);
+                    issue_s(s_next);
+                    ++s_next;
+                    t_last = globaltimer_ns();
+                    continue;
                 }
-            }
-            for (int i = 0; ok && i < n; ++i) {
-                if (i + 2 < n) {
-                    ok = mbar_wait(kv_full((i + 2) % NS), ((i + 2) / NS) & 1, abort_flag,
-                                   WAIT_NS) &&
-                         mbar_wait(s_free, (i + 1) & 1, abort_flag, WAIT_NS);
-                    if (!ok) break;
+                if (pv_next < s_next && mbar_test(p_full, pv_next & 1)) {
                     tc_fence_after();
-                    issue_s(i + 2);
-                }
-                if (!(ok = mbar_wait(p_full, i & 1, abort_flag, WAIT_NS))) break;
-                tc_fence_after();
-                const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
+                    const int i = pv_next;
+                    const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ts(tmem + TM_O, tmem + TM_P + 8 * kk,
-                              sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV,
-                              (i > 0 || kk > 0));
-                tc_commit(kv_empty(i % NS));
-                tc_commit(pv_done);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_ts(tmem + TM_O, tmem + TM_P + 8 * kk,
+                                  sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV,
+                                  (i > 0 || kk > 0));
+                    tc_commit(kv_empty(i % NS));
+                    tc_commit(pv_done);
+                    ++pv_next;
+                    t_last = globaltimer_ns();
+                    continue;
+                }
+                if ((++spins & 63) == 0) {
+                    if (*abort_flag) ok = false;
+                    else if (globaltimer_ns() - t_last > WAIT_NS) {
+                        *abort_flag = 1;
+                        ok = false;
+                    }
+                }
             }
             // every MMA this thread issued has finished before TMEM is released
             tc_commit(mma_drain);
             drain_wait(mma_drain, 0);
         }
         __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------------ score exchange
+        // One thread ships each staged partial (H rows x 272 B) to the peer with a bulk
+        // copy; distributed shared memory moves ~14 B/clk per SM, and the copy engine
+        // keeps that transfer off every warp's instruction queue.
+        if (lane == 0) {
+            for (int k = 0; k < n; ++k) {
+                if (!mbar_wait(send_ready, k & 1, abort_flag, WAIT_NS)) break;
+                // the peer's slot k % 2 held tile k - 2: wait until it has been read
+                if (k >= 2 && !mbar_wait(send_ok(k & 1), ((k >> 1) - 1) & 1, abort_flag, WAIT_NS))
+                    break;
+                bulk_copy_to_peer(mapa(sb + RECV_OFF + (k & 1) * XBUF, peer), sb + SEND_OFF,
+                                  H * XROW, mapa(recv_full(k & 1), peer));
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(send_free);
+            }
+        }
+        __syncwarp();
     } else {
-        // ------------------------------------------- softmax / exchange / output
+        // ------------------------------------------------- softmax / output
         const int wq = warp & 3;
         const int row = wq * 32 + lane;  // head row == TMEM lane
+        const bool live_row = row < H;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t recv_local = sb + RECV_OFF + row * RECV_STRIDE;
-        const uint32_t recv_remote = mapa(recv_local, peer);
-        const uint32_t recv_full_remote = mapa(recv_full, peer);
-        const uint32_t send_ok_remote = mapa(send_ok, peer);
+        const uint32_t xrow = row * XROW;
+        const uint32_t send_ok_remote0 = mapa(send_ok(0), peer);
+        const uint32_t send_ok_remote1 = mapa(send_ok(1), peer);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // waits are warp-uniform: a lane that gives up takes its whole warp with it
@@ -264,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (row < H) v = c < 4 ? qsrc[8 * c + k] : rsrc[k];
+                    if (live_row) v = c < 4 ? qsrc[8 * c + k] : rsrc[k];
                     r[4 * k] = v.x;
                     r[4 * k + 1] = v.y;
                     r[4 * k + 2] = v.z;
@@ -278,11 +319,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(q_ready);
         }
 
-        // Own partial scores of the next tile: read from TMEM, release the S buffer,
-        // and send them to the peer (whose copy of the previous tile was consumed).
+        // Read this CTA's partial scores of tile k out of TMEM (releasing the S buffer)
+        // and stage them in send buffer k % 2 for the copy thread.
         uint32_t own[64];
-        auto load_and_send = [&](int i) -> bool {
-            if (!wait_w(s_full, i & 1)) return false;
+        auto stage_partial = [&](int k) -> bool {
+            if (!wait_w(s_full, k & 1)) return false;
             tc_fence_after();
             tmem_ld32(tl + TM_S, *reinterpret_cast<uint32_t(*)[32]>(&own[0]));
             tmem_ld32(tl + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&own[32]));
@@ -290,40 +331,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            if (i > 0 && !wait_w(send_ok, (i - 1) & 1)) return false;
+            if (k >= 1 && !wait_w(send_free, (k - 1) & 1)) return false;
+            const uint32_t dst = sb + SEND_OFF + xrow;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                st_async_v4(recv_remote + 16 * k, own[4 * k], own[4 * k + 1], own[4 * k + 2],
-                            own[4 * k + 3], recv_full_remote);
+            for (int c = 0; c < 16; ++c)
+                st_shared_v4(dst + ((c ^ (row & 7)) << 4), own[4 * c], own[4 * c + 1],
+                             own[4 * c + 2], own[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(send_ready);
             return true;
         };
 
-        if (n > 0) ok = load_and_send(0);
+        if (n > 0) ok = stage_partial(0);
         int blk_next = n > 0 ? btab[t_begin] : 0;  // block ids are fetched one tile ahead
         for (int i = 0; ok && i < n; ++i) {
             const int tile = t_begin + i;
             const int blk = blk_next;
             if (i + 1 < n) blk_next = btab[tile + 1];
-            // (a) the peer's partial of tile i -> full scores
-            if (row == 0) mbar_arrive_expect_tx(recv_full, 128 * 64 * 4);
-            if (!(ok = wait_wc(recv_full, i & 1))) break;
             float s[64];
 #pragma unroll
+            for (int j = 0; j < 64; ++j) s[j] = __uint_as_float(own[j]);
+            // stage the next tile's partial first, so its transfer overlaps this softmax
+            if (i + 1 < n && !(ok = stage_partial(i + 1))) break;
+            // the peer's partial of tile i -> full scores
+            const int slot = i & 1;
+            if (row == 0) mbar_arrive_expect_tx(recv_full(slot), H * XROW);
+            if (!(ok = wait_wc(recv_full(slot), (i >> 1) & 1))) break;
+            const uint32_t src = sb + RECV_OFF + slot * XBUF + xrow;
+#pragma unroll
             for (int k = 0; k < 16; ++k) {
-                float4 v = ld_shared_v4f(recv_local + 16 * k);
-                s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
-                s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
-                s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
-                s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
+                float4 v = ld_shared_v4f(src + ((k ^ (row & 7)) << 4));
+                s[4 * k + 0] += v.x;
+                s[4 * k + 1] += v.y;
+                s[4 * k + 2] += v.z;
+                s[4 * k + 3] += v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote_relaxed(send_ok_remote);
-            // (b) start the exchange of tile i+1 so that it overlaps this tile's softmax
-            if (i + 1 < n && !(ok = load_and_send(i + 1))) break;
+            if (lane == 0) mbar_arrive_remote_relaxed(slot ? send_ok_remote1 : send_ok_remote0);
 
-            // (c) online softmax of tile i on this head row
+            // online softmax of tile i on this head row
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
-            const int valid = blk_ok ? min(TOK, L - tile * TOK) : 0;
+            const int tvalid = blk_ok ? min(TOK, L - tile * TOK) : 0;  // valid tokens of the tile
+            const int valid = live_row ? tvalid : 0;                    // columns this row keeps
             if (valid < TOK) {
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
@@ -374,11 +424,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // rows past the valid tokens (the whole tile if its block is bad) may hold
             // stale or poisoned data: zero them in the four chunks P.V reads, since
             // 0 * NaN would still poison the product
-            if (valid < TOK) {
+            if (tvalid < TOK) {
                 const uint32_t st = sb + KV_OFF + (i % NS) * KV_STAGE;
-                const int nchunks = (TOK - valid) * 32;  // 16-byte chunks: rows x 4 x 8
+                const int nchunks = (TOK - tvalid) * 32;  // 16-byte chunks: rows x 4 x 8
                 for (int e = row; e < nchunks; e += 128) {
-                    const int r = valid + (e >> 5), c = (e >> 3) & 3, k = e & 7;
+                    const int r = tvalid + (e >> 5), c = (e >> 3) & 3, k = e & 7;
                     st_shared_v4(st + c * KVCH + r * 128 + k * 16, 0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
