@@ -175,19 +175,61 @@ def _host_cores():
         return os.cpu_count() or 1
 
 
+def _head_slice(d, hs):
+    """Weights of the first hs heads (the per-head slices of W_UQ, W_QR, W_UK, W_UV, W_O)."""
+    H, ql, dm = d["H"], d["q_lora"], d["d_model"]
+    return dict(
+        w_uq=np.ascontiguousarray(d["w_uq"].reshape(H, 128, ql)[:hs].reshape(-1, ql)),
+        w_qr=np.ascontiguousarray(d["w_qr"].reshape(H, 64, ql)[:hs].reshape(-1, ql)),
+        w_uk=np.ascontiguousarray(d["w_uk"][:hs]), w_uv=np.ascontiguousarray(d["w_uv"][:hs]),
+        w_o=np.ascontiguousarray(d["w_o"].reshape(dm, H, 128)[:, :hs].reshape(dm, -1)))
+
+
+def time_oracle_heads(d, ws, seq: int = 0) -> float:
+    """The oracle's full step for one sequence restricted to the heads in ws; seconds."""
+    import oracle
+    r = [seq]
+    cache = d["kv_cache"]
+    t0 = time.perf_counter()
+    oracle.append_kv(d["h"][r], d["w_dkr"], d["pos"][r], d["block_table"][r], cache)
+    q_lat, q_rope = oracle.absorb_q(d["h"][r], d["w_dq"], ws["w_uq"], ws["w_qr"], ws["w_uk"],
+                                    d["pos"][r], d["rope_theta"])
+    o_lat, _ = oracle.decode_absorbed(q_lat, q_rope, cache, d["block_table"][r],
+                                      d["seqlens_after"][r], d["scale"])
+    oracle.out_absorb(o_lat, ws["w_uv"], ws["w_o"])
+    return time.perf_counter() - t0
+
+
 def run_reference(args, d, costs, metric, unit):
+    """The fp64 oracle on the host cores. Each step is one sequence of the full step with a
+    head subset sized so that warm-up + all steps take about two minutes; its time is
+    scaled to the whole batch: 128 x (per-sequence part + 128 x per-head part), with the
+    two parts calibrated from a 1-head and an all-head run of one sequence."""
     world, rank, _ = _dist_init()
     if rank != 0:
         return
-    n_seq = args.ref_sample
-    B = d["B"]
+    B, H = d["B"], d["H"]
+    full = _head_slice(d, H)
+    one = _head_slice(d, 1)
+    t_all = min(time_oracle_heads(d, full) for _ in range(2))
+    t_one = min(time_oracle_heads(d, one) for _ in range(2))
+    t_head = max((t_all - t_one) / (H - 1), 1e-9)
+    t_seq = max(t_one - t_head, 0.0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    hs = H
+    while hs > 1 and t_seq + hs * t_head > budget:
+        hs //= 2
+    ws = _head_slice(d, hs)
     for _ in range(args.warmup):
-        time_oracle(d, 1)
-    ts = [time_oracle(d, n_seq) for _ in range(args.steps)]
-    t_step = statistics.median(ts) * B / n_seq
+        time_oracle_heads(d, ws)
+    ts = [time_oracle_heads(d, ws) for _ in range(args.steps)]
+    t_sample = statistics.median(ts)
+    # measured sample (1 sequence, hs heads) -> whole step
+    t_step = B * (t_sample + (H - hs) * t_head)
     value = costs["bytes"] / t_step / 1e9
-    sample = f"{n_seq} of {B} sequences of the full step (all 128 heads, 8192 tokens), " \
-             f"scaled linearly to the batch"
+    sample = (f"1 of {B} sequences x {hs} of {H} heads per step (full 8192-token attention, "
+              f"its projections); scaled to the batch with per-sequence {t_seq*1e3:.1f} ms and "
+              f"per-head {t_head*1e3:.2f} ms parts calibrated on the same host")
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -338,6 +380,76 @@ def run_gpu(args, d, costs, metric, unit):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_attention(args, w, metric, unit):
+    """Decode attention alone on one of the attention workloads (profiling / per-config lines)."""
+    import torch
+    world, rank, local = _dist_init()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_kv_13_gb300 import mla, synth
+    d = synth.make_attention_inputs(w, seed=0)
+
+    def dbf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    ql, qr, cache = dbf(d["q_lat"]), dbf(d["q_rope"]), dbf(d["kv_cache"])
+    bt = torch.from_numpy(d["block_table"]).to(dev)
+    L = torch.from_numpy(d["seqlens"]).to(dev)
+    B, H = d["B"], d["H"]
+    max_len = int(d["seqlens"].max())
+    ws = mla.alloc_workspace(mla.decode_workspace_size(B, H, max_len, args.num_splits))
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        mla.decode_attention(ql, qr, cache, bt, L, max_len, d["scale"], args.num_splits, out, lse,
+                             ws)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize(dev)
+    # inputs below L2 size are rotated through distinct cache copies (cold L2 per step)
+    nbytes = d["kv_cache"].nbytes
+    copies = [cache]
+    if nbytes * 2 < 256 << 20:
+        copies += [cache.clone() for _ in range(max(1, (256 << 20) // nbytes))]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        c = copies[i % len(copies)]
+        mla.decode_attention(ql, qr, c, bt, L, max_len, d["scale"], args.num_splits, out, lse,
+                             ws)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if mla.check_device_status(ws) != 0:
+        raise RuntimeError("device error in the timed region")
+    t_ms = _max_over_ranks(start.elapsed_time(end), world, dev)
+    if rank != 0:
+        return
+    peaks = _measured_peaks()
+    byts = synth.algorithmic_attention_bytes(d["seqlens"], H)
+    flops = synth.attention_flops(d["seqlens"], H)
+    ms = t_ms / args.steps
+    gbs = byts / (ms * 1e-3) / 1e9
+    roof_s = max(byts / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    line = {"metric": metric, "value": gbs * world, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(w.describe(), l2=("rotating %d cache copies" % len(copies))
+                           if len(copies) > 1 else "inputs larger than L2"),
+            "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": B / (ms * 1e-3),
+            "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": roof_s / (ms * 1e-3), "traffic": None,
+                         "peak_source": peaks["source"] + " (burst copy)"},
+            "gpu_launches": args.steps * (1 if ws.numel() <= 256 else 2)}
+    print(json.dumps(line), flush=True)
+
+
 def step_launches(step) -> int:
     """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1 (+1 combine), out 3."""
     from mla_latent_kv_13_gb300 import mla
@@ -359,12 +471,15 @@ def _kernel_hash() -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["step", "tiny", "v3", "mixed", "long"],
+                    help="step = the full decode step (default); the others time decode "
+                         "attention alone on that attention workload")
     ap.add_argument("--cpu-sample", type=int, default=32)
-    ap.add_argument("--ref-sample", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -373,11 +488,16 @@ def main():
     import sys
     sys.path.insert(0, HERE)
     from mla_latent_kv_13_gb300 import synth
+    metric = "MLA decode attn: latent-KV GB/s, TFLOP/s and % roofline on 1 GB300"
+    if args.workload != "step":
+        if args.impl == "reference":
+            raise SystemExit("--impl reference is defined on the full-step workload")
+        run_gpu_attention(args, synth.WORKLOADS[args.workload], metric, "GB/s")
+        return
     w = synth.WORKLOADS[WORKLOAD]
     d = synth.make_step_inputs(w, seed=0)
     d["_cfg"] = dict(w.describe(), seqlen=int(d["seqlens_after"].max()), prefilled=int(d["pos"][0]))
     costs = step_costs(d)
-    metric = "MLA decode attn: latent-KV GB/s, TFLOP/s and % roofline on 1 GB300"
     if args.impl == "reference":
         run_reference(args, d, costs, metric, "GB/s")
     else:

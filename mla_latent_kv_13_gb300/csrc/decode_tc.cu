@@ -65,6 +65,7 @@ constexpr uint32_t TM_P = 480;               // P: bf16 pairs, columns [480, 512
 constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                  // lazy-rescale threshold (log2 units)
+constexpr int PF_DIST = 4;                   // tiles prefetched into L2 beyond the stage ring
 
 constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
@@ -176,6 +177,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
+            // Tiles beyond the shared-memory ring are prefetched into L2, so that a load
+            // issued when a stage frees up is served from L2 rather than from HBM.
+            auto prefetch = [&](int t) {
+                if (t >= n) return;
+                const int blk = btab[t_begin + t];
+                if (blk < 0 || blk >= p.num_blocks) return;
+                for (int c = 0; c < nch; ++c)
+                    tma_prefetch_l2_2d(&map_kv, 64 * (4 * rank + c), blk * TOK);
+            };
+            for (int t = NS; t < NS + PF_DIST; ++t) prefetch(t);
             int issued = 0;
             for (int i = 0; i < n; ++i) {
                 const int s = i % NS;
@@ -191,6 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     mbar_arrive(kv_full(s));  // no data: the consumers mask the tile
                 }
                 issued = i + 1;
+                if (i >= NS) prefetch(i + PF_DIST);
             }
             // copies still in flight must land before this CTA may exit
             for (int i = max(0, issued - NS); i < issued; ++i)
