@@ -458,11 +458,16 @@ def step_launches(step) -> int:
     return 2 + 6 + decode + 3
 
 
+DECODE_SOURCES = ("decode_tc.cu", "sm100.cuh", "common.cuh")
+
+
 def _kernel_hash() -> str:
+    """Hash of the decode kernel's sources: recorded DRAM traffic is only reported while
+    the kernel it was measured on is unchanged."""
     import hashlib
     hsh = hashlib.sha256()
     csrc = os.path.join(HERE, "mla_latent_kv_13_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in DECODE_SOURCES:
         with open(os.path.join(csrc, n), "rb") as f:
             hsh.update(f.read())
     return hsh.hexdigest()[:16]
