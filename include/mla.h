@@ -141,6 +141,34 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
 mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                                 mla_bf16_t *out, float *lse, mla_stream_t stream);
 
+/*
+ * mla_decode_attention without a workspace: the same computation and outputs, for
+ * callers that cannot obtain device memory for scratch -- code running while a
+ * stream is captured into a CUDA graph, plugins whose host framework owns all device
+ * allocations, serving loops that must not call cudaMalloc/cudaFree on their hot
+ * path. (The pages describe no such entry point; it is a property of this library.)
+ *
+ * The split-KV scratch (partial outputs, their log-sum-exps, the error word) lives in
+ * one array of MLA_NOALLOC_SCRATCH_BYTES that is part of the library image: every GPU
+ * that loads the library holds it until the process exits. Requests whose scratch
+ * (the figure mla_decode_workspace_size reports for the same B, H, max_seqlen and
+ * num_splits) exceeds that size are rejected with MLA_ERR_WORKSPACE before anything
+ * is launched; num_splits = 1 needs no partials and always fits.
+ * The first call on a device looks up the array's device address (no allocation) and
+ * should happen before any stream capture. All calls share the array and it keeps the
+ * last call's contents, so calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller. Device-detected range errors
+ * skip the offending tokens as in mla_decode_attention but are not reported (there is
+ * no workspace to read them from). Allocates nothing.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+mla_status_t mla_decode_attention_noalloc(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                          const mla_bf16_t *kv_cache, int num_blocks,
+                                          const int32_t *block_table, int max_blocks,
+                                          const int32_t *seqlens, int B, int H, int max_seqlen,
+                                          float scale, int num_splits, mla_bf16_t *out,
+                                          float *lse, mla_stream_t stream);
+
 /* ------------------------------------------------- absorbed projections */
 
 /*

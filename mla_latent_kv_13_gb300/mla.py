@@ -50,6 +50,8 @@ _SIGS = {
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "mla_decode_attention_noalloc": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
+                                      _vp, _vp], _i),
     "mla_absorb_q_workspace_size": ([_i, _i, _i, _i, _szp], _i),
     "mla_absorb_q": ([_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _f, _vp, _sz, _vp, _vp,
                       _vp], _i),
@@ -165,6 +167,26 @@ def decode_attention(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, 
                                    workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
     _ok(rc, "mla_decode_attention")
     return out, lse, workspace
+
+
+def decode_attention_noalloc(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, scale,
+                             num_splits=0, out=None, lse=None, stream=None):
+    """mla_decode_attention_noalloc: same results, scratch in the library's own device
+    array (no workspace). Returns (out, lse)."""
+    B, H, _ = q_lat.shape
+    dev = q_lat.device
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    rc = _lib.mla_decode_attention_noalloc(_ptr(_bits(q_lat)), _ptr(_bits(q_rope)),
+                                           _ptr(_bits(kv_cache)), kv_cache.shape[0],
+                                           _ptr(block_table), block_table.shape[1],
+                                           _ptr(seqlens), B, H, int(max_seqlen), float(scale),
+                                           int(num_splits), _ptr(out), _ptr(lse),
+                                           _stream(stream))
+    _ok(rc, "mla_decode_attention_noalloc")
+    return out, lse
 
 
 def decode_combine(o_part, lse_part, out=None, lse=None, stream=None):
