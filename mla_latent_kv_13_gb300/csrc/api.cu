@@ -24,16 +24,24 @@ mla_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA
 
 bool heads_ok(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
 
-// K cut into ranges (multiples of 64) so that n-tiles x m-tiles x splits covers
-// about two waves of the SMs.
-void plan_ksplit(int M, int N, int K, int &splits, int &per) {
-    int tiles = ((N + 63) / 64) * ((M + 63) / 64);
-    int target = 2 * device_sm_count();
-    int kblocks = K / 64;
-    int s = (target + tiles - 1) / tiles;
-    if (s < 1) s = 1;
-    if (s > kblocks) s = kblocks;
-    per = ((kblocks + s - 1) / s) * 64;
+// K cut into ranges (multiples of 64) for the tensor-core GEMM (128 x 128 output tiles,
+// one CTA per SM): minimise waves x (k-blocks per range + a fixed per-CTA cost of about
+// three k-blocks for filling and draining its pipeline).
+void plan_ksplit(int M, int N, int K, int batch, int &splits, int &per) {
+    const long tiles = (long)((N + 127) / 128) * ((M + 127) / 128) * batch;
+    const int slots = device_sm_count();
+    const int kblocks = K / 64;
+    int best = 1;
+    long best_cost = -1;
+    for (int s = 1; s <= kblocks; ++s) {
+        const long waves = (tiles * s + slots - 1) / slots;
+        const long cost = waves * ((kblocks + s - 1) / s + 3);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    per = ((kblocks + best - 1) / best) * 64;
     splits = (K + per - 1) / per;
 }
 
@@ -100,7 +108,7 @@ const char *mla_status_string(mla_status_t s) {
 mla_status_t mla_append_kv_workspace_size(int B, int d_model, size_t *bytes) {
     if (!bytes || B < 1 || B > 4096 || d_model < 64 || d_model % 64) return MLA_ERR_INVALID_ARG;
     int splits, per;
-    plan_ksplit(B, D_QK, d_model, splits, per);
+    plan_ksplit(B, D_QK, d_model, 1, splits, per);
     *bytes = HDR + align256((size_t)splits * B * D_QK * sizeof(float));
     return MLA_OK;
 }
@@ -122,7 +130,7 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
     if (ws_bytes < need) return MLA_ERR_WORKSPACE;
 
     int splits, per;
-    plan_ksplit(B, D_QK, d_model, splits, per);
+    plan_ksplit(B, D_QK, d_model, 1, splits, per);
     float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + HDR);
     GemmParams g{};
     g.A = h; g.lda = d_model; g.a_bstride = 0;
@@ -130,7 +138,7 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
     g.M = B; g.N = D_QK; g.K = d_model; g.batch = 1;
     g.k_splits = splits; g.k_per_split = per;
     g.c_part = part;
-    cudaError_t e = launch_gemm(g, false, S(stream));
+    cudaError_t e = launch_gemm_tc(g, false, S(stream), err_word(workspace));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_append_finalize(part, splits, B, pos, block_table, max_blocks, kv_cache, num_blocks,
                                rope_theta, err_word(workspace), S(stream));
@@ -203,13 +211,15 @@ mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int 
 namespace {
 struct AbsorbQLayout {
     int s1, per1;     // split of c_q = h W_DQ^T
+    int s2, per2;     // split of c_q W_QR^T (q_rope before rotation)
     size_t part, cq, qn, total;
 };
 AbsorbQLayout absorb_q_layout(int B, int d_model, int q_lora, int H) {
     AbsorbQLayout L{};
-    plan_ksplit(B, q_lora, d_model, L.s1, L.per1);
+    plan_ksplit(B, q_lora, d_model, 1, L.s1, L.per1);
+    plan_ksplit(B, H * D_ROPE, q_lora, 1, L.s2, L.per2);
     size_t part1 = (size_t)L.s1 * B * q_lora * sizeof(float);
-    size_t part2 = (size_t)B * H * D_ROPE * sizeof(float);
+    size_t part2 = (size_t)L.s2 * B * H * D_ROPE * sizeof(float);
     L.part = HDR;
     L.cq = L.part + align256(part1 > part2 ? part1 : part2);
     L.qn = L.cq + align256((size_t)B * q_lora * 2);
@@ -250,12 +260,14 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     uint16_t *qn = reinterpret_cast<uint16_t *>(w + L.qn);
     cudaStream_t st = S(stream);
 
+    uint32_t *err = err_word(workspace);
+
     // c_q = h W_DQ^T (bf16 intermediate)
     GemmParams g{};
     g.A = h; g.lda = d_model; g.B = w_dq; g.ldb = d_model;
     g.M = B; g.N = q_lora; g.K = d_model; g.batch = 1;
     g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
-    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
     if (launch_reduce_bf16(part, L.s1, 1, B, q_lora, cq, q_lora, 0, st) != cudaSuccess)
         return MLA_ERR_CUDA;
 
@@ -264,15 +276,15 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
     g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
     g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
-    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
 
     // q_rope = RoPE(c_q W_QR^T)
     g = GemmParams{};
     g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
     g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
-    g.k_splits = 1; g.k_per_split = q_lora; g.c_part = part;
-    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
-    if (launch_qrope_finalize(part, 1, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
+    g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
+    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_qrope_finalize(part, L.s2, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
         return MLA_ERR_CUDA;
 
     // q_lat[b, i] = q_nope[b, i] W_UK_i  (per-head product, W_UK_i stored [128][512])
@@ -282,7 +294,7 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     g.M = B; g.N = D_C; g.K = D_NOPE; g.batch = H;
     g.k_splits = 1; g.k_per_split = D_NOPE;
     g.c_bf16 = q_lat; g.ldc = (long)H * D_C; g.c_bstride = D_C;
-    return cuda_status(launch_gemm(g, true, st));
+    return cuda_status(launch_gemm_tc(g, true, st, err));
 }
 
 // ---------------------------------------------------------- out_absorb
@@ -294,7 +306,7 @@ struct OutLayout {
 };
 OutLayout out_layout(int B, int H, int d_model) {
     OutLayout L{};
-    plan_ksplit(B, d_model, H * D_V, L.s2, L.per2);
+    plan_ksplit(B, d_model, H * D_V, 1, L.s2, L.per2);
     L.ov = HDR;
     L.part = L.ov + align256((size_t)B * H * D_V * 2);
     L.total = L.part + align256((size_t)L.s2 * B * d_model * sizeof(float));
@@ -325,6 +337,8 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     float *part = reinterpret_cast<float *>(w + L.part);
     cudaStream_t st = S(stream);
 
+    uint32_t *err = err_word(workspace);
+
     // o_v[b, i] = W_UV_i o_lat[b, i]   (per head: A = o_lat [B][512], B = W_UV_i [128][512])
     GemmParams g{};
     g.A = o_lat; g.lda = (long)H * D_C; g.a_bstride = D_C;
@@ -332,14 +346,14 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     g.M = B; g.N = D_V; g.K = D_C; g.batch = H;
     g.k_splits = 1; g.k_per_split = D_C;
     g.c_bf16 = ov; g.ldc = (long)H * D_V; g.c_bstride = D_V;
-    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
 
     // y = o_v W_O^T
     g = GemmParams{};
     g.A = ov; g.lda = (long)H * D_V; g.B = w_o; g.ldb = (long)H * D_V;
     g.M = B; g.N = d_model; g.K = H * D_V; g.batch = 1;
     g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
-    if (launch_gemm(g, false, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_status(launch_reduce_bf16(part, L.s2, 1, B, d_model, y, d_model, 0, st));
 }
 

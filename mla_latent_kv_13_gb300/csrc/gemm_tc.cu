@@ -1,0 +1,281 @@
+// gemm_tc.cu -- bf16 GEMM for the absorbed projections on the sm_100-family tensor
+// cores: TMA-fed, tcgen05.mma into TMEM, one 128 x 128 output tile per CTA.
+//
+// C[m][n] = sum_k A[m][k] * B(k, n), fp32 accumulation, where the batch rows (the
+// decode batch, M <= 128 per tile) are A and the weights are B:
+//   "TN": B stored [N][K] (row n is output feature n: the [out, in] layout), or
+//   "NN": B stored [K][N] (W_UK, whose rows are per-head key dims).
+// Operands are addressed through 2-D tensor maps; a batch index (one per head for the
+// per-head products) shifts the A columns and the B rows by fixed amounts, so one map
+// serves every head. K is cut into k_splits ranges whose fp32 partials a finalize
+// kernel reduces: these products are weight-bandwidth bound (M = batch is small), and
+// the split keeps every SM streaming weights even when there are few output tiles.
+//
+// Roles (192 threads): warp 0 issues TMA (one lane), warp 1 owns TMEM and issues the
+// MMAs (one lane), warps 2-5 read the accumulator out of TMEM and store it. Waits are
+// bounded (one second); a wait that gives up records MLA_ERR_TIMEOUT.
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int NS = 6;                       // smem stages
+constexpr int TILE_A = BM * BK * 2;         // 16 KB
+constexpr int TILE_B = BN * BK * 2;         // 16 KB
+constexpr int STAGE = TILE_A + TILE_B;
+constexpr int BAR_OFF = NS * STAGE;
+constexpr int SMEM_TOTAL = BAR_OFF + 256 + 1024;
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint64_t WAIT_NS = 1000000000ull;
+
+constexpr uint32_t IDESC_TN = idesc_bf16(BM, BN, false, false);
+constexpr uint32_t IDESC_NN = idesc_bf16(BM, BN, false, true);
+
+static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+
+struct TcGemmArgs {
+    int M, N, K, batch, k_splits, k_per_split;
+    int a_bx;   // A column offset per batch
+    int b_bx;   // B (TN) column offset per batch
+    int b_by;   // B row offset per batch (TN: rows of N; NN: rows of K)
+    float *c_part;
+    uint16_t *c_bf16;
+    long ldc, c_bstride;
+    uint32_t *err;
+};
+
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = globaltimer_ns();
+    while (!mbar_test(bar, parity))
+        if (globaltimer_ns() - t0 > 200000000ull) return;
+}
+
+template <bool NN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, TcGemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sb - raw);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+    const int batch = blockIdx.z / g.k_splits, split = blockIdx.z % g.k_splits;
+    const int k_begin = split * g.k_per_split;
+    const int k_end = min(g.K, k_begin + g.k_per_split);
+    const int nkb = (k_end - k_begin + BK - 1) / BK;
+
+    const uint32_t bar = sb + BAR_OFF;
+    auto full = [&](int s) { return bar + 8u * s; };
+    auto empty = [&](int s) { return bar + 8u * (NS + s); };
+    const uint32_t done = bar + 8u * (2 * NS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + BAR_OFF + 8 * (2 * NS + 1));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + BAR_OFF + 8 * (2 * NS + 2));
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % NS;
+                if (!mbar_wait(empty(s), ((kb / NS) & 1) ^ 1, abort_flag, WAIT_NS)) break;
+                const int k = k_begin + kb * BK;
+                const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
+                mbar_arrive_expect_tx(full(s), STAGE);
+                tma_load_2d(sa, &map_a, full(s), batch * g.a_bx + k, m0);
+                if (!NN) {
+                    tma_load_2d(sbb, &map_b, full(s), batch * g.b_bx + k, batch * g.b_by + n0);
+                } else {
+                    tma_load_2d(sbb, &map_b, full(s), n0, batch * g.b_by + k);
+                    tma_load_2d(sbb + TILE_B / 2, &map_b, full(s), n0 + 64, batch * g.b_by + k);
+                }
+                issued = kb + 1;
+            }
+            for (int kb = max(0, issued - NS); kb < issued; ++kb) drain(full(kb % NS), (kb / NS) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % NS;
+                if (!(ok = mbar_wait(full(s), (kb / NS) & 1, abort_flag, WAIT_NS))) break;
+                tc_fence_after();
+                const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                    const uint64_t bd = NN ? sdesc_sw128(sbb + kk * 2048, TILE_B / 2, 1024)
+                                           : sdesc_sw128(sbb + kk * 32, 16, 1024);
+                    tc_mma(tmem, ad, bd, NN ? IDESC_NN : IDESC_TN, (kb | kk) != 0);
+                }
+                tc_commit(empty(s));
+            }
+            tc_commit(done);  // arrives once every MMA above has finished
+            drain(done, 0);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: thread = output row m0 + (warp % 4) * 32 + lane
+        const int wq = warp & 3;
+        const int m = m0 + wq * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const bool ok =
+            __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tl + 32 * c, r);
+                tmem_ld_wait();
+                const int nb = n0 + 32 * c;
+                if (m < g.M && nb < g.N) {
+                    if (g.c_part) {
+                        float *dst = g.c_part + (((size_t)split * g.batch + batch) * g.M + m) *
+                                                    (size_t)g.N + nb;
+                        if (nb + 32 <= g.N) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                reinterpret_cast<float4 *>(dst)[k] =
+                                    make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                __uint_as_float(r[4 * k + 2]),
+                                                __uint_as_float(r[4 * k + 3]));
+                        } else {
+                            for (int j = 0; j < g.N - nb; ++j) dst[j] = __uint_as_float(r[j]);
+                        }
+                    } else {
+                        uint16_t *dst = g.c_bf16 + batch * g.c_bstride + (size_t)m * g.ldc + nb;
+                        if (nb + 32 <= g.N) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                reinterpret_cast<uint4 *>(dst)[k] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(r[8 * k]), __uint_as_float(r[8 * k + 1])),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 2]), __uint_as_float(r[8 * k + 3])),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 4]), __uint_as_float(r[8 * k + 5])),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 6]), __uint_as_float(r[8 * k + 7])));
+                        } else {
+                            for (int j = 0; j < g.N - nb; ++j) dst[j] = f32_to_bf16(__uint_as_float(r[j]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (tid == 0 && *abort_flag) flag_error(g.err, MLA_ERR_TIMEOUT, blockIdx.x);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// bf16 matrix with `rows` rows of `cols` elements, row pitch `ld` elements, as a 2-D map
+// with 128-byte swizzled boxes of box_rows x 64 columns.
+bool map_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+            uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column
+// offset batch * a_bx; B is [rows_b][ldb] with every batch's slice at row offset
+// batch * b_by (TN: [N][K] slice; NN: [K][N] slice).
+cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, uint32_t *err) {
+    TcGemmArgs g{};
+    g.M = p.M; g.N = p.N; g.K = p.K; g.batch = p.batch;
+    g.k_splits = p.k_splits; g.k_per_split = p.k_per_split;
+    g.c_part = p.c_part; g.c_bf16 = p.c_bf16; g.ldc = p.ldc; g.c_bstride = p.c_bstride;
+    g.err = err;
+    // A: rows = M, columns = lda (the batch slices side by side)
+    g.a_bx = static_cast<int>(p.a_bstride);
+    CUtensorMap ma, mb;
+    if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM))
+        return cudaErrorInvalidValue;
+    if (!nn) {
+        // B slices are [N][K] blocks stacked by rows (b_bstride = rows * ldb elements)
+        g.b_bx = 0;
+        g.b_by = static_cast<int>(p.b_bstride / p.ldb);
+        const uint64_t rows = (uint64_t)p.N + (uint64_t)g.b_by * (p.batch - 1);
+        if (!map_2d(&mb, p.B, (uint64_t)p.ldb, rows, (uint64_t)p.ldb, BN))
+            return cudaErrorInvalidValue;
+    } else {
+        g.b_bx = 0;
+        g.b_by = static_cast<int>(p.b_bstride / p.ldb);
+        const uint64_t rows = (uint64_t)p.K + (uint64_t)g.b_by * (p.batch - 1);
+        if (!map_2d(&mb, p.B, (uint64_t)p.ldb, rows, (uint64_t)p.ldb, BK))
+            return cudaErrorInvalidValue;
+    }
+    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM, p.batch * p.k_splits);
+    if (nn) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+        if (e != cudaSuccess) return e;
+        gemm_tc_kernel<true><<<grid, NTHREADS, SMEM_TOTAL, stream>>>(ma, mb, g);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+        if (e != cudaSuccess) return e;
+        gemm_tc_kernel<false><<<grid, NTHREADS, SMEM_TOTAL, stream>>>(ma, mb, g);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mla

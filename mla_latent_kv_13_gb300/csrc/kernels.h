@@ -19,6 +19,8 @@ struct GemmParams {
 };
 
 cudaError_t launch_gemm(const GemmParams &p, bool nn, cudaStream_t stream);
+// tcgen05/TMA version (one 128 x 128 tile per CTA, 1 CTA per SM); err = workspace error word
+cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, uint32_t *err);
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
                                long ldc, long c_bstride, cudaStream_t stream);
 
