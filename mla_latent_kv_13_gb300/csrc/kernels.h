@@ -18,8 +18,7 @@ struct GemmParams {
     long ldc, c_bstride;
 };
 
-cudaError_t launch_gemm(const GemmParams &p, bool nn, cudaStream_t stream);
-// tcgen05/TMA version (one 128 x 128 tile per CTA, 1 CTA per SM); err = workspace error word
+// tcgen05/TMA GEMM (one 128 x 128 tile per CTA, 1 CTA per SM); err = workspace error word
 cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, uint32_t *err);
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
                                long ldc, long c_bstride, cudaStream_t stream);
@@ -50,7 +49,6 @@ struct DecodeParams {
     uint32_t *err;
 };
 
-cudaError_t launch_decode_mma(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
 int decode_tc_cluster_slots();
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
