@@ -50,16 +50,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// RoPE rotation of one pair (x0, x1) for pair index i of a 64-wide vector at
-// position pos. The angle is formed in double so that large positions keep
-// their fractional part; the rotation itself is done in fp32.
-__device__ __forceinline__ void rope_pair(float &x0, float &x1, int i, int pos, float theta) {
-    double freq = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(D_ROPE));
-    double s, c;
-    sincos(static_cast<double>(pos) * freq, &s, &c);
-    float cf = static_cast<float>(c), sf = static_cast<float>(s);
-    float y0 = x0 * cf - x1 * sf;
-    float y1 = x0 * sf + x1 * cf;
+// RoPE rotation frequencies theta^(-2i/64), i = 0..31, computed on the host in double
+// and passed by value (a pow per element on the device costs far more than the
+// rotation itself: fp64 throughput on this part is small).
+struct RopeFreqs {
+    double f[D_ROPE / 2];
+};
+
+// cos / sin of pos * freq. The product is formed in double and reduced to [-pi, pi]
+// with a double fma (both exact enough for positions in the millions); the reduced
+// angle is then evaluated in fp32.
+__device__ __forceinline__ void rope_cos_sin(int pos, double freq, float &c, float &s) {
+    const double a = static_cast<double>(pos) * freq;
+    const double two_pi = 6.283185307179586476925286766559;
+    const double k = rint(a * (1.0 / two_pi));
+    const float r = static_cast<float>(fma(-k, two_pi, a));
+    sincosf(r, &s, &c);
+}
+
+// Rotate the pair (x0, x1) by the angle pos * freq.
+__device__ __forceinline__ void rope_pair(float &x0, float &x1, int pos, double freq) {
+    float c, s;
+    rope_cos_sin(pos, freq, c, s);
+    const float y0 = x0 * c - x1 * s;
+    const float y1 = x0 * s + x1 * c;
     x0 = y0;
     x1 = y1;
 }

@@ -40,8 +40,16 @@ namespace {
 
 using namespace sm100;
 
+#ifndef MLA_DECODE_STAGES
+#define MLA_DECODE_STAGES 4
+#endif
+#ifndef MLA_DECODE_RECV_SLOTS
+#define MLA_DECODE_RECV_SLOTS 1
+#endif
+
 constexpr int TOK = 64;
-constexpr int NS = 3;                        // cache-tile stages
+constexpr int NS = MLA_DECODE_STAGES;        // cache-tile stages
+constexpr int RS = MLA_DECODE_RECV_SLOTS;    // receive slots for the peer's partial scores
 constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
 constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
 constexpr int KV_OFF = 0;
@@ -49,8 +57,8 @@ constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
 constexpr int XROW = 256;                    // exchange row: 64 fp32, 16-byte chunks XOR-swizzled
 constexpr int XBUF = 128 * XROW;             // 32768
 constexpr int SEND_OFF = KV_OFF + NS * KV_STAGE;   // one send buffer
-constexpr int RECV_OFF = SEND_OFF + XBUF;          // two receive buffers
-constexpr int BAR_OFF = RECV_OFF + 2 * XBUF;
+constexpr int RECV_OFF = SEND_OFF + XBUF;          // RS receive buffers
+constexpr int BAR_OFF = RECV_OFF + RS * XBUF;
 constexpr int NBAR = 24;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
@@ -72,7 +80,7 @@ constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(SEND_OFF >= KV_OFF + NS * KV_STAGE && RECV_OFF >= SEND_OFF + XBUF &&
-                  BAR_OFF >= RECV_OFF + 2 * XBUF && MISC_OFF >= BAR_OFF + NBAR * 8,
+                  BAR_OFF >= RECV_OFF + RS * XBUF && MISC_OFF >= BAR_OFF + NBAR * 8,
               "shared-memory regions must not overlap");
 static_assert(SEND_OFF % 1024 == 0 && RECV_OFF % 16 == 0 && XBUF % 16 == 0,
               "bulk-copy and swizzle alignment");
@@ -156,7 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mbar_init(mma_drain, 1);
         mbar_init(send_ready, 4);
         mbar_init(send_free, 1);
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < RS; ++k) {
             mbar_init(recv_full(k), 1);
             mbar_init(send_ok(k), 4);
         }
@@ -275,11 +283,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             for (int k = 0; k < n; ++k) {
                 if (!mbar_wait(send_ready, k & 1, abort_flag, WAIT_NS)) break;
-                // the peer's slot k % 2 held tile k - 2: wait until it has been read
-                if (k >= 2 && !mbar_wait(send_ok(k & 1), ((k >> 1) - 1) & 1, abort_flag, WAIT_NS))
+                // the peer's slot k % RS held tile k - RS: wait until it has been read
+                if (k >= RS &&
+                    !mbar_wait(send_ok(k % RS), ((k / RS) - 1) & 1, abort_flag, WAIT_NS))
                     break;
-                bulk_copy_to_peer(mapa(sb + RECV_OFF + (k & 1) * XBUF, peer), sb + SEND_OFF,
-                                  H * XROW, mapa(recv_full(k & 1), peer));
+                bulk_copy_to_peer(mapa(sb + RECV_OFF + (k % RS) * XBUF, peer), sb + SEND_OFF,
+                                  H * XROW, mapa(recv_full(k % RS), peer));
                 bulk_commit();
                 bulk_wait_read_all();
                 mbar_arrive(send_free);
@@ -294,7 +303,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t xrow = row * XROW;
         const uint32_t send_ok_remote0 = mapa(send_ok(0), peer);
-        const uint32_t send_ok_remote1 = mapa(send_ok(1), peer);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // waits are warp-uniform: a lane that gives up takes its whole warp with it
@@ -367,9 +375,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // stage the next tile's partial first, so its transfer overlaps this softmax
             if (i + 1 < n && !(ok = stage_partial(i + 1))) break;
             // the peer's partial of tile i -> full scores
-            const int slot = i & 1;
+            const int slot = i % RS;
             if (row == 0) mbar_arrive_expect_tx(recv_full(slot), H * XROW);
-            if (!(ok = wait_wc(recv_full(slot), (i >> 1) & 1))) break;
+            if (!(ok = wait_wc(recv_full(slot), (i / RS) & 1))) break;
             const uint32_t src = sb + RECV_OFF + slot * XBUF + xrow;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -380,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 s[4 * k + 3] += v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote_relaxed(slot ? send_ok_remote1 : send_ok_remote0);
+            if (lane == 0) mbar_arrive_remote_relaxed(send_ok_remote0 + 8u * slot);
 
             // online softmax of tile i on this head row
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;

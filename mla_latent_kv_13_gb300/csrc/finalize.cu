@@ -1,5 +1,7 @@
 // finalize.cu -- epilogues of the projection products: split-K reduction, RoPE on the
 // decoupled position branch, bf16 rounding, and the paged-cache scatter of append.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -11,7 +13,7 @@ namespace {
 // 256..287 own RoPE pair t-256 (columns 512 + 2i, 513 + 2i).
 __global__ void __launch_bounds__(288) append_finalize_kernel(
     const float *part, int S, int B, const int32_t *pos, const int32_t *block_table,
-    int max_blocks, uint16_t *cache, int num_blocks, float theta, uint32_t *err) {
+    int max_blocks, uint16_t *cache, int num_blocks, RopeFreqs freqs, uint32_t *err) {
     const int b = blockIdx.x, t = threadIdx.x;
     const int p = pos[b];
     if (p < 0 || p >= max_blocks * BLOCK) {
@@ -30,27 +32,20 @@ __global__ void __launch_bounds__(288) append_finalize_kernel(
         x0 += v.x;
         x1 += v.y;
     }
-    if (col >= D_C) rope_pair(x0, x1, (col - D_C) / 2, p, theta);
+    if (col >= D_C) rope_pair(x0, x1, p, freqs.f[(col - D_C) / 2]);
     uint16_t *dst = cache + ((size_t)blk * BLOCK + (p % BLOCK)) * D_QK + col;
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(x0, x1);
 }
 
-// One CTA per sequence: the 32 rotation angles of its position are formed once
-// (in double, so large positions keep their fractional part), then every head's
-// 32 pairs of c_q W_QR^T are reduced over the k-splits, rotated and stored as bf16.
+// One CTA per sequence: the 32 rotations of its position are formed once, then every
+// head's 32 pairs of c_q W_QR^T are reduced over the k-splits, rotated and stored bf16.
 __global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, int S, int B,
                                                              int H, const int32_t *pos,
-                                                             float theta, uint16_t *q_rope) {
+                                                             RopeFreqs freqs, uint16_t *q_rope) {
     __shared__ float cs[D_ROPE / 2], sn[D_ROPE / 2];
     const int b = blockIdx.x;
-    if (threadIdx.x < D_ROPE / 2) {
-        const int i = threadIdx.x;
-        double freq = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(D_ROPE));
-        double sv, cv;
-        sincos(static_cast<double>(pos[b]) * freq, &sv, &cv);
-        cs[i] = static_cast<float>(cv);
-        sn[i] = static_cast<float>(sv);
-    }
+    if (threadIdx.x < D_ROPE / 2)
+        rope_cos_sin(pos[b], freqs.f[threadIdx.x], cs[threadIdx.x], sn[threadIdx.x]);
     __syncthreads();
     const long row_len = (long)H * D_ROPE;
     for (int e = threadIdx.x; e < H * (D_ROPE / 2); e += blockDim.x) {
@@ -68,6 +63,13 @@ __global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, 
     }
 }
 
+RopeFreqs make_freqs(float theta) {
+    RopeFreqs r;
+    for (int i = 0; i < D_ROPE / 2; ++i)
+        r.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(D_ROPE));
+    return r;
+}
+
 }  // namespace
 
 cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_t *pos,
@@ -75,13 +77,13 @@ cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_
                                    int num_blocks, float theta, uint32_t *err,
                                    cudaStream_t stream) {
     append_finalize_kernel<<<B, 288, 0, stream>>>(part, S, B, pos, block_table, max_blocks, cache,
-                                                  num_blocks, theta, err);
+                                                  num_blocks, make_freqs(theta), err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const int32_t *pos,
                                   float theta, uint16_t *q_rope, cudaStream_t stream) {
-    qrope_finalize_kernel<<<B, 256, 0, stream>>>(part, S, B, H, pos, theta, q_rope);
+    qrope_finalize_kernel<<<B, 256, 0, stream>>>(part, S, B, H, pos, make_freqs(theta), q_rope);
     return cudaGetLastError();
 }
 
