@@ -114,9 +114,12 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  * seqlens [B] int32 (0 <= seqlens[b] <= 64 * max_blocks; checked on the device),
  * out [B][H][512] bf16, lse [B][H] fp32.
  * scale must be finite and > 0 (1/sqrt(d_nope + d_rope) for DeepSeek-shaped heads).
- * H must be 16, 32, 64 or 128. num_splits: 0 = chosen by the library, else the
- * number of token ranges each sequence is cut into (1..256); the ranges are
- * merged exactly by their log-sum-exp (split-KV combine).
+ * H must be 16, 32, 64 or 128; 1 <= B <= 4096. num_splits: the number of equal token
+ * ranges each sequence is cut into (1..256), merged exactly by their log-sum-exps
+ * (split-KV combine); 0 = chosen by the library: such a fixed split when it fits the
+ * GPU in one pass, else a balanced schedule (the concatenated token blocks of all
+ * sequences cut into one equal share per resident work unit, sequences cut between
+ * shares merged the same way).
  * Workspace: mla_decode_workspace_size(B, H, max_seqlen, num_splits) with the
  * same B, H and num_splits; max_seqlen is an upper bound of seqlens.
  */

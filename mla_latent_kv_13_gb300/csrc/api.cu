@@ -45,35 +45,67 @@ void plan_ksplit(int M, int N, int K, int batch, int &splits, int &per) {
     splits = (K + per - 1) / per;
 }
 
-// Token ranges per sequence for decode: minimise waves x tiles-per-range.
+// Token ranges per sequence. An explicit request is taken as is. Otherwise the best
+// fixed split (fewest waves x tiles per range, plus the partials' traffic, assuming all
+// sequences are max_seqlen long) is used when it fits in one wave of clusters; when it
+// would not, 0 is returned: the balanced schedule (equal shares of the concatenated
+// tiles) avoids the partly empty last wave, at the price of restarting the pipeline at
+// every sequence boundary inside a share.
 int plan_decode_splits(int B, int H, int max_seqlen, int requested) {
+    if (requested > 0) return requested;
     int T = (max_seqlen + BLOCK - 1) / BLOCK;
     if (T < 1) T = 1;
-    if (requested > 0) return requested;
-    // one 2-CTA cluster per (sequence, range); a range's partial output costs about
-    // H * 512 * 4 * 2 bytes of extra traffic, i.e. H / 18 cache tiles of 64 tokens
     const int slots = decode_tc_cluster_slots();
     const double part_cost = (double)H * D_C * 4 * 2 / (BLOCK * D_QK * 2);
     int best = 1;
+    long best_waves = 1;
     double best_cost = -1;
     for (int s = 1; s <= 64 && s <= T; ++s) {
-        long items = (long)B * s;
-        long waves = (items + slots - 1) / slots;
-        double cost = (double)waves * ((T + s - 1) / s) +
-                      (s > 1 ? (double)items * part_cost / slots : 0.0);
+        const long items = (long)B * s;
+        const long waves = (items + slots - 1) / slots;
+        const double cost = (double)waves * ((T + s - 1) / s) +
+                            (s > 1 ? (double)items * part_cost / slots : 0.0);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = s;
+            best_waves = waves;
         }
     }
-    return best;
+    return best_waves == 1 ? best : 0;
 }
 
-size_t decode_ws_bytes(int B, int H, int splits) {
-    if (splits <= 1) return HDR;
-    size_t o = align256((size_t)B * splits * H * D_C * sizeof(float));
-    size_t l = align256((size_t)B * splits * H * sizeof(float));
-    return HDR + o + l;
+// Clusters of the balanced schedule: every resident 2-CTA cluster, at most one per tile.
+int sched_clusters(int B, int max_seqlen) {
+    const long tiles = (long)B * ((max_seqlen + BLOCK - 1) / BLOCK);
+    const int slots = decode_tc_cluster_slots();
+    return (int)(tiles < 1 ? 1 : (tiles < slots ? tiles : slots));
+}
+
+struct DecodeLayout {
+    size_t tile_start, part_begin, nparts, o_part, lse_part, total;
+};
+
+DecodeLayout decode_layout(int B, int H, int max_seqlen, int splits) {
+    DecodeLayout L{};
+    if (splits == 1) {
+        L.total = HDR;
+        return L;
+    }
+    if (splits > 1) {
+        L.o_part = HDR;
+        L.lse_part = L.o_part + align256((size_t)B * splits * H * D_C * sizeof(float));
+        L.total = L.lse_part + align256((size_t)B * splits * H * sizeof(float));
+        return L;
+    }
+    const int P = sched_clusters(B, max_seqlen);
+    const size_t parts = 2 * (size_t)P;  // each cluster cuts at most two sequences
+    L.tile_start = HDR;
+    L.part_begin = L.tile_start + align256((size_t)(B + 1) * 4);
+    L.nparts = L.part_begin + align256((size_t)B * 4);
+    L.o_part = L.nparts + align256((size_t)B * 4);
+    L.lse_part = L.o_part + align256(parts * H * D_C * sizeof(float));
+    L.total = L.lse_part + align256(parts * H * sizeof(float));
+    return L;
 }
 
 }  // namespace
@@ -149,10 +181,10 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
 
 mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_splits,
                                        size_t *bytes) {
-    if (!bytes || B < 1 || max_seqlen < 0 || num_splits < 0 || num_splits > 256)
+    if (!bytes || B < 1 || B > 4096 || max_seqlen < 0 || num_splits < 0 || num_splits > 256)
         return MLA_ERR_INVALID_ARG;
     if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
-    *bytes = decode_ws_bytes(B, H, plan_decode_splits(B, H, max_seqlen, num_splits));
+    *bytes = decode_layout(B, H, max_seqlen, plan_decode_splits(B, H, max_seqlen, num_splits)).total;
     return MLA_OK;
 }
 
@@ -165,7 +197,7 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
                                   mla_stream_t stream) {
     if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !workspace || !out || !lse)
         return MLA_ERR_INVALID_ARG;
-    if (B < 1 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
+    if (B < 1 || B > 4096 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
         max_seqlen > max_blocks * BLOCK || num_splits < 0 || num_splits > 256 ||
         !(scale > 0.f) || !isfinite(scale))
         return MLA_ERR_INVALID_ARG;
@@ -174,28 +206,49 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
         !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
         return MLA_ERR_INVALID_ARG;
     const int splits = plan_decode_splits(B, H, max_seqlen, num_splits);
-    if (ws_bytes < decode_ws_bytes(B, H, splits)) return MLA_ERR_WORKSPACE;
+    const DecodeLayout lay = decode_layout(B, H, max_seqlen, splits);
+    if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE;
 
     const int T = (max_seqlen + BLOCK - 1) / BLOCK;
+    char *w = static_cast<char *>(workspace);
     DecodeParams p{};
     p.q_lat = q_lat; p.q_rope = q_rope; p.cache = kv_cache;
     p.block_table = block_table; p.seqlens = seqlens;
     p.num_blocks = num_blocks; p.max_blocks = max_blocks; p.B = B; p.H = H;
-    p.num_splits = splits;
-    p.tiles_per_split = T > 0 ? (T + splits - 1) / splits : 1;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.lse = lse;
     p.err = err_word(workspace);
-    if (splits > 1) {
-        char *w = static_cast<char *>(workspace) + HDR;
-        p.o_part = reinterpret_cast<float *>(w);
-        p.lse_part = reinterpret_cast<float *>(
-            w + align256((size_t)B * splits * H * D_C * sizeof(float)));
+    cudaStream_t st = S(stream);
+    if (splits >= 1) {
+        p.num_splits = splits;
+        p.tiles_per_split = T > 0 ? (T + splits - 1) / splits : 1;
+        if (splits > 1) {
+            p.o_part = reinterpret_cast<float *>(w + lay.o_part);
+            p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
+        }
+        cudaError_t e = launch_decode_tc(p, B * splits, st);
+        if (e != cudaSuccess) return MLA_ERR_CUDA;
+        if (splits > 1) e = launch_combine(p.o_part, p.lse_part, B, splits, H, out, lse, st);
+        return cuda_status(e);
     }
-    cudaError_t e = launch_decode_tc(p, S(stream));
-    if (e != cudaSuccess) return MLA_ERR_CUDA;
-    if (splits > 1) e = launch_combine(p.o_part, p.lse_part, B, splits, H, out, lse, S(stream));
-    return cuda_status(e);
+    // balanced schedule: tile offsets on the device, P persistent clusters, merge of cut sequences
+    const int P = sched_clusters(B, max_seqlen);
+    int32_t *tile_start = reinterpret_cast<int32_t *>(w + lay.tile_start);
+    int32_t *part_begin = reinterpret_cast<int32_t *>(w + lay.part_begin);
+    int32_t *nparts = reinterpret_cast<int32_t *>(w + lay.nparts);
+    p.num_splits = 1;
+    p.tiles_per_split = T;
+    p.tile_start = tile_start;
+    p.part_begin = part_begin;
+    p.nparts = nparts;
+    p.o_part = reinterpret_cast<float *>(w + lay.o_part);
+    p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
+    if (launch_decode_schedule(seqlens, B, max_blocks, P, tile_start, part_begin, nparts, p.err,
+                               st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_status(launch_combine_sched(p.o_part, p.lse_part, tile_start, part_begin, nparts,
+                                            B, H, out, lse, st));
 }
 
 mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S_, int H,

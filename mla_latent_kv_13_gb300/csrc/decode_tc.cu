@@ -1,7 +1,8 @@
 // decode_tc.cu -- absorbed MLA decode attention on the sm_100-family tensor cores
 // (tcgen05 + TMEM), fed by TMA, one 2-CTA thread-block cluster per work item.
 //
-// Work item = (sequence b, token range s). All heads of a sequence score the same
+// Work item = (sequence b, token range s); with the balanced schedule a cluster runs the
+// segments of one equal share of all sequences' tiles in turn. All heads of a sequence score the same
 // latent cache rows [c_kv (512) | k_rope (64)], so the 128 head rows form the M=128
 // side of both products and a 64-token cache tile the N (scores) or K (output) side:
 //   S   = Q [128 x 576] . K^T [576 x 64]      (scores)
@@ -119,8 +120,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    const int item = blockIdx.x >> 1;
-    const int b = item / p.num_splits, split = item % p.num_splits;
     const int H = p.H;
     const int nch = rank == 0 ? 4 : 5;  // 64-column chunks of Q and of each tile owned here
 
@@ -140,18 +139,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
-    int L = p.seqlens[b];
-    if (L < 0 || L > p.max_blocks * TOK) {
-        if (tid == 0 && rank == 0 && split == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
-        L = L < 0 ? 0 : p.max_blocks * TOK;
+    // ---- work: one (sequence, token range) per cluster, or, with the balanced
+    // schedule, the segments of this cluster's equal share of the concatenated tiles
+    const bool sched = p.tile_start != nullptr;
+    const int cl = blockIdx.x >> 1;
+    int P = gridDim.x >> 1;
+    long T = 0, r0 = 0, r1 = 0;
+    int seg_b = 0;
+    if (sched) {
+        T = p.tile_start[p.B];
+        if (T < P) P = static_cast<int>(T);  // as in the schedule: no empty ranges
+        if (cl < P) {
+            r0 = (cl * T) / P;
+            r1 = ((cl + 1) * T) / P;
+        }
+        int lo = 0, hi = p.B - 1;  // largest b with tile_start[b] <= r0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= r0) lo = mid;
+            else hi = mid - 1;
+        }
+        seg_b = lo;
     }
-    const int ntiles = (L + TOK - 1) / TOK;
-    const int t_begin = split * p.tiles_per_split;
-    const int t_end = min(ntiles, t_begin + p.tiles_per_split);
-    const int n = max(0, t_end - t_begin);
-    const int32_t *btab = p.block_table + (size_t)b * p.max_blocks;
-
-    if (tid == 0) {
+    auto init_barriers = [&]() {
         for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -168,8 +178,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             mbar_init(recv_full(k), 1);
             mbar_init(send_ok(k), 4);
         }
-        *abort_flag = 0;
         fence_mbar_init();
+    };
+    if (tid == 0) {
+        init_barriers();
+        *abort_flag = 0;
     }
     if (warp == 0 && lane == 0) tma_prefetch_map(&map_kv);
     if (warp == 1) {
@@ -181,6 +194,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     cluster_sync();  // the peer's barriers exist before any remote operation
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    for (int seg = 0;; ++seg) {
+    // -------- this segment: sequence b, tiles [t_begin, t_end), output slot
+    int b, t_begin, t_end, part;
+    bool direct;
+    if (!sched) {
+        if (seg > 0) break;
+        const int item = blockIdx.x >> 1;
+        b = item / p.num_splits;
+        const int split = item % p.num_splits;
+        t_begin = split * p.tiles_per_split;
+        t_end = t_begin + p.tiles_per_split;  // clipped to the sequence below
+        direct = p.num_splits == 1;
+        part = b * p.num_splits + split;
+    } else {
+        while (seg_b < p.B && p.tile_start[seg_b + 1] == p.tile_start[seg_b]) ++seg_b;
+        if (seg_b >= p.B || p.tile_start[seg_b] >= r1 || r0 >= r1) break;
+        b = seg_b++;
+        const long ts = p.tile_start[b], te = p.tile_start[b + 1];
+        t_begin = static_cast<int>((r0 > ts ? r0 : ts) - ts);
+        t_end = static_cast<int>((r1 < te ? r1 : te) - ts);
+        direct = ts >= r0 && te <= r1;
+        part = direct ? 0 : p.part_begin[b] + (cl - cluster_of_tile(ts, T, P));
+    }
+    int L = p.seqlens[b];
+    if (L < 0 || L > p.max_blocks * TOK) {
+        if (!sched && tid == 0 && rank == 0 && t_begin == 0)
+            flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
+        L = L < 0 ? 0 : p.max_blocks * TOK;
+    }
+    const int ntiles = (L + TOK - 1) / TOK;
+    t_end = min(ntiles, t_end);
+    const int n = max(0, t_end - t_begin);
+    const int32_t *btab = p.block_table + (size_t)b * p.max_blocks;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -460,7 +507,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
 
         // ------------------------------------------------------------- output
-        const bool direct = p.num_splits == 1;
         const int col0 = 256 * rank;
         if (n > 0 && ok && wait_w(pv_done, (n - 1) & 1)) {
             tc_fence_after();
@@ -487,8 +533,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                             __uint_as_float(r[8 * k + 7]) * inv));
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(
-                            p.o_part + (((size_t)b * p.num_splits + split) * H + row) * D_C +
-                            col0 + 32 * c);
+                            p.o_part + ((size_t)part * H + row) * D_C + col0 + 32 * c);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv,
@@ -505,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
             } else {
                 float4 *dst = reinterpret_cast<float4 *>(
-                    p.o_part + (((size_t)b * p.num_splits + split) * H + row) * D_C + col0);
+                    p.o_part + ((size_t)part * H + row) * D_C + col0);
                 for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             l = 0.f;
@@ -515,11 +560,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (direct)
                 p.lse[(size_t)b * H + row] = lse;
             else
-                p.lse_part[((size_t)b * p.num_splits + split) * H + row] = lse;
+                p.lse_part[(size_t)part * H + row] = lse;
         }
     }
 
-    if (tid == 0 && *abort_flag) flag_error(p.err, MLA_ERR_TIMEOUT, b);
+    // -------- end of segment: the peer has drained our last partials (its arrives must
+    // not land on re-initialised barriers), every role is idle, then barriers restart
+    if (warp == 6 && lane == 0)
+        for (int k = max(0, n - RS); k < n; ++k) drain_wait(send_ok(k % RS), (k / RS) & 1);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (!sched || *abort_flag) break;
+    if (tid == 0) init_barriers();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    }  // segments
+
+    if (tid == 0 && *abort_flag) flag_error(p.err, MLA_ERR_TIMEOUT, blockIdx.x);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // no remote access into this CTA after this point
@@ -591,14 +650,14 @@ int decode_tc_cluster_slots() {
     return slots;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream) {
     CUtensorMap mkv;
     if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, TOK))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * p.B * p.num_splits);
+    dim3 grid(2 * clusters);
     decode_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mkv, p);
     return cudaGetLastError();
 }

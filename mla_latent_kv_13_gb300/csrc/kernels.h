@@ -44,12 +44,34 @@ struct DecodeParams {
     float scale_log2;          // scale * log2(e)
     uint16_t *out;             // [B][H][512]  (written when num_splits == 1)
     float *lse;                // [B][H]       (written when num_splits == 1)
-    float *o_part;             // [B][S][H][512] (num_splits > 1)
-    float *lse_part;           // [B][S][H]      (num_splits > 1)
+    float *o_part;             // [B][S][H][512] (num_splits > 1); [2P][H][512] if scheduled
+    float *lse_part;           // [B][S][H]      (num_splits > 1); [2P][H]      if scheduled
     uint32_t *err;
+    // Balanced schedule (num_splits == 0): P clusters each take an equal contiguous range
+    // of the concatenated tile list; sequences cut between clusters become parts.
+    const int32_t *tile_start;  // [B+1] exclusive prefix of tiles per sequence
+    const int32_t *part_begin;  // [B]   first part index of a sequence that is cut
+    const int32_t *nparts;      // [B]   number of parts (0 = whole in one cluster)
 };
 
-cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream);
+// The cluster (of P) whose tile range [c*T/P, (c+1)*T/P) holds global tile t.
+__host__ __device__ inline int cluster_of_tile(long t, long T, int P) {
+    long c = (t * P) / T;
+    while (c + 1 < P && ((c + 1) * T) / P <= t) ++c;
+    while (c > 0 && (c * T) / P > t) --c;
+    return static_cast<int>(c);
+}
+
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
+                                   int32_t *tile_start, int32_t *part_begin, int32_t *nparts,
+                                   uint32_t *err, cudaStream_t stream);
+cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
+                                 const int32_t *tile_start, const int32_t *part_begin,
+                                 const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
+                                 cudaStream_t stream);
+
+// grid = `clusters` two-CTA clusters (one per work item, or P with the schedule)
+cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream);
 int decode_tc_cluster_slots();
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                            uint16_t *out, float *lse, cudaStream_t stream);

@@ -59,7 +59,146 @@ __global__ void reduce_partials_bf16(const float *part, int S, int batch, int M,
     }
 }
 
+// Block-wide exclusive scan of v over n <= 4 * blockDim.x elements (1024 threads).
+__device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_tot) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int a[4], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = 4 * t + k;
+        a[k] = i < n ? v[i] : 0;
+        sum += a[k];
+    }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_tot[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        const int x = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+        int xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, xi, o);
+            if (lane >= o) xi += y;
+        }
+        warp_tot[lane] = xi - x;  // exclusive prefix of the warp totals
+        if (lane == 31) warp_tot[32] = xi;
+    }
+    __syncthreads();
+    int run = warp_tot[w] + inc - sum;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = 4 * t + k;
+        if (i < n) out[i] = run;
+        run += a[k];
+    }
+    const int total = warp_tot[32];
+    __syncthreads();
+    return total;
+}
+
+// One CTA of 1024 threads (B <= 4096): tiles per sequence -> tile_start; parts of the
+// sequences that the equal split of the tile list cuts between clusters.
+__global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seqlens, int B,
+                                                               int max_blocks, int P,
+                                                               int32_t *tile_start,
+                                                               int32_t *part_begin,
+                                                               int32_t *nparts, uint32_t *err) {
+    __shared__ int v[4096], ex[4096], warp_tot[33];
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int L = seqlens[b];
+        if (L < 0 || L > max_blocks * BLOCK) {
+            flag_error(err, MLA_ERR_OUT_OF_RANGE, b);
+            L = L < 0 ? 0 : max_blocks * BLOCK;
+        }
+        v[b] = (L + BLOCK - 1) / BLOCK;
+    }
+    __syncthreads();
+    const int T = block_exclusive_scan4(v, B, ex, warp_tot);
+    // never more ranges than tiles, so that every range is non-empty and a sequence cut
+    // between clusters c0..c1 gets exactly one part from each of them
+    const int Pe = T < P ? T : P;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        tile_start[b] = ex[b];
+        int np = 0;
+        if (v[b] > 0 && T > 0) {
+            const int c0 = cluster_of_tile(ex[b], T, Pe);
+            const int c1 = cluster_of_tile(ex[b] + v[b] - 1, T, Pe);
+            np = c1 > c0 ? c1 - c0 + 1 : 0;
+        }
+        nparts[b] = np;
+    }
+    if (threadIdx.x == 0) tile_start[B] = T;
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) v[b] = nparts[b];
+    __syncthreads();
+    block_exclusive_scan4(v, B, ex, warp_tot);
+    for (int b = threadIdx.x; b < B; b += blockDim.x) part_begin[b] = ex[b];
+}
+
+// Merge of the parts of each cut sequence; empty sequences get out = 0, lse = -inf;
+// sequences finished inside one cluster were written by the attention kernel itself.
+__global__ void __launch_bounds__(128) combine_sched_kernel(
+    const float *o_part, const float *lse_part, const int32_t *tile_start,
+    const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *lse) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int np = nparts[b];
+    const bool empty = tile_start[b + 1] == tile_start[b];
+    if (np == 0 && !empty) return;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float tot = -INFINITY;
+    if (np > 0) {
+        const int p0 = part_begin[b];
+        float m = -INFINITY;
+        for (int s = 0; s < np; ++s) m = fmaxf(m, lse_part[(size_t)(p0 + s) * H + h]);
+        if (m != -INFINITY) {
+            float den = 0.f;
+            for (int s = 0; s < np; ++s) {
+                const float l = lse_part[(size_t)(p0 + s) * H + h];
+                if (l != -INFINITY) den += __expf(l - m);
+            }
+            tot = m + __logf(den);
+            for (int s = 0; s < np; ++s) {
+                const float l = lse_part[(size_t)(p0 + s) * H + h];
+                if (l == -INFINITY) continue;
+                const float w = __expf(l - tot);
+                const float4 x = *reinterpret_cast<const float4 *>(
+                    o_part + ((size_t)(p0 + s) * H + h) * D_C + threadIdx.x * 4);
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+                acc[2] += w * x.z;
+                acc[3] += w * x.w;
+            }
+        }
+    }
+    const uint2 pk = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+    *reinterpret_cast<uint2 *>(out + ((size_t)b * H + h) * D_C + threadIdx.x * 4) = pk;
+    if (threadIdx.x == 0) lse[(size_t)b * H + h] = tot;
+}
+
 }  // namespace
+
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
+                                   int32_t *tile_start, int32_t *part_begin, int32_t *nparts,
+                                   uint32_t *err, cudaStream_t stream) {
+    decode_schedule_kernel<<<1, 1024, 0, stream>>>(seqlens, B, max_blocks, P, tile_start,
+                                                   part_begin, nparts, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
+                                 const int32_t *tile_start, const int32_t *part_begin,
+                                 const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
+                                 cudaStream_t stream) {
+    dim3 grid(H, B);
+    combine_sched_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, tile_start, part_begin,
+                                                   nparts, H, out, lse);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                            uint16_t *out, float *lse, cudaStream_t stream) {

@@ -183,3 +183,29 @@ def test_full_size_workloads_sampled(mla, name, rows):
     assert_lse(lse[rows], lref)
     # property that holds at any size: every row is finite and lse >= max possible floor
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_balanced_schedule_many_ragged_sequences(mla):
+    """The default schedule cuts the concatenated tiles of all sequences into equal
+    ranges: sequences land whole in one range, cut across several, or are empty."""
+    rng = np.random.default_rng(11)
+    L = rng.integers(0, 700, 300)
+    L[::17] = 0
+    L[5] = 64
+    d = _case(len(L), 64, tuple(int(x) for x in L), seed=12)
+    out, lse, st = _run(mla, d, num_splits=0)
+    assert st == 0
+    ref, lref = _oracle(d)
+    assert_close_rows(out, ref)
+    assert_lse(lse, lref)
+
+
+def test_balanced_schedule_matches_fixed_split(mla):
+    # more sequences than resident clusters: the library's own choice is the schedule
+    L = np.random.default_rng(13).integers(0, 5000, 100)
+    L[:4] = (5000, 1, 0, 64)
+    d = _case(100, 128, tuple(int(x) for x in L), seed=13)
+    a = _run(mla, d, num_splits=0)
+    b = _run(mla, d, num_splits=1)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-2, atol=2e-3)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-4)
