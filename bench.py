@@ -451,10 +451,10 @@ def run_gpu_attention(args, w, metric, unit):
 
 
 def step_launches(step) -> int:
-    """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1 (+1 combine), out 3."""
+    """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1-3 (the library's
+    own plan: + merge, + schedule), out 3."""
     from mla_latent_kv_13_gb300 import mla
-    ws_bytes = mla.decode_workspace_size(step.B, step.H, step.max_seqlen, step.num_splits)
-    decode = 1 if ws_bytes <= mla.WS_HEADER_BYTES else 2
+    _, decode = mla.decode_plan(step.B, step.H, step.max_seqlen, step.num_splits)
     return 2 + 6 + decode + 3
 
 

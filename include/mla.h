@@ -125,6 +125,16 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  */
 mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_splits,
                                        size_t *bytes);
+/*
+ * The plan mla_decode_attention takes for these arguments (no counterpart on the pages:
+ * a query of this library's launch plan). *splits = the fixed number of token ranges
+ * per sequence (1 = no merge), or 0 for the balanced schedule; *launches = the kernels
+ * one call launches (1, 2 with a merge, 3 with the schedule). The plan depends on the
+ * device's resident-cluster count, read as mla_decode_workspace_size reads it (a default
+ * when no device is visible). Either output pointer may be null.
+ */
+mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *splits,
+                             int *launches);
 mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                                   const mla_bf16_t *kv_cache, int num_blocks,
                                   const int32_t *block_table, int max_blocks,

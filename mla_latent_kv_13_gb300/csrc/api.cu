@@ -188,6 +188,17 @@ mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_spl
     return MLA_OK;
 }
 
+mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *splits,
+                             int *launches) {
+    if (B < 1 || B > 4096 || max_seqlen < 0 || num_splits < 0 || num_splits > 256)
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    const int s = plan_decode_splits(B, H, max_seqlen, num_splits);
+    if (splits) *splits = s;
+    if (launches) *launches = s == 0 ? 3 : (s > 1 ? 2 : 1);
+    return MLA_OK;
+}
+
 mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                                   const mla_bf16_t *kv_cache, int num_blocks,
                                   const int32_t *block_table, int max_blocks,

@@ -11,7 +11,7 @@
 // two CTAs of a cluster split the latent columns: CTA r stages only its columns of
 // each tile -- r = 0: c_kv[0:256); r = 1: c_kv[256:512) and k_rope -- computes the
 // partial scores over them, swaps the 128 x 64 fp32 partial with its peer through
-// distributed shared memory (st.async), and both CTAs then run the same softmax on
+// distributed shared memory (one bulk copy), and both CTAs then run the same softmax on
 // the same full scores (bit-identical, since fp32 addition commutes) and accumulate
 // their own 256 output columns. No cache byte is read twice and no product is
 // computed twice; the only duplicated work is the (cheap) softmax.

@@ -47,6 +47,7 @@ _SIGS = {
     "mla_append_kv_workspace_size": ([_i, _i, _szp], _i),
     "mla_append_kv": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _f, _vp, _sz, _vp], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _szp], _i),
+    "mla_decode_plan": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
@@ -122,6 +123,16 @@ def append_kv_workspace_size(B, d_model):
 
 def decode_workspace_size(B, H, max_seqlen, num_splits=0):
     return _size("mla_decode_workspace_size", B, H, max_seqlen, num_splits)
+
+
+def decode_plan(B, H, max_seqlen, num_splits=0):
+    """(splits, launches) of mla_decode_attention for these arguments: splits = 0 for the
+    balanced schedule, else the fixed token ranges per sequence."""
+    s, n = _i(0), _i(0)
+    rc = _lib.mla_decode_plan(B, H, max_seqlen, num_splits, ctypes.byref(s), ctypes.byref(n))
+    if rc != 0:
+        raise MLAError(rc, "mla_decode_plan")
+    return s.value, n.value
 
 
 def absorb_q_workspace_size(B, d_model, q_lora, H):

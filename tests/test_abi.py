@@ -68,3 +68,16 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.mla_append_kv_workspace_size(128, 7000, ctypes.byref(sz)) == 1
     assert lib.mla_absorb_q_workspace_size(128, 7168, 1536, 128, ctypes.byref(sz)) == 0
     assert lib.mla_out_absorb_workspace_size(128, 128, 7168, ctypes.byref(sz)) == 0
+
+
+def test_decode_plan_reports_splits_and_launches(lib):
+    from mla_latent_kv_13_gb300 import mla
+    assert mla.decode_plan(16, 128, 4096, 1) == (1, 1)        # no merge
+    assert mla.decode_plan(16, 128, 4096, 4) == (4, 2)        # decode + merge
+    # far more tiles than one pass of resident clusters: the balanced schedule
+    assert mla.decode_plan(4096, 128, 32768, 0) == (0, 3)
+    s, n = mla.decode_plan(2, 128, 64, 0)                     # one tile per sequence
+    assert s >= 1 and n == (1 if s == 1 else 2)
+    i = ctypes.c_int(0)
+    assert lib.mla_decode_plan(0, 128, 64, 0, ctypes.byref(i), None) == 1
+    assert lib.mla_decode_plan(4, 48, 64, 0, None, None) == 2
