@@ -11,20 +11,23 @@
 // two CTAs of a cluster split the latent columns: CTA r stages only its columns of
 // each tile -- r = 0: c_kv[0:256); r = 1: c_kv[256:512) and k_rope -- computes the
 // partial scores over them, swaps the 128 x 64 fp32 partial with its peer through
-// distributed shared memory (one bulk copy), and both CTAs then run the same softmax on
+// distributed shared memory (bulk copies), and both CTAs then run the same softmax on
 // the same full scores (bit-identical, since fp32 addition commutes) and accumulate
 // their own 256 output columns. No cache byte is read twice and no product is
 // computed twice; the only duplicated work is the (cheap) softmax.
 //
-// Roles per CTA (224 threads): warp 0 issues TMA loads (one elected lane); warp 1
+// Roles per CTA (192 threads): warp 0 issues TMA loads (one elected lane); warp 1
 // allocates TMEM and issues tcgen05.mma / tcgen05.commit (one elected lane); warps
 // 2-5 (thread = head row = TMEM lane) load Q into TMEM, combine the two partial
 // scores, run the online softmax in the exp2 domain, write P (bf16) into TMEM and
-// finish the output; they also stage this CTA's partial scores of the next tile in
-// shared memory, from where one thread of warp 6 bulk-copies them to the peer. The
-// exchange (64 fp32 per head row per tile) is bounded by distributed-shared-memory
-// bandwidth (~14 B/clk per SM measured), so it runs one tile ahead on the copy
-// engine, overlapping the softmax of the current tile.
+// finish the output. The exchange is a ping-pong over two 32 KB buffers per CTA: the
+// peer's partial of tile k lands in buffer (k+1) % 2; once a warp has read its 32 rows
+// of it, it overwrites them with its own partial of tile k+1 and bulk-copies them into
+// the peer's buffer k % 2 -- which the peer emptied before it sent tile k. Arrival of
+// data is the only signal: a buffer is always free by the time a copy targets it. The
+// exchange (64 fp32 per head row per tile, ~20 B/clk of distributed shared memory per
+// SM) thus runs one tile ahead on the copy engine, overlapping the softmax of the
+// current tile, and each warp ships its own rows without waiting for the others.
 // Both products read their A operand (Q, P) from TMEM and their B operand (the
 // cache tile, 128-byte swizzled as TMA wrote it) from shared memory. The running maximum
 // is only raised (and O rescaled in TMEM) when a score exceeds it by more than 2^8,
@@ -44,28 +47,24 @@ using namespace sm100;
 #ifndef MLA_DECODE_STAGES
 #define MLA_DECODE_STAGES 4
 #endif
-#ifndef MLA_DECODE_RECV_SLOTS
-#define MLA_DECODE_RECV_SLOTS 1
-#endif
 
 constexpr int TOK = 64;
 constexpr int NS = MLA_DECODE_STAGES;        // cache-tile stages
-constexpr int RS = MLA_DECODE_RECV_SLOTS;    // receive slots for the peer's partial scores
 constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
 constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
 constexpr int KV_OFF = 0;
 constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
 constexpr int XROW = 256;                    // exchange row: 64 fp32, 16-byte chunks XOR-swizzled
-constexpr int XBUF = 128 * XROW;             // 32768
-constexpr int SEND_OFF = KV_OFF + NS * KV_STAGE;   // one send buffer
-constexpr int RECV_OFF = SEND_OFF + XBUF;          // RS receive buffers
-constexpr int BAR_OFF = RECV_OFF + RS * XBUF;
+constexpr int XQ = 32 * XROW;                // the 32 rows of one warp (8 KB)
+constexpr int XBUF = 4 * XQ;                 // 32768
+constexpr int X_OFF = KV_OFF + NS * KV_STAGE;  // two exchange buffers (ping-pong)
+constexpr int BAR_OFF = X_OFF + 2 * XBUF;
 constexpr int NBAR = 24;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
-constexpr int NTHREADS = 224;                // 7 warps
+constexpr int NTHREADS = 192;                // 6 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                 // O: fp32 columns [0, 256)
 constexpr uint32_t TM_S = 256;               // S: fp32 columns [256, 320)
@@ -80,11 +79,10 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(SEND_OFF >= KV_OFF + NS * KV_STAGE && RECV_OFF >= SEND_OFF + XBUF &&
-                  BAR_OFF >= RECV_OFF + RS * XBUF && MISC_OFF >= BAR_OFF + NBAR * 8,
+static_assert(X_OFF >= KV_OFF + NS * KV_STAGE && BAR_OFF >= X_OFF + 2 * XBUF &&
+                  MISC_OFF >= BAR_OFF + NBAR * 8,
               "shared-memory regions must not overlap");
-static_assert(SEND_OFF % 1024 == 0 && RECV_OFF % 16 == 0 && XBUF % 16 == 0,
-              "bulk-copy and swizzle alignment");
+static_assert(X_OFF % 16 == 0 && XQ % 16 == 0, "bulk-copy alignment");
 static_assert((BAR_OFF % 8) == 0, "mbarrier alignment");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -132,10 +130,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t p_full = q_ready + 24;
     const uint32_t pv_done = q_ready + 32;
     const uint32_t mma_drain = q_ready + 40;
-    const uint32_t send_ready = q_ready + 48;  // our partial of the next tile is staged
-    const uint32_t send_free = q_ready + 56;   // the send buffer may be rewritten
-    auto recv_full = [&](int k) { return q_ready + 64 + 8u * k; };  // peer's partial in slot k
-    auto send_ok = [&](int k) { return q_ready + 80 + 8u * k; };    // peer drained its slot k
+    // the peer's partial scores of the rows of warp quadrant q have landed in buffer x
+    auto recv_full = [&](int q, int x) { return q_ready + 48 + 8u * (2 * q + x); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
@@ -172,12 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
         mbar_init(mma_drain, 1);
-        mbar_init(send_ready, 4);
-        mbar_init(send_free, 1);
-        for (int k = 0; k < RS; ++k) {
-            mbar_init(recv_full(k), 1);
-            mbar_init(send_ok(k), 4);
-        }
+        for (int k = 0; k < 8; ++k) mbar_init(recv_full(k >> 1, k & 1), 1);
         fence_mbar_init();
     };
     if (tid == 0) {
@@ -322,26 +313,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             drain_wait(mma_drain, 0);
         }
         __syncwarp();
-    } else if (warp == 6) {
-        // ------------------------------------------------------ score exchange
-        // One thread ships each staged partial (H rows x 272 B) to the peer with a bulk
-        // copy; distributed shared memory moves ~14 B/clk per SM, and the copy engine
-        // keeps that transfer off every warp's instruction queue.
-        if (lane == 0) {
-            for (int k = 0; k < n; ++k) {
-                if (!mbar_wait(send_ready, k & 1, abort_flag, WAIT_NS)) break;
-                // the peer's slot k % RS held tile k - RS: wait until it has been read
-                if (k >= RS &&
-                    !mbar_wait(send_ok(k % RS), ((k / RS) - 1) & 1, abort_flag, WAIT_NS))
-                    break;
-                bulk_copy_to_peer(mapa(sb + RECV_OFF + (k % RS) * XBUF, peer), sb + SEND_OFF,
-                                  H * XROW, mapa(recv_full(k % RS), peer));
-                bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(send_free);
-            }
-        }
-        __syncwarp();
     } else {
         // ------------------------------------------------- softmax / output
         const int wq = warp & 3;
@@ -349,7 +320,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const bool live_row = row < H;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t xrow = row * XROW;
-        const uint32_t send_ok_remote0 = mapa(send_ok(0), peer);
+        // rows of this warp that hold a head: only those are exchanged (both CTAs agree)
+        const int nlive = min(32, max(0, H - wq * 32));
+        const uint32_t xbytes = static_cast<uint32_t>(nlive) * XROW;
+        const uint32_t xq = sb + X_OFF + wq * XQ;            // + XBUF for buffer 1
+        const uint32_t xq_peer = mapa(xq, peer);
+        const uint32_t recv_peer = mapa(recv_full(wq, 0), peer);  // + 8 for buffer 1
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // waits are warp-uniform: a lane that gives up takes its whole warp with it
@@ -386,8 +362,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(q_ready);
         }
 
-        // Read this CTA's partial scores of tile k out of TMEM (releasing the S buffer)
-        // and stage them in send buffer k % 2 for the copy thread.
+        // Read this CTA's partial scores of tile k out of TMEM (releasing the S buffer),
+        // stage this warp's rows of them in buffer k % 2 (the peer's tile k-1 there has
+        // been read) and copy them into the peer's buffer (k+1) % 2.
         uint32_t own[64];
         auto stage_partial = [&](int k) -> bool {
             if (!wait_w(s_full, k & 1)) return false;
@@ -398,15 +375,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-            if (k >= 1 && !wait_w(send_free, (k - 1) & 1)) return false;
-            const uint32_t dst = sb + SEND_OFF + xrow;
+            if (nlive > 0) {
+                const uint32_t buf = (k & 1) * XBUF;
+                const uint32_t dst = sb + X_OFF + buf + xrow;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                st_shared_v4(dst + ((c ^ (row & 7)) << 4), own[4 * c], own[4 * c + 1],
-                             own[4 * c + 2], own[4 * c + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(send_ready);
+                for (int c = 0; c < 16; ++c)
+                    st_shared_v4(dst + ((c ^ (row & 7)) << 4), own[4 * c], own[4 * c + 1],
+                                 own[4 * c + 2], own[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t nb = XBUF - buf;  // the peer's buffer (k+1) % 2
+                    bulk_copy_to_peer(xq_peer + nb, xq + buf, xbytes,
+                                      recv_peer + 8u * ((k + 1) & 1));
+                    bulk_commit();
+                }
+            }
             return true;
         };
 
@@ -419,23 +403,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             float s[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) s[j] = __uint_as_float(own[j]);
-            // stage the next tile's partial first, so its transfer overlaps this softmax
-            if (i + 1 < n && !(ok = stage_partial(i + 1))) break;
-            // the peer's partial of tile i -> full scores
-            const int slot = i % RS;
-            if (row == 0) mbar_arrive_expect_tx(recv_full(slot), H * XROW);
-            if (!(ok = wait_wc(recv_full(slot), (i / RS) & 1))) break;
-            const uint32_t src = sb + RECV_OFF + slot * XBUF + xrow;
+            // the peer's partial of tile i (buffer (i+1) % 2) -> full scores
+            if (nlive > 0) {
+                const int x = (i + 1) & 1;
+                if (lane == 0) mbar_arrive_expect_tx(recv_full(wq, x), xbytes);
+                if (!(ok = wait_wc(recv_full(wq, x), (i >> 1) & 1))) break;
+                const uint32_t src = sb + X_OFF + x * XBUF + xrow;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                float4 v = ld_shared_v4f(src + ((k ^ (row & 7)) << 4));
-                s[4 * k + 0] += v.x;
-                s[4 * k + 1] += v.y;
-                s[4 * k + 2] += v.z;
-                s[4 * k + 3] += v.w;
+                for (int k = 0; k < 16; ++k) {
+                    float4 v = ld_shared_v4f(src + ((k ^ (row & 7)) << 4));
+                    s[4 * k + 0] += v.x;
+                    s[4 * k + 1] += v.y;
+                    s[4 * k + 2] += v.z;
+                    s[4 * k + 3] += v.w;
+                }
+                __syncwarp();
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote_relaxed(send_ok_remote0 + 8u * slot);
+            // then the next tile's partial into the rows just read, so its transfer
+            // overlaps this softmax
+            if (i + 1 < n && !(ok = stage_partial(i + 1))) break;
 
             // online softmax of tile i on this head row
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
@@ -564,10 +550,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
     }
 
-    // -------- end of segment: the peer has drained our last partials (its arrives must
-    // not land on re-initialised barriers), every role is idle, then barriers restart
-    if (warp == 6 && lane == 0)
-        for (int k = max(0, n - RS); k < n; ++k) drain_wait(send_ok(k % RS), (k / RS) & 1);
+    // -------- end of segment: every copy into this CTA has landed (each was waited for),
+    // our own copies have read their rows, every role is idle; then barriers restart
+    if (warp >= 2 && lane == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
     cluster_sync();
