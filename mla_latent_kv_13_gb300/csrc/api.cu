@@ -28,7 +28,8 @@ bool heads_ok(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
 // one CTA per SM): minimise waves x (k-blocks per range + a fixed per-CTA cost of about
 // three k-blocks for filling and draining its pipeline).
 void plan_ksplit(int M, int N, int K, int batch, int &splits, int &per) {
-    const long tiles = (long)((N + 127) / 128) * ((M + 127) / 128) * batch;
+    const int bn = gemm_block_n(N, K);
+    const long tiles = (long)((N + bn - 1) / bn) * ((M + 127) / 128) * batch;
     const int slots = device_sm_count();
     const int kblocks = K / 64;
     int best = 1;

@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(288) append_finalize_kernel(
     }
     const int col = 2 * t;  // 0..574
     float x0 = 0.f, x1 = 0.f;
+    // the split partials are summed in split order; unrolled so the loads overlap
+#pragma unroll 8
     for (int s = 0; s < S; ++s) {
         float2 v = *reinterpret_cast<const float2 *>(part + ((size_t)s * B + b) * D_QK + col);
         x0 += v.x;
@@ -37,8 +39,9 @@ __global__ void __launch_bounds__(288) append_finalize_kernel(
     *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(x0, x1);
 }
 
-// One CTA per sequence: the 32 rotations of its position are formed once, then every
-// head's 32 pairs of c_q W_QR^T are reduced over the k-splits, rotated and stored bf16.
+// CTA (b, y): 256 of the H x 32 (head, pair) entries of sequence b. The 32 rotations of
+// its position are formed first; each thread reduces one pair of c_q W_QR^T over the
+// k-splits (in split order), rotates it and stores it bf16.
 __global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, int S, int B,
                                                              int H, const int32_t *pos,
                                                              RopeFreqs freqs, uint16_t *q_rope) {
@@ -47,20 +50,21 @@ __global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, 
     if (threadIdx.x < D_ROPE / 2)
         rope_cos_sin(pos[b], freqs.f[threadIdx.x], cs[threadIdx.x], sn[threadIdx.x]);
     __syncthreads();
+    const int e = blockIdx.y * blockDim.x + threadIdx.x;
+    if (e >= H * (D_ROPE / 2)) return;
     const long row_len = (long)H * D_ROPE;
-    for (int e = threadIdx.x; e < H * (D_ROPE / 2); e += blockDim.x) {
-        const int h = e / (D_ROPE / 2), pair = e % (D_ROPE / 2);
-        const long off = (long)b * row_len + (long)h * D_ROPE + 2 * pair;
-        float x0 = 0.f, x1 = 0.f;
-        for (int s = 0; s < S; ++s) {
-            float2 v = *reinterpret_cast<const float2 *>(part + (long)s * B * row_len + off);
-            x0 += v.x;
-            x1 += v.y;
-        }
-        const float y0 = x0 * cs[pair] - x1 * sn[pair];
-        const float y1 = x0 * sn[pair] + x1 * cs[pair];
-        *reinterpret_cast<uint32_t *>(q_rope + off) = pack_bf16x2(y0, y1);
+    const int h = e / (D_ROPE / 2), pair = e % (D_ROPE / 2);
+    const long off = (long)b * row_len + (long)h * D_ROPE + 2 * pair;
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) {
+        float2 v = *reinterpret_cast<const float2 *>(part + (long)s * B * row_len + off);
+        x0 += v.x;
+        x1 += v.y;
     }
+    const float y0 = x0 * cs[pair] - x1 * sn[pair];
+    const float y1 = x0 * sn[pair] + x1 * cs[pair];
+    *reinterpret_cast<uint32_t *>(q_rope + off) = pack_bf16x2(y0, y1);
 }
 
 RopeFreqs make_freqs(float theta) {
@@ -83,7 +87,8 @@ cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_
 
 cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const int32_t *pos,
                                   float theta, uint16_t *q_rope, cudaStream_t stream) {
-    qrope_finalize_kernel<<<B, 256, 0, stream>>>(part, S, B, H, pos, make_freqs(theta), q_rope);
+    const dim3 grid(B, (H * (D_ROPE / 2) + 255) / 256);
+    qrope_finalize_kernel<<<grid, 256, 0, stream>>>(part, S, B, H, pos, make_freqs(theta), q_rope);
     return cudaGetLastError();
 }
 

@@ -1,5 +1,7 @@
 // gemm_tc.cu -- bf16 GEMM for the absorbed projections on the sm_100-family tensor
-// cores: TMA-fed, tcgen05.mma into TMEM, one 128 x 128 output tile per CTA.
+// cores: TMA-fed, tcgen05.mma into TMEM, one 128 x BN output tile per CTA (BN = 256 for
+// long, wide products: the activation tile, re-read once per output tile, then costs
+// half as much traffic per weight byte).
 //
 // C[m][n] = sum_k A[m][k] * B(k, n), fp32 accumulation, where the batch rows (the
 // decode batch, M <= 128 per tile) are A and the weights are B:
@@ -14,6 +16,9 @@
 // Roles (192 threads): warp 0 issues TMA (one lane), warp 1 owns TMEM and issues the
 // MMAs (one lane), warps 2-5 read the accumulator out of TMEM and store it. Waits are
 // bounded (one second); a wait that gives up records MLA_ERR_TIMEOUT.
+// The stage ring holds min(6, k-blocks of a CTA) stages and shared memory is sized to
+// it, so products with little K per tile (the per-head absorptions) run several CTAs
+// per SM instead of one.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -24,24 +29,24 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int NS = 6;                       // smem stages
+constexpr int BM = 128, BK = 64;
 constexpr int TILE_A = BM * BK * 2;         // 16 KB
-constexpr int TILE_B = BN * BK * 2;         // 16 KB
-constexpr int STAGE = TILE_A + TILE_B;
-constexpr int BAR_OFF = NS * STAGE;
-constexpr int SMEM_TOTAL = BAR_OFF + 256 + 1024;
+constexpr int NN_GROUP = BK * 64 * 2;       // NN B tile: one 64-column group of BK rows (8 KB)
+constexpr int SMEM_EXTRA = 256 + 1024;      // barriers + slack to align the base
 constexpr int NTHREADS = 192;
-constexpr uint32_t TMEM_COLS = 128;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
-constexpr uint32_t IDESC_TN = idesc_bf16(BM, BN, false, false);
-constexpr uint32_t IDESC_NN = idesc_bf16(BM, BN, false, true);
-
-static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+template <int BN> struct Tile {
+    static constexpr int TILE_B = BN * BK * 2;           // 16 or 32 KB
+    static constexpr int STAGE = TILE_A + TILE_B;
+    static constexpr int NS = BN == 128 ? 6 : 4;         // stages at most
+    static constexpr int SMEM_TOTAL = NS * STAGE + SMEM_EXTRA;
+    static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+};
 
 struct TcGemmArgs {
     int M, N, K, batch, k_splits, k_per_split;
+    int ns;     // stages in the ring (1..NS)
     int a_bx;   // A column offset per batch
     int b_bx;   // B (TN) column offset per batch
     int b_by;   // B row offset per batch (TN: rows of N; NN: rows of K)
@@ -57,10 +62,13 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
-template <bool NN>
+template <bool NN, int BN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, TcGemmArgs g) {
+    constexpr int TILE_B = Tile<BN>::TILE_B, STAGE = Tile<BN>::STAGE;
+    constexpr uint32_t TMEM_COLS = BN;
+    constexpr uint32_t IDESC = idesc_bf16(BM, BN, false, NN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -73,15 +81,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int k_end = min(g.K, k_begin + g.k_per_split);
     const int nkb = (k_end - k_begin + BK - 1) / BK;
 
-    const uint32_t bar = sb + BAR_OFF;
+    const int ns = g.ns;
+    const int bar_off = ns * STAGE;
+    const uint32_t bar = sb + bar_off;
     auto full = [&](int s) { return bar + 8u * s; };
-    auto empty = [&](int s) { return bar + 8u * (NS + s); };
-    const uint32_t done = bar + 8u * (2 * NS);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + BAR_OFF + 8 * (2 * NS + 1));
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + BAR_OFF + 8 * (2 * NS + 2));
+    auto empty = [&](int s) { return bar + 8u * (ns + s); };
+    const uint32_t done = bar + 8u * (2 * ns);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + bar_off + 8 * (2 * ns + 1));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + bar_off + 8 * (2 * ns + 2));
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < ns; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
@@ -106,8 +116,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % NS;
-                if (!mbar_wait(empty(s), ((kb / NS) & 1) ^ 1, abort_flag, WAIT_NS)) break;
+                const int s = kb % ns;
+                if (!mbar_wait(empty(s), ((kb / ns) & 1) ^ 1, abort_flag, WAIT_NS)) break;
                 const int k = k_begin + kb * BK;
                 const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
                 mbar_arrive_expect_tx(full(s), STAGE);
@@ -115,27 +125,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!NN) {
                     tma_load_2d(sbb, &map_b, full(s), batch * g.b_bx + k, batch * g.b_by + n0);
                 } else {
-                    tma_load_2d(sbb, &map_b, full(s), n0, batch * g.b_by + k);
-                    tma_load_2d(sbb + TILE_B / 2, &map_b, full(s), n0 + 64, batch * g.b_by + k);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sbb + j * NN_GROUP, &map_b, full(s), n0 + 64 * j,
+                                    batch * g.b_by + k);
                 }
                 issued = kb + 1;
             }
-            for (int kb = max(0, issued - NS); kb < issued; ++kb) drain(full(kb % NS), (kb / NS) & 1);
+            for (int kb = max(0, issued - ns); kb < issued; ++kb) drain(full(kb % ns), (kb / ns) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = true;
             for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % NS;
-                if (!(ok = mbar_wait(full(s), (kb / NS) & 1, abort_flag, WAIT_NS))) break;
+                const int s = kb % ns;
+                if (!(ok = mbar_wait(full(s), (kb / ns) & 1, abort_flag, WAIT_NS))) break;
                 tc_fence_after();
                 const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t bd = NN ? sdesc_sw128(sbb + kk * 2048, TILE_B / 2, 1024)
+                    const uint64_t bd = NN ? sdesc_sw128(sbb + kk * 2048, NN_GROUP, 1024)
                                            : sdesc_sw128(sbb + kk * 32, 16, 1024);
-                    tc_mma(tmem, ad, bd, NN ? IDESC_NN : IDESC_TN, (kb | kk) != 0);
+                    tc_mma(tmem, ad, bd, IDESC, (kb | kk) != 0);
                 }
                 tc_commit(empty(s));
             }
@@ -233,7 +245,27 @@ bool map_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool NN, int BN>
+cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs g,
+                        const GemmParams &p, cudaStream_t stream) {
+    using T = Tile<BN>;
+    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM, p.batch * p.k_splits);
+    const int kblocks = (p.k_per_split + BK - 1) / BK;
+    g.ns = kblocks < 1 ? 1 : (kblocks < T::NS ? kblocks : T::NS);
+    const int smem = g.ns * T::STAGE + SMEM_EXTRA;
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    gemm_tc_kernel<NN, BN><<<grid, NTHREADS, smem, stream>>>(ma, mb, g);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+// 256-wide tiles halve the activation re-reads per weight byte, which pays on long,
+// wide products (the output projection); shorter ones do better with a deeper ring and
+// fewer k-splits at width 128 (measured).
+int gemm_block_n(int N, int K) { return (N >= 4096 && K >= 4096 && N % 256 == 0) ? 256 : 128; }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column
 // offset batch * a_bx; B is [rows_b][ldb] with every batch's slice at row offset
@@ -249,33 +281,24 @@ cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, ui
     CUtensorMap ma, mb;
     if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM))
         return cudaErrorInvalidValue;
+    const int bn = gemm_block_n(p.N, p.K);
+    g.b_bx = 0;
+    g.b_by = static_cast<int>(p.b_bstride / p.ldb);
     if (!nn) {
         // B slices are [N][K] blocks stacked by rows (b_bstride = rows * ldb elements)
-        g.b_bx = 0;
-        g.b_by = static_cast<int>(p.b_bstride / p.ldb);
         const uint64_t rows = (uint64_t)p.N + (uint64_t)g.b_by * (p.batch - 1);
-        if (!map_2d(&mb, p.B, (uint64_t)p.ldb, rows, (uint64_t)p.ldb, BN))
+        if (!map_2d(&mb, p.B, (uint64_t)p.ldb, rows, (uint64_t)p.ldb, bn))
             return cudaErrorInvalidValue;
     } else {
-        g.b_bx = 0;
-        g.b_by = static_cast<int>(p.b_bstride / p.ldb);
+        // B slices are [K][N] blocks stacked by rows, loaded as 64-column groups of BK rows
         const uint64_t rows = (uint64_t)p.K + (uint64_t)g.b_by * (p.batch - 1);
         if (!map_2d(&mb, p.B, (uint64_t)p.ldb, rows, (uint64_t)p.ldb, BK))
             return cudaErrorInvalidValue;
     }
-    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM, p.batch * p.k_splits);
-    if (nn) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-        if (e != cudaSuccess) return e;
-        gemm_tc_kernel<true><<<grid, NTHREADS, SMEM_TOTAL, stream>>>(ma, mb, g);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-        if (e != cudaSuccess) return e;
-        gemm_tc_kernel<false><<<grid, NTHREADS, SMEM_TOTAL, stream>>>(ma, mb, g);
-    }
-    return cudaGetLastError();
+    if (nn) return bn == 256 ? launch_tile<true, 256>(ma, mb, g, p, stream)
+                             : launch_tile<true, 128>(ma, mb, g, p, stream);
+    return bn == 256 ? launch_tile<false, 256>(ma, mb, g, p, stream)
+                     : launch_tile<false, 128>(ma, mb, g, p, stream);
 }
 
 }  // namespace mla

@@ -50,7 +50,8 @@ __global__ void reduce_partials_bf16(const float *part, int S, int batch, int M,
         long bm = e / N;
         int m = bm % M, bt = bm / M;
         float v0 = 0.f, v1 = 0.f;
-        for (int s = 0; s < S; ++s) {
+#pragma unroll 8
+        for (int s = 0; s < S; ++s) {  // split order; unrolled so the loads overlap
             float2 t = *reinterpret_cast<const float2 *>(part + ((long)s * batch * M * N) + e);
             v0 += t.x;
             v1 += t.y;

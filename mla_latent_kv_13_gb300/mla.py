@@ -280,16 +280,27 @@ class DecodeStep:
         self.o_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.y = torch.empty((B, self.dm), dtype=torch.bfloat16, device=dev)
+        # append_kv and absorb_q read only h and pos: the append runs on a side stream,
+        # forked from and joined back into the caller's stream by events
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_join = torch.cuda.Event()
 
     def __call__(self, h, pos, seqlens_after, block_table, kv_cache, stream=None):
         w = self.w
-        append_kv(h, w["w_dkr"], pos, block_table, kv_cache, self.theta, self.ws_append, stream)
+        main = torch.cuda.current_stream() if stream is None else stream
+        self.ev_fork.record(main)
+        self.side.wait_event(self.ev_fork)
+        append_kv(h, w["w_dkr"], pos, block_table, kv_cache, self.theta, self.ws_append,
+                  self.side)
+        self.ev_join.record(self.side)
         absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, self.theta, self.q_lat,
-                 self.q_rope, self.ws_q, stream)
+                 self.q_rope, self.ws_q, main)
+        main.wait_event(self.ev_join)  # attention reads the row the append wrote
         decode_attention(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
                          self.max_seqlen, self.scale, self.num_splits, self.o_lat, self.lse,
-                         self.ws_att, stream)
-        out_absorb(self.o_lat, w["w_uv"], w["w_o"], self.y, self.ws_out, stream)
+                         self.ws_att, main)
+        out_absorb(self.o_lat, w["w_uv"], w["w_o"], self.y, self.ws_out, main)
         return self.y
 
     def check(self, stream=None) -> int:
