@@ -66,7 +66,7 @@ template <bool NN, int BN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, TcGemmArgs g) {
-    constexpr int TILE_B = Tile<BN>::TILE_B, STAGE = Tile<BN>::STAGE;
+    constexpr int STAGE = Tile<BN>::STAGE;
     constexpr uint32_t TMEM_COLS = BN;
     constexpr uint32_t IDESC = idesc_bf16(BM, BN, false, NN);
     extern __shared__ uint8_t smem_raw[];
