@@ -176,6 +176,24 @@ def decode_absorbed(q_lat, q_rope, kv_cache, block_table, seqlens, scale, want_p
     return (out, lse, probs) if want_probs else (out, lse)
 
 
+def decode_absorbed_mq(q_lat, q_rope, kv_cache, block_table, seqlens, scale):
+    """Decode attention for s_q query tokens per sequence (the draft tokens a main model
+    verifies in one pass: "When MoE meets MLA" §5.3 item 3, "DeepSeek V3 MoE inference"
+    §6). The draft rows are the last s_q of each sequence's seqlens[b] cached rows, and
+    draft token t (0-based) attends causally: to the rows j < seqlens[b] - (s_q - 1 - t).
+    Each (b, t) is therefore the absorbed decode of a sequence of that length over b's
+    blocks. q_lat [B,s_q,H,d_c], q_rope [B,s_q,H,d_r] -> (out [B,s_q,H,d_c], lse [B,s_q,H])."""
+    q_lat, q_rope = _f64(q_lat), _f64(q_rope)
+    B, s_q, H, d_c = q_lat.shape
+    d_r = q_rope.shape[3]
+    bt, L = _i32(block_table), _i32(seqlens)
+    visible = np.maximum(L[:, None] - (s_q - 1 - np.arange(s_q))[None, :], 0)
+    out, lse = decode_absorbed(q_lat.reshape(B * s_q, H, d_c), q_rope.reshape(B * s_q, H, d_r),
+                               kv_cache, np.repeat(bt, s_q, axis=0),
+                               visible.reshape(-1).astype(np.int32), scale)
+    return out.reshape(B, s_q, H, d_c), lse.reshape(B, s_q, H)
+
+
 def decode_expanded(q_nope, q_rope, kv_cache, block_table, seqlens, w_uk, w_uv, scale):
     """Expanded (explicit K/V per head) decode attention. Returns (out_v [B,H,d_v], lse [B,H])."""
     q_nope, q_rope, w_uk, w_uv = _f64(q_nope), _f64(q_rope), _f64(w_uk), _f64(w_uv)

@@ -420,3 +420,52 @@ def test_out_absorb_matches_matrix_products():
     y = oracle.out_absorb(o_lat, p["w_uv"], p["w_o"])
     ov = np.einsum("hdc,bhc->bhd", widen(p["w_uv"]), o_lat).reshape(B, H * 128)
     np.testing.assert_allclose(y, ov @ widen(p["w_o"]).T, rtol=1e-11, atol=1e-13)
+
+
+# ---------------------------------------------------------------- multi-query decode
+
+
+@pytest.mark.parametrize("L,s_q", [(1, 1), (5, 2), (64, 4), (65, 3), (130, 4)])
+def test_multi_query_zero_query_sees_exactly_its_causal_prefix(L, s_q):
+    """q = 0 turns every draft token's output into the mean of the rows it sees and its
+    lse into ln(count): draft token t sees L - (s_q - 1 - t) rows (closed form)."""
+    d = _random_case(1, 2, [L], seed=40)
+    q0 = np.zeros((1, s_q, 2, 512))
+    r0 = np.zeros((1, s_q, 2, 64))
+    out, lse = oracle.decode_absorbed_mq(q0, r0, d["kv_cache"], d["block_table"], [L],
+                                         d["scale"])
+    rows = np.stack([widen(d["kv_cache"][d["block_table"][0, j // 64], j % 64, :512])
+                     for j in range(L)])
+    for t in range(s_q):
+        n = L - (s_q - 1 - t)
+        if n <= 0:
+            assert np.all(out[0, t] == 0) and np.all(np.isneginf(lse[0, t]))
+            continue
+        np.testing.assert_allclose(out[0, t, 1], rows[:n].mean(axis=0), rtol=1e-12, atol=1e-14)
+        assert lse[0, t, 0] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_multi_query_draft_tokens_never_see_later_rows():
+    """Poisoning the rows after draft token t's visible prefix leaves its result alone and
+    changes the later tokens'; the last token sees the whole sequence."""
+    B, H, s_q, L = 2, 4, 3, 150
+    d = _random_case(B, H, [L, L - 20], seed=41)
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((B, s_q, H, 512)) * 0.3
+    r = rng.standard_normal((B, s_q, H, 64)) * 0.3
+    Ls = [L, L - 20]
+    out, lse = oracle.decode_absorbed_mq(q, r, d["kv_cache"], d["block_table"], Ls, d["scale"])
+    cache = d["kv_cache"].copy()
+    for b in range(B):  # overwrite the last two rows of each sequence
+        for j in (Ls[b] - 2, Ls[b] - 1):
+            cache[d["block_table"][b, j // 64], j % 64, :] = bf16(rng.standard_normal(576) * 5)
+    out2, lse2 = oracle.decode_absorbed_mq(q, r, cache, d["block_table"], Ls, d["scale"])
+    np.testing.assert_array_equal(out2[:, 0], out[:, 0])   # sees rows < L - 2
+    np.testing.assert_array_equal(lse2[:, 0], lse[:, 0])
+    assert not np.allclose(out2[:, 1], out[:, 1])            # sees row L - 2
+    assert not np.allclose(out2[:, 2], out[:, 2])
+    for b in range(B):  # the last draft token is plain decode over the whole sequence
+        o1, l1 = oracle.decode_absorbed(q[b:b + 1, s_q - 1], r[b:b + 1, s_q - 1], d["kv_cache"],
+                                        d["block_table"][b:b + 1], [Ls[b]], d["scale"])
+        np.testing.assert_array_equal(out[b, s_q - 1], o1[0])
+        np.testing.assert_array_equal(lse[b, s_q - 1], l1[0])
