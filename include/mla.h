@@ -144,6 +144,29 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
                                   mla_stream_t stream);
 
 /*
+ * Decode attention for s_q query tokens per sequence: the draft tokens a main model
+ * verifies in one pass ("When MoE meets MLA" §5.3 item 3, "DeepSeek V3 MoE inference"
+ * §6). The draft tokens' own cache rows are the last s_q of the seqlens[b] rows already
+ * in the cache, and draft token t (0-based) attends causally, to the rows
+ * j < seqlens[b] - (s_q - 1 - t); a token that sees no row gets out = 0, lse = -inf.
+ * Otherwise as mla_decode_attention, with the query rows of a sequence ordered
+ * (token, head): q_lat [B][s_q][H][512], q_rope [B][s_q][H][64] bf16,
+ * out [B][s_q][H][512] bf16, lse [B][s_q][H] fp32. H must be 16, 32, 64 or 128 with
+ * s_q * H <= 128 (MLA_ERR_UNSUPPORTED otherwise); s_q >= 1. s_q = 1 is exactly
+ * mla_decode_attention. Workspace: mla_decode_mq_workspace_size with the same B, s_q, H
+ * and num_splits.
+ */
+mla_status_t mla_decode_mq_workspace_size(int B, int s_q, int H, int max_seqlen, int num_splits,
+                                          size_t *bytes);
+mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                     const mla_bf16_t *kv_cache, int num_blocks,
+                                     const int32_t *block_table, int max_blocks,
+                                     const int32_t *seqlens, int B, int s_q, int H,
+                                     int max_seqlen, float scale, int num_splits, void *workspace,
+                                     size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                     mla_stream_t stream);
+
+/*
  * The split-KV merge on its own (the last step of mla_decode_attention):
  *   lse[b][h] = ln sum_s exp(lse_part[b][s][h]);
  *   out[b][h] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h]

@@ -200,20 +200,24 @@ mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *
     return MLA_OK;
 }
 
-mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
-                                  const mla_bf16_t *kv_cache, int num_blocks,
-                                  const int32_t *block_table, int max_blocks,
-                                  const int32_t *seqlens, int B, int H, int max_seqlen,
-                                  float scale, int num_splits, void *workspace,
-                                  size_t ws_bytes, mla_bf16_t *out, float *lse,
-                                  mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Decode over H = s_q x hq query rows per sequence (query token t, head h at row t*hq + h);
+// token t sees the rows j < seqlens[b] - (s_q - 1 - t). Plain decode: s_q = 1, hq = H.
+mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                        const mla_bf16_t *kv_cache, int num_blocks, const int32_t *block_table,
+                        int max_blocks, const int32_t *seqlens, int B, int s_q, int hq,
+                        int max_seqlen, float scale, int num_splits, void *workspace,
+                        size_t ws_bytes, mla_bf16_t *out, float *lse, mla_stream_t stream) {
+    const int H = s_q * hq;
     if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !workspace || !out || !lse)
         return MLA_ERR_INVALID_ARG;
     if (B < 1 || B > 4096 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
         max_seqlen > max_blocks * BLOCK || num_splits < 0 || num_splits > 256 ||
-        !(scale > 0.f) || !isfinite(scale))
+        !(scale > 0.f) || !isfinite(scale) || s_q < 1)
         return MLA_ERR_INVALID_ARG;
-    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!heads_ok(hq) || H > 128) return MLA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||
         !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
         return MLA_ERR_INVALID_ARG;
@@ -227,6 +231,7 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
     p.q_lat = q_lat; p.q_rope = q_rope; p.cache = kv_cache;
     p.block_table = block_table; p.seqlens = seqlens;
     p.num_blocks = num_blocks; p.max_blocks = max_blocks; p.B = B; p.H = H;
+    p.s_q = s_q; p.hq = hq;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = out; p.lse = lse;
     p.err = err_word(workspace);
@@ -261,6 +266,44 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
     if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_status(launch_combine_sched(p.o_part, p.lse_part, tile_start, part_begin, nparts,
                                             B, H, out, lse, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                  const mla_bf16_t *kv_cache, int num_blocks,
+                                  const int32_t *block_table, int max_blocks,
+                                  const int32_t *seqlens, int B, int H, int max_seqlen,
+                                  float scale, int num_splits, void *workspace,
+                                  size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                  mla_stream_t stream) {
+    return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
+                      1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
+}
+
+mla_status_t mla_decode_mq_workspace_size(int B, int s_q, int H, int max_seqlen, int num_splits,
+                                          size_t *bytes) {
+    if (s_q < 1) return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H) || s_q * H > 128) return MLA_ERR_UNSUPPORTED;
+    if (!bytes || B < 1 || B > 4096 || max_seqlen < 0 || num_splits < 0 || num_splits > 256)
+        return MLA_ERR_INVALID_ARG;
+    const int rows = s_q * H;
+    *bytes = decode_layout(B, rows, max_seqlen, plan_decode_splits(B, rows, max_seqlen, num_splits))
+                 .total;
+    return MLA_OK;
+}
+
+mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                     const mla_bf16_t *kv_cache, int num_blocks,
+                                     const int32_t *block_table, int max_blocks,
+                                     const int32_t *seqlens, int B, int s_q, int H,
+                                     int max_seqlen, float scale, int num_splits, void *workspace,
+                                     size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                     mla_stream_t stream) {
+    return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
+                      s_q, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
 }
 
 mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S_, int H,

@@ -318,6 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int wq = warp & 3;
         const int row = wq * 32 + lane;  // head row == TMEM lane
         const bool live_row = row < H;
+        // row = (query token t, head): token t of s_q sees the rows j < L - (s_q - 1 - t)
+        const int back = live_row ? p.s_q - 1 - row / p.hq : 0;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t xrow = row * XROW;
         // rows of this warp that hold a head: only those are exchanged (both CTAs agree)
@@ -426,7 +428,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // online softmax of tile i on this head row
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int tvalid = blk_ok ? min(TOK, L - tile * TOK) : 0;  // valid tokens of the tile
-            const int valid = live_row ? tvalid : 0;                    // columns this row keeps
+            // columns this row keeps
+            const int valid = live_row ? min(tvalid, max(0, L - back - tile * TOK)) : 0;
             if (valid < TOK) {
 #pragma unroll
                 for (int j = 0; j < 64; ++j)

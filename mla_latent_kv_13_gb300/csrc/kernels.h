@@ -40,7 +40,8 @@ struct DecodeParams {
     const uint16_t *cache;     // [num_blocks][64][576]
     const int32_t *block_table;
     const int32_t *seqlens;
-    int num_blocks, max_blocks, B, H;
+    int num_blocks, max_blocks, B, H;  // H = query rows per sequence (s_q x hq)
+    int s_q, hq;  // query tokens per sequence (draft tokens, causal among them), heads each
     int num_splits, tiles_per_split;
     float scale_log2;          // scale * log2(e)
     uint16_t *out;             // [B][H][512]  (written when num_splits == 1)

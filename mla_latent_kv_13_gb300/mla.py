@@ -51,6 +51,9 @@ _SIGS = {
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "mla_decode_mq_workspace_size": ([_i, _i, _i, _i, _i, _szp], _i),
+    "mla_decode_attention_mq": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _f, _i, _vp,
+                                 _sz, _vp, _vp, _vp], _i),
     "mla_decode_attention_noalloc": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
                                       _vp, _vp], _i),
     "mla_absorb_q_workspace_size": ([_i, _i, _i, _i, _szp], _i),
@@ -177,6 +180,33 @@ def decode_attention(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, 
                                    float(scale), int(num_splits), _ptr(workspace),
                                    workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
     _ok(rc, "mla_decode_attention")
+    return out, lse, workspace
+
+
+def decode_mq_workspace_size(B, s_q, H, max_seqlen, num_splits=0):
+    return _size("mla_decode_mq_workspace_size", B, s_q, H, max_seqlen, num_splits)
+
+
+def decode_attention_mq(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, scale,
+                        num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """mla_decode_attention_mq: q_lat [B,s_q,H,512], q_rope [B,s_q,H,64] (draft tokens,
+    causal among them). Returns (out [B,s_q,H,512] bf16, lse [B,s_q,H] fp32, workspace)."""
+    B, s_q, H, _ = q_lat.shape
+    dev = q_lat.device
+    if out is None:
+        out = torch.empty((B, s_q, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(decode_mq_workspace_size(B, s_q, H, max_seqlen, num_splits),
+                                    stream=stream)
+    rc = _lib.mla_decode_attention_mq(_ptr(_bits(q_lat)), _ptr(_bits(q_rope)),
+                                      _ptr(_bits(kv_cache)), kv_cache.shape[0],
+                                      _ptr(block_table), block_table.shape[1], _ptr(seqlens), B,
+                                      s_q, H, int(max_seqlen), float(scale), int(num_splits),
+                                      _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                                      _stream(stream))
+    _ok(rc, "mla_decode_attention_mq")
     return out, lse, workspace
 
 

@@ -81,3 +81,22 @@ def test_decode_plan_reports_splits_and_launches(lib):
     i = ctypes.c_int(0)
     assert lib.mla_decode_plan(0, 128, 64, 0, ctypes.byref(i), None) == 1
     assert lib.mla_decode_plan(4, 48, 64, 0, None, None) == 2
+
+
+def test_multi_query_validation_before_launch(lib):
+    from mla_latent_kv_13_gb300 import mla
+    # s_q * H rows must fit the 128 TMEM lanes; H itself a supported head count
+    assert mla.decode_mq_workspace_size(4, 2, 64, 256) > 0
+    sz = ctypes.c_size_t(0)
+    assert lib.mla_decode_mq_workspace_size(4, 2, 128, 256, 0, ctypes.byref(sz)) == 2
+    assert lib.mla_decode_mq_workspace_size(4, 3, 48, 256, 0, ctypes.byref(sz)) == 2
+    assert lib.mla_decode_mq_workspace_size(4, 0, 16, 256, 0, ctypes.byref(sz)) == 1
+    # s_q = 1 sizes exactly like plain decode
+    assert mla.decode_mq_workspace_size(8, 1, 128, 4096, 3) == \
+        mla.decode_workspace_size(8, 128, 4096, 3)
+    null = ctypes.c_void_p(0)
+    lib.mla_decode_attention_mq.restype = ctypes.c_int
+    rc = lib.mla_decode_attention_mq(null, null, null, 1, null, 1, null, 1, 2, 16, 64,
+                                     ctypes.c_float(0.07), 0, null, ctypes.c_size_t(0), null,
+                                     null, null)
+    assert rc == 1
