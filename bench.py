@@ -395,16 +395,27 @@ def run_gpu_attention(args, w, metric, unit):
     ql, qr, cache = dbf(d["q_lat"]), dbf(d["q_rope"]), dbf(d["kv_cache"])
     bt = torch.from_numpy(d["block_table"]).to(dev)
     L = torch.from_numpy(d["seqlens"]).to(dev)
-    B, H = d["B"], d["H"]
+    B, H = d["B"], d["H"]  # H = query rows per sequence (s_q tokens x H / s_q heads)
+    s_q = w.s_q
     max_len = int(d["seqlens"].max())
     ws = mla.alloc_workspace(mla.decode_workspace_size(B, H, max_len, args.num_splits))
     out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if s_q > 1:  # draft tokens: the same rows, causal among the s_q tokens
+        ql, qr = ql.view(B, s_q, H // s_q, 512), qr.view(B, s_q, H // s_q, 64)
+        out, lse = out.view(B, s_q, H // s_q, 512), lse.view(B, s_q, H // s_q)
+
+    def attend(c):
+        if s_q > 1:
+            mla.decode_attention_mq(ql, qr, c, bt, L, max_len, d["scale"], args.num_splits, out,
+                                    lse, ws)
+        else:
+            mla.decode_attention(ql, qr, c, bt, L, max_len, d["scale"], args.num_splits, out,
+                                 lse, ws)
 
     def one():
-        mla.decode_attention(ql, qr, cache, bt, L, max_len, d["scale"], args.num_splits, out, lse,
-                             ws)
+        attend(cache)
 
     for _ in range(args.warmup):
         one()
@@ -419,9 +430,7 @@ def run_gpu_attention(args, w, metric, unit):
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(args.steps):
-        c = copies[i % len(copies)]
-        mla.decode_attention(ql, qr, c, bt, L, max_len, d["scale"], args.num_splits, out, lse,
-                             ws)
+        attend(copies[i % len(copies)])
     end.record(stream)
     torch.cuda.synchronize(dev)
     if mla.check_device_status(ws) != 0:
@@ -441,12 +450,12 @@ def run_gpu_attention(args, w, metric, unit):
             "data": "synthetic",
             "config": dict(w.describe(), l2=("rotating %d cache copies" % len(copies))
                            if len(copies) > 1 else "inputs larger than L2"),
-            "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": B / (ms * 1e-3),
+            "tflops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": B * s_q / (ms * 1e-3),
             "roofline": {"kernel": "decode_attention", "bound": "hbm", "achieved": gbs,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": roof_s / (ms * 1e-3), "traffic": None,
                          "peak_source": peaks["source"] + " (burst copy)"},
-            "gpu_launches": args.steps * (1 if ws.numel() <= 256 else 2)}
+            "gpu_launches": args.steps * mla.decode_plan(B, H, max_len, args.num_splits)[1]}
     print(json.dumps(line), flush=True)
 
 
@@ -481,7 +490,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["step", "tiny", "v3", "mixed", "long"],
+                    choices=["step", "tiny", "v3", "mixed", "long", "mtp"],
                     help="step = the full decode step (default); the others time decode "
                          "attention alone on that attention workload")
     ap.add_argument("--cpu-sample", type=int, default=32)

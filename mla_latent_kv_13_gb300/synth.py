@@ -50,10 +50,13 @@ class Workload:
     full_step: bool = False
     d_model: int = 7168
     q_lora: int = 1536
+    s_q: int = 1  # query tokens per sequence; `heads` counts query rows (s_q x heads each)
 
     def describe(self) -> dict:
-        d = {"workload": self.name, "batch": self.batch, "heads": self.heads,
+        d = {"workload": self.name, "batch": self.batch, "heads": self.heads // self.s_q,
              "d_c": D_C, "d_rope": D_ROPE, "block": BLOCK}
+        if self.s_q > 1:
+            d["query_tokens"] = self.s_q
         if self.seqlens is not None:
             d["seqlens"] = list(self.seqlens) if len(set(self.seqlens)) > 1 else self.seqlens[0]
         else:
@@ -68,6 +71,8 @@ WORKLOADS = {
     "v3": Workload("v3", 16, 128, (4096,) * 16, None, shuffled=True),
     "mixed": Workload("mixed", 128, 128, None, (1024, 8192), shuffled=True),
     "long": Workload("long", 32, 64, (32768,) * 32, None, shuffled=True),
+    # draft-token verification: 2 query tokens x 64 heads = 128 query rows per sequence
+    "mtp": Workload("mtp", 128, 128, (8192,) * 128, None, shuffled=True, s_q=2),
     "step": Workload("step", 128, 128, (8192,) * 128, None, shuffled=True, full_step=True),
 }
 
