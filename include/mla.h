@@ -167,6 +167,17 @@ mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *
                                      mla_stream_t stream);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages: a check of this library).
+ * Launches one CTA that waits, with the bounded mbarrier wait every kernel of the library
+ * uses, on a barrier that nothing completes; after limit_us microseconds (1..1000000) the
+ * wait gives up and MLA_ERR_TIMEOUT is recorded in the workspace error word (detail = the
+ * microseconds waited), to be read with mla_check_device_status. Nothing faults and the
+ * context stays usable. workspace: at least the 256-byte header, 256-byte aligned.
+ */
+mla_status_t mla_selftest_wait_timeout(unsigned limit_us, void *workspace, size_t ws_bytes,
+                                       mla_stream_t stream);
+
+/*
  * The split-KV merge on its own (the last step of mla_decode_attention):
  *   lse[b][h] = ln sum_s exp(lse_part[b][s][h]);
  *   out[b][h] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h]

@@ -306,6 +306,15 @@ mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *
                       s_q, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
 }
 
+mla_status_t mla_selftest_wait_timeout(unsigned limit_us, void *workspace, size_t ws_bytes,
+                                       mla_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000 || !workspace || ws_bytes < MLA_WS_HEADER_BYTES ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000u,
+                                                    err_word(workspace), S(stream)));
+}
+
 mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int B, int S_, int H,
                                 mla_bf16_t *out, float *lse, mla_stream_t stream) {
     if (!o_part || !lse_part || !out || !lse || B < 1 || S_ < 1 || H < 1 || H > 65535)

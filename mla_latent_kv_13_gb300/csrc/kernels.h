@@ -80,4 +80,7 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, in
 
 int device_sm_count();
 
+// One CTA waits on a barrier nothing completes; records MLA_ERR_TIMEOUT after limit_ns.
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t stream);
+
 }  // namespace mla

@@ -62,6 +62,7 @@ _SIGS = {
     "mla_out_absorb_workspace_size": ([_i, _i, _i, _szp], _i),
     "mla_out_absorb": ([_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "mla_clear_device_status": ([_vp, _vp], _i),
+    "mla_selftest_wait_timeout": ([ctypes.c_uint, _vp, _sz, _vp], _i),
     "mla_check_device_status": ([_vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -279,6 +280,16 @@ def out_absorb(o_lat, w_uv, w_o, y=None, workspace=None, stream=None):
 def check_device_status(workspace, stream=None) -> int:
     """Synchronise and return (and clear) the workspace's device error word."""
     return int(_lib.mla_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def selftest_wait_timeout(limit_us, workspace, stream=None):
+    """Run the failure-detection self-test; returns (status, detail) from the workspace
+    header after it (expected: MLA_ERR_TIMEOUT and at least limit_us microseconds)."""
+    _ok(_lib.mla_selftest_wait_timeout(int(limit_us), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "mla_selftest_wait_timeout")
+    torch.cuda.synchronize(workspace.device)
+    hdr = workspace[:8].view(torch.int32).cpu().tolist()
+    return hdr[0] & 0xFFFFFFFF, hdr[1] & 0xFFFFFFFF
 
 
 def clear_device_status(workspace, stream=None):

@@ -100,3 +100,10 @@ def test_multi_query_validation_before_launch(lib):
                                      ctypes.c_float(0.07), 0, null, ctypes.c_size_t(0), null,
                                      null, null)
     assert rc == 1
+
+
+def test_selftest_validation_before_launch(lib):
+    null = ctypes.c_void_p(0)
+    lib.mla_selftest_wait_timeout.restype = ctypes.c_int
+    assert lib.mla_selftest_wait_timeout(ctypes.c_uint(0), null, ctypes.c_size_t(256), null) == 1
+    assert lib.mla_selftest_wait_timeout(ctypes.c_uint(100), null, ctypes.c_size_t(256), null) == 1
