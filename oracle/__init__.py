@@ -215,6 +215,21 @@ def decode_expanded(q_nope, q_rope, kv_cache, block_table, seqlens, w_uk, w_uv, 
     return out, lse
 
 
+def prefill_expanded(q_nope, q_rope, kv_cache, block_table_row, prefix, w_uk, w_uv, scale):
+    """Chunked prefill of one sequence in the expanded (un-absorbed) form ("LLM inference:
+    from the memory wall to the compute wall" §2.2: prefill is compute-bound, so the keys
+    and values are projected back per head instead of absorbing the projections into the
+    query). The chunk's C tokens sit at positions prefix .. prefix + C - 1 of the cache
+    (already appended); query i attends causally to the positions j <= prefix + i, i.e. it
+    is the expanded decode of a sequence of length prefix + i + 1.
+    q_nope [C,H,d_h], q_rope [C,H,d_r] -> (out_v [C,H,d_v], lse [C,H])."""
+    q_nope, q_rope = _f64(q_nope), _f64(q_rope)
+    C = q_nope.shape[0]
+    bt = np.repeat(_i32(block_table_row).reshape(1, -1), C, axis=0)
+    lengths = (int(prefix) + 1 + np.arange(C)).astype(np.int32)
+    return decode_expanded(q_nope, q_rope, kv_cache, bt, lengths, w_uk, w_uv, scale)
+
+
 def combine(o_part, lse_part):
     """Merge split results: o_part [B,S,H,d], lse_part [B,S,H] -> (out [B,H,d], lse [B,H])."""
     o_part, lse_part = _f64(o_part), _f64(lse_part)

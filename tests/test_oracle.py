@@ -469,3 +469,68 @@ def test_multi_query_draft_tokens_never_see_later_rows():
                                         d["block_table"][b:b + 1], [Ls[b]], d["scale"])
         np.testing.assert_array_equal(out[b, s_q - 1], o1[0])
         np.testing.assert_array_equal(lse[b, s_q - 1], l1[0])
+
+
+# ---------------------------------------------------------------- chunked prefill
+
+
+@pytest.mark.parametrize("prefix,C", [(0, 5), (70, 3), (128, 2)])
+def test_prefill_zero_query_averages_the_projected_prefix(prefix, C):
+    """q = 0: query i weighs its prefix + i + 1 visible rows equally, so out_v is W_UV
+    applied to their mean latent and lse = ln(prefix + i + 1) (closed form)."""
+    L = prefix + C
+    d = _random_case(1, 2, [L], seed=50)
+    rng = np.random.default_rng(51)
+    w_uk = rng.standard_normal((2, 128, 512)) * 0.05
+    w_uv = rng.standard_normal((2, 128, 512)) * 0.05
+    out, lse = oracle.prefill_expanded(np.zeros((C, 2, 128)), np.zeros((C, 2, 64)),
+                                       d["kv_cache"], d["block_table"][0], prefix, w_uk, w_uv,
+                                       d["scale"])
+    rows = np.stack([widen(d["kv_cache"][d["block_table"][0, j // 64], j % 64, :512])
+                     for j in range(L)])
+    for i in range(C):
+        n = prefix + i + 1
+        np.testing.assert_allclose(out[i, 1], w_uv[1] @ rows[:n].mean(axis=0), rtol=1e-11,
+                                   atol=1e-13)
+        assert lse[i, 0] == pytest.approx(math.log(n), abs=1e-13)
+
+
+def test_prefill_expanded_equals_absorbed_per_query():
+    """Each query of the chunk, expanded (K, V projected per head), equals the absorbed form
+    (W_UK folded into the query, W_UV applied to the latent output) over its causal prefix."""
+    prefix, C, H = 90, 6, 3
+    d = _random_case(1, H, [prefix + C], seed=52)
+    rng = np.random.default_rng(53)
+    q_nope = rng.standard_normal((C, H, 128))
+    q_rope = rng.standard_normal((C, H, 64))
+    w_uk = rng.standard_normal((H, 128, 512)) * 0.05
+    w_uv = rng.standard_normal((H, 128, 512)) * 0.05
+    out, lse = oracle.prefill_expanded(q_nope, q_rope, d["kv_cache"], d["block_table"][0],
+                                       prefix, w_uk, w_uv, d["scale"])
+    for i in range(C):
+        q_lat = np.einsum("hdc,hd->hc", w_uk, q_nope[i])[None]
+        o_lat, l_a = oracle.decode_absorbed(q_lat, q_rope[i][None], d["kv_cache"],
+                                            d["block_table"], [prefix + i + 1], d["scale"])
+        np.testing.assert_allclose(lse[i], l_a[0], rtol=1e-12)
+        np.testing.assert_allclose(out[i], np.einsum("hdc,hc->hd", w_uv, o_lat[0]), rtol=1e-10,
+                                   atol=1e-12)
+
+
+def test_prefill_query_never_sees_later_rows():
+    prefix, C, H = 40, 4, 2
+    d = _random_case(1, H, [prefix + C], seed=54)
+    rng = np.random.default_rng(55)
+    q_nope = rng.standard_normal((C, H, 128))
+    q_rope = rng.standard_normal((C, H, 64))
+    w_uk = rng.standard_normal((H, 128, 512)) * 0.05
+    w_uv = rng.standard_normal((H, 128, 512)) * 0.05
+    bt = d["block_table"][0]
+    out, lse = oracle.prefill_expanded(q_nope, q_rope, d["kv_cache"], bt, prefix, w_uk, w_uv,
+                                       d["scale"])
+    cache = d["kv_cache"].copy()
+    j = prefix + C - 1  # the chunk's last row: only the last query sees it
+    cache[bt[j // 64], j % 64, :] = bf16(rng.standard_normal(576) * 4)
+    out2, lse2 = oracle.prefill_expanded(q_nope, q_rope, cache, bt, prefix, w_uk, w_uv, d["scale"])
+    np.testing.assert_array_equal(out2[:C - 1], out[:C - 1])
+    np.testing.assert_array_equal(lse2[:C - 1], lse[:C - 1])
+    assert not np.allclose(out2[C - 1], out[C - 1])
