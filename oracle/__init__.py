@@ -220,14 +220,38 @@ def prefill_expanded(q_nope, q_rope, kv_cache, block_table_row, prefix, w_uk, w_
     from the memory wall to the compute wall" §2.2: prefill is compute-bound, so the keys
     and values are projected back per head instead of absorbing the projections into the
     query). The chunk's C tokens sit at positions prefix .. prefix + C - 1 of the cache
-    (already appended); query i attends causally to the positions j <= prefix + i, i.e. it
-    is the expanded decode of a sequence of length prefix + i + 1.
+    (already appended); query i attends causally to the positions j <= prefix + i:
+      k_nope_j = W_UK[h] c_kv_j,  v_j = W_UV[h] c_kv_j,  s_j = scale (q_nope . k_nope_j +
+      q_rope . k_rope_j),  out = sum_j softmax(s)_j v_j,  lse = ln sum_j exp(s_j),
+    in fp64 from the bf16 inputs, each latent row projected once (numpy matmuls).
     q_nope [C,H,d_h], q_rope [C,H,d_r] -> (out_v [C,H,d_v], lse [C,H])."""
-    q_nope, q_rope = _f64(q_nope), _f64(q_rope)
-    C = q_nope.shape[0]
-    bt = np.repeat(_i32(block_table_row).reshape(1, -1), C, axis=0)
-    lengths = (int(prefix) + 1 + np.arange(C)).astype(np.int32)
-    return decode_expanded(q_nope, q_rope, kv_cache, bt, lengths, w_uk, w_uv, scale)
+    q_nope, q_rope, w_uk, w_uv = _f64(q_nope), _f64(q_rope), _f64(w_uk), _f64(w_uv)
+    C, H, _ = q_nope.shape
+    bt = _i32(block_table_row).reshape(-1)
+    cache = _u16(kv_cache)
+    nb, bs, D = cache.shape
+    d_c = w_uk.shape[2]
+    T = int(prefix) + C
+    blk = bt[np.arange(T) // bs]
+    if np.any(blk < 0) or np.any(blk >= nb):
+        raise ValueError("block id out of range")
+    bits = cache[blk, np.arange(T) % bs].astype(np.uint32) << 16
+    rows = bits.view(np.float32).astype(np.float64)          # [T][D], exact bf16 values
+    ckv, kr = rows[:, :d_c], rows[:, d_c:]
+    k_nope = np.einsum("hdc,tc->htd", w_uk, ckv)              # [H][T][d_h]
+    v = np.einsum("hdc,tc->htd", w_uv, ckv)                   # [H][T][d_v]
+    out = np.zeros((C, H, w_uv.shape[1]))
+    lse = np.zeros((C, H))
+    for i in range(C):
+        n = int(prefix) + i + 1
+        for h in range(H):
+            s = scale * (k_nope[h, :n] @ q_nope[i, h] + kr[:n] @ q_rope[i, h])
+            mx = s.max()
+            e = np.exp(s - mx)
+            den = e.sum()
+            out[i, h] = (e / den) @ v[h, :n]
+            lse[i, h] = mx + np.log(den)
+    return out, lse
 
 
 def combine(o_part, lse_part):
