@@ -167,6 +167,31 @@ mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *
                                      mla_stream_t stream);
 
 /*
+ * "LLM inference: from the memory wall to the compute wall" §2.2: chunked prefill of one
+ * sequence in the expanded (un-absorbed) form. The chunk's tokens must already be in the
+ * cache, at positions prefix .. prefix + chunk - 1 (mla_append_kv); the cached latent rows of
+ * positions 0 .. prefix + chunk - 1 are projected back per head,
+ *   k_nope_j = W_UK[h] c_kv_j (128),  v_j = W_UV[h] c_kv_j (128),  k_rope_j shared,
+ * (kept bf16), and query i of the chunk attends causally to the positions j <= prefix + i:
+ *   s_j = scale * (q_nope[i][h] . k_nope_j + q_rope[i][h] . k_rope_j),
+ *   out[i][h] = sum_j softmax(s)_j v_j,  lse[i][h] = ln sum_j exp(s_j).
+ * q_nope [chunk][H][128], q_rope [chunk][H][64] bf16 (rotated at their positions);
+ * block_table [max_blocks] int32 of this sequence (ids checked on the device);
+ * w_uk, w_uv [H][128][512] bf16; out [chunk][H][128] bf16, lse [chunk][H] fp32.
+ * H must be 16, 32, 64 or 128; prefix >= 0, chunk >= 1, prefix + chunk <= 64 * max_blocks.
+ * Workspace: mla_prefill_workspace_size(H, prefix, chunk) (it holds the projected K and V:
+ * about 512 * H bytes per position).
+ */
+mla_status_t mla_prefill_workspace_size(int H, int prefix, int chunk, size_t *bytes);
+mla_status_t mla_prefill_attention(const mla_bf16_t *q_nope, const mla_bf16_t *q_rope,
+                                   const mla_bf16_t *kv_cache, int num_blocks,
+                                   const int32_t *block_table, int max_blocks, int prefix,
+                                   int chunk, int H, const mla_bf16_t *w_uk,
+                                   const mla_bf16_t *w_uv, float scale, void *workspace,
+                                   size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                   mla_stream_t stream);
+
+/*
  * Failure-detection self-test (no counterpart on the pages: a check of this library).
  * Launches one CTA that waits, with the bounded mbarrier wait every kernel of the library
  * uses, on a barrier that nothing completes; after limit_us microseconds (1..1000000) the

@@ -306,6 +306,76 @@ mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *
                       s_q, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
 }
 
+// ------------------------------------------------------------- prefill
+
+namespace {
+struct PrefillLayout {
+    size_t ckv, kr, kn, v, total;
+};
+PrefillLayout prefill_layout(int H, int T) {
+    PrefillLayout L{};
+    L.ckv = HDR;
+    L.kr = L.ckv + align256((size_t)T * D_C * 2);
+    L.kn = L.kr + align256((size_t)T * D_ROPE * 2);
+    L.v = L.kn + align256((size_t)T * H * D_NOPE * 2);
+    L.total = L.v + align256((size_t)T * H * D_V * 2);
+    return L;
+}
+}  // namespace
+
+mla_status_t mla_prefill_workspace_size(int H, int prefix, int chunk, size_t *bytes) {
+    if (!bytes || prefix < 0 || chunk < 1 || (long)prefix + chunk > (1L << 24))
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    *bytes = prefill_layout(H, prefix + chunk).total;
+    return MLA_OK;
+}
+
+mla_status_t mla_prefill_attention(const mla_bf16_t *q_nope, const mla_bf16_t *q_rope,
+                                   const mla_bf16_t *kv_cache, int num_blocks,
+                                   const int32_t *block_table, int max_blocks, int prefix,
+                                   int chunk, int H, const mla_bf16_t *w_uk,
+                                   const mla_bf16_t *w_uv, float scale, void *workspace,
+                                   size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                   mla_stream_t stream) {
+    if (!q_nope || !q_rope || !kv_cache || !block_table || !w_uk || !w_uv || !workspace || !out ||
+        !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (num_blocks < 1 || max_blocks < 1 || prefix < 0 || chunk < 1 ||
+        (long)prefix + chunk > (long)max_blocks * BLOCK || !(scale > 0.f) || !isfinite(scale))
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(q_nope, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||
+        !aligned(w_uk, 16) || !aligned(w_uv, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    const int T = prefix + chunk;
+    const PrefillLayout lay = prefill_layout(H, T);
+    if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE;
+    char *w = static_cast<char *>(workspace);
+    uint16_t *ckv = reinterpret_cast<uint16_t *>(w + lay.ckv);
+    uint16_t *kr = reinterpret_cast<uint16_t *>(w + lay.kr);
+    uint16_t *kn = reinterpret_cast<uint16_t *>(w + lay.kn);
+    uint16_t *v = reinterpret_cast<uint16_t *>(w + lay.v);
+    uint32_t *err = err_word(workspace);
+    cudaStream_t st = S(stream);
+    // the sequence's latent rows, then K_nope = c_kv W_UK^T and V = c_kv W_UV^T per head
+    if (launch_gather_rows(kv_cache, num_blocks, block_table, max_blocks, T, ckv, kr, err, st) !=
+        cudaSuccess)
+        return MLA_ERR_CUDA;
+    for (int k = 0; k < 2; ++k) {
+        GemmParams g{};
+        g.A = ckv; g.lda = D_C; g.a_bstride = 0;
+        g.B = k == 0 ? w_uk : w_uv; g.ldb = D_C; g.b_bstride = 0;
+        g.M = T; g.N = H * (k == 0 ? D_NOPE : D_V); g.K = D_C; g.batch = 1;
+        g.k_splits = 1; g.k_per_split = D_C;
+        g.c_bf16 = k == 0 ? kn : v; g.ldc = g.N; g.c_bstride = 0;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    return cuda_status(launch_prefill_tc(q_nope, q_rope, kn, kr, v, chunk, T, H, prefix, scale,
+                                         out, lse, err, st));
+}
+
 mla_status_t mla_selftest_wait_timeout(unsigned limit_us, void *workspace, size_t ws_bytes,
                                        mla_stream_t stream) {
     if (limit_us < 1 || limit_us > 1000000 || !workspace || ws_bytes < MLA_WS_HEADER_BYTES ||

@@ -80,6 +80,16 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, in
 
 int device_sm_count();
 
+// Chunked prefill: gather one sequence's first T cache rows contiguous (c_kv, k_rope), then
+// causal attention of the C chunk queries in the expanded form.
+cudaError_t launch_gather_rows(const uint16_t *cache, int num_blocks, const int32_t *block_table,
+                               int max_blocks, int T, uint16_t *ckv, uint16_t *kr, uint32_t *err,
+                               cudaStream_t stream);
+cudaError_t launch_prefill_tc(const uint16_t *q_nope, const uint16_t *q_rope,
+                              const uint16_t *k_nope, const uint16_t *k_rope, const uint16_t *v,
+                              int C, int T, int H, int prefix, float scale, uint16_t *out,
+                              float *lse, uint32_t *err, cudaStream_t stream);
+
 // One CTA waits on a barrier nothing completes; records MLA_ERR_TIMEOUT after limit_ns.
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t *err, cudaStream_t stream);
 

@@ -63,6 +63,9 @@ _SIGS = {
     "mla_out_absorb": ([_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "mla_clear_device_status": ([_vp, _vp], _i),
     "mla_selftest_wait_timeout": ([ctypes.c_uint, _vp, _sz, _vp], _i),
+    "mla_prefill_workspace_size": ([_i, _i, _i, _szp], _i),
+    "mla_prefill_attention": ([_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _f, _vp, _sz,
+                               _vp, _vp, _vp], _i),
     "mla_check_device_status": ([_vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -280,6 +283,33 @@ def out_absorb(o_lat, w_uv, w_o, y=None, workspace=None, stream=None):
 def check_device_status(workspace, stream=None) -> int:
     """Synchronise and return (and clear) the workspace's device error word."""
     return int(_lib.mla_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def prefill_workspace_size(H, prefix, chunk):
+    return _size("mla_prefill_workspace_size", H, prefix, chunk)
+
+
+def prefill_attention(q_nope, q_rope, kv_cache, block_table_row, prefix, w_uk, w_uv, scale,
+                      out=None, lse=None, workspace=None, stream=None):
+    """mla_prefill_attention: q_nope [C,H,128], q_rope [C,H,64] of one sequence's chunk at
+    positions prefix.. (already appended). Returns (out [C,H,128] bf16, lse [C,H] fp32,
+    workspace)."""
+    C, H, _ = q_nope.shape
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((C, H, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((C, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prefill_workspace_size(H, prefix, C), stream=stream)
+    rc = _lib.mla_prefill_attention(_ptr(_bits(q_nope)), _ptr(_bits(q_rope)),
+                                    _ptr(_bits(kv_cache)), kv_cache.shape[0],
+                                    _ptr(block_table_row), block_table_row.numel(), int(prefix),
+                                    C, H, _ptr(_bits(w_uk)), _ptr(_bits(w_uv)), float(scale),
+                                    _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                                    _stream(stream))
+    _ok(rc, "mla_prefill_attention")
+    return out, lse, workspace
 
 
 def selftest_wait_timeout(limit_us, workspace, stream=None):

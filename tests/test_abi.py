@@ -107,3 +107,12 @@ def test_selftest_validation_before_launch(lib):
     lib.mla_selftest_wait_timeout.restype = ctypes.c_int
     assert lib.mla_selftest_wait_timeout(ctypes.c_uint(0), null, ctypes.c_size_t(256), null) == 1
     assert lib.mla_selftest_wait_timeout(ctypes.c_uint(100), null, ctypes.c_size_t(256), null) == 1
+
+
+def test_prefill_validation_before_launch(lib):
+    from mla_latent_kv_13_gb300 import mla
+    assert mla.prefill_workspace_size(128, 0, 4096) > 4096 * 128 * 256 * 2
+    sz = ctypes.c_size_t(0)
+    assert lib.mla_prefill_workspace_size(48, 0, 64, ctypes.byref(sz)) == 2
+    assert lib.mla_prefill_workspace_size(16, -1, 64, ctypes.byref(sz)) == 1
+    assert lib.mla_prefill_workspace_size(16, 0, 0, ctypes.byref(sz)) == 1
