@@ -459,6 +459,78 @@ def run_gpu_attention(args, w, metric, unit):
     print(json.dumps(line), flush=True)
 
 
+def run_gpu_prefill(args):
+    """Chunked prefill of one sequence (expanded form): 128 heads, a 4096-token chunk after a
+    4096-token prefix, timed through mla_prefill_attention (row gather, the two per-head
+    up-projections and the causal attention) against the bf16 tensor peak."""
+    import torch
+    world, rank, local = _dist_init()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_kv_13_gb300 import mla, synth
+    H, prefix, C = 128, 4096, 4096
+    T = prefix + C
+    d = synth.make_attention_inputs(synth.Workload("prefill", 1, H, (T,), None, True), seed=0)
+    rng = np.random.default_rng(1)
+
+    def dbf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def rnd(shape, sigma):
+        return dbf(synth.f32_to_bf16_bits((rng.standard_normal(shape) * sigma).astype(np.float32)))
+
+    qn, qr = rnd((C, H, 128), 1.0), rnd((C, H, 64), 1.0)
+    w_uk, w_uv = rnd((H, 128, 512), 0.02), rnd((H, 128, 512), 0.02)
+    cache = dbf(d["kv_cache"])
+    bt = torch.from_numpy(d["block_table"][0]).to(dev)
+    ws = mla.alloc_workspace(mla.prefill_workspace_size(H, prefix, C))
+    out = torch.empty((C, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((C, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        mla.prefill_attention(qn, qr, cache, bt, prefix, w_uk, w_uv, d["scale"], out, lse, ws)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if mla.check_device_status(ws) != 0:
+        raise RuntimeError("device error in the timed region")
+    t_ms = _max_over_ranks(start.elapsed_time(end), world, dev)
+    if rank != 0:
+        return
+    peaks = _measured_peaks()
+    ms = t_ms / args.steps
+    visible = sum(prefix + i + 1 for i in range(C))
+    attn_flops = 2 * H * (192 + 128) * visible
+    proj_flops = 2 * 2 * T * 512 * H * 128
+    flops = attn_flops + proj_flops
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "MLA chunked prefill (expanded form): TFLOP/s on 1 GB300", "value": tf * world,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "prefill", "heads": H, "prefix": prefix, "chunk": C,
+                       "d_c": 512, "d_nope": 128, "d_rope": 64, "d_v": 128,
+                       "l2": "inputs larger than L2 (537 MB of projected K/V)"},
+            "tokens_per_s": C / (ms * 1e-3),
+            "roofline": {"kernel": "prefill_attention", "bound": "tensor", "achieved": tf,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": peaks["source"] + " (cuBLAS bf16 burst)",
+                         "flops_per_launch": flops, "attention_flops": attn_flops},
+            "gpu_launches": args.steps * 4}
+    print(json.dumps(line), flush=True)
+
+
 def step_launches(step) -> int:
     """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1-3 (the library's
     own plan: + merge, + schedule), out 3."""
@@ -490,7 +562,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["step", "tiny", "v3", "mixed", "long", "mtp"],
+                    choices=["step", "tiny", "v3", "mixed", "long", "mtp", "prefill"],
                     help="step = the full decode step (default); the others time decode "
                          "attention alone on that attention workload")
     ap.add_argument("--cpu-sample", type=int, default=32)
@@ -506,7 +578,10 @@ def main():
     if args.workload != "step":
         if args.impl == "reference":
             raise SystemExit("--impl reference is defined on the full-step workload")
-        run_gpu_attention(args, synth.WORKLOADS[args.workload], metric, "GB/s")
+        if args.workload == "prefill":
+            run_gpu_prefill(args)
+        else:
+            run_gpu_attention(args, synth.WORKLOADS[args.workload], metric, "GB/s")
         return
     w = synth.WORKLOADS[WORKLOAD]
     d = synth.make_step_inputs(w, seed=0)

@@ -28,7 +28,7 @@ bool heads_ok(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
 // one CTA per SM): minimise waves x (k-blocks per range + a fixed per-CTA cost of about
 // three k-blocks for filling and draining its pipeline).
 void plan_ksplit(int M, int N, int K, int batch, int &splits, int &per) {
-    const int bn = gemm_block_n(N, K);
+    const int bn = gemm_block_n(M, N, K);
     const long tiles = (long)((N + bn - 1) / bn) * ((M + 127) / 128) * batch;
     const int slots = device_sm_count();
     const int kblocks = K / 64;

@@ -266,6 +266,10 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
 // wide products (the output projection); shorter ones do better with a deeper ring and
 // fewer k-splits at width 128 (measured).
 int gemm_block_n(int N, int K) { return (N >= 4096 && K >= 4096 && N % 256 == 0) ? 256 : 128; }
+int gemm_block_n(int M, int N, int K) {
+    // many row tiles (prefill up-projections): fewer, longer-lived CTAs at width 256
+    return (M >= 1024 && N >= 4096 && N % 256 == 0) ? 256 : gemm_block_n(N, K);
+}
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column
 // offset batch * a_bx; B is [rows_b][ldb] with every batch's slice at row offset
@@ -281,7 +285,7 @@ cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, ui
     CUtensorMap ma, mb;
     if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM))
         return cudaErrorInvalidValue;
-    const int bn = gemm_block_n(p.N, p.K);
+    const int bn = gemm_block_n(p.M, p.N, p.K);
     g.b_bx = 0;
     g.b_by = static_cast<int>(p.b_bstride / p.ldb);
     if (!nn) {

@@ -21,6 +21,7 @@ struct GemmParams {
 // tcgen05/TMA GEMM (one 128 x gemm_block_n(N, K) tile per CTA); err = workspace error word
 cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, uint32_t *err);
 int gemm_block_n(int N, int K);  // output-tile width the GEMM uses (128 or 256)
+int gemm_block_n(int M, int N, int K);
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
                                long ldc, long c_bstride, cudaStream_t stream);
 

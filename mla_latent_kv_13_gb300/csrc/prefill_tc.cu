@@ -10,7 +10,9 @@
 // and V [128 keys x 128] tiles stream through two shared-memory stages:
 //   S  = Q . K^T   (M = 128 queries, N = 128 keys, K = 192; A and B from shared memory)
 //   O += P . V     (M = 128, N = 128, K = 128 keys; A = P from TMEM, B = V, MN-major)
-// with the online softmax (exp2 domain, lazy rescale as in decode) between them.
+// with the online softmax (exp2 domain, lazy rescale as in decode) between them. S is
+// double-buffered in TMEM, so the scores of tile t+1 are computed while the softmax works
+// on tile t.
 // Roles (192 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-5 softmax/output
 // (thread = query row = TMEM lane). Every wait is bounded (one second).
 #include "common.cuh"
@@ -39,8 +41,8 @@ constexpr int SMEM_TOTAL = MISC_OFF + 64 + 1024;
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                 // O: fp32 [0, 128)
-constexpr uint32_t TM_S = 128;               // S: fp32 [128, 256)
-constexpr uint32_t TM_P = 256;               // P: bf16 pairs [256, 320)
+constexpr uint32_t TM_S = 128;               // S: fp32 [128, 256) and [256, 384)
+constexpr uint32_t TM_P = 384;               // P: bf16 pairs [384, 448)
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr float TAU = 8.0f;
 
@@ -84,8 +86,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto kv_full = [&](int s) { return bar + 8u * s; };
     auto kv_empty = [&](int s) { return bar + 8u * (NSTG + s); };
     const uint32_t q_full = bar + 8u * (2 * NSTG);
-    const uint32_t s_full = q_full + 8, s_free = q_full + 16, p_full = q_full + 24;
-    const uint32_t pv_done = q_full + 32, mma_drain = q_full + 40;
+    const uint32_t p_full = q_full + 8, pv_done = q_full + 16, mma_drain = q_full + 24;
+    // S buffer x (tiles t with t % 2 == x): computed / read out by the softmax
+    auto s_full = [&](int x) { return q_full + 32 + 8u * x; };
+    auto s_free = [&](int x) { return q_full + 48 + 8u * x; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
@@ -95,8 +99,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(kv_empty(s), 1);
         }
         mbar_init(q_full, 1);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_free(x), 4);
+        }
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
         mbar_init(mma_drain, 1);
@@ -150,17 +156,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint64_t t_last = globaltimer_ns();
             uint32_t spins = 0;
             while (ok && pv_next < nkt) {
+                // S(t) into buffer t % 2 once the softmax has read tile t-2 out of it
                 if (s_next < nkt && mbar_test(kv_full(s_next % NSTG), (s_next / NSTG) & 1) &&
-                    (s_next == 0 || mbar_test(s_free, (s_next - 1) & 1))) {
+                    (s_next < 2 || mbar_test(s_free(s_next & 1), ((s_next >> 1) - 1) & 1))) {
                     tc_fence_after();
                     const uint32_t st = sb + STG_OFF + (s_next % NSTG) * STG;
+                    const uint32_t ts = tmem + TM_S + 128 * (s_next & 1);
                     for (int c = 0; c < K_CH; ++c)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(tmem + TM_S, sdesc_sw128(sb + Q_OFF + c * CH + kk * 32, 16, 1024),
+                            tc_mma(ts, sdesc_sw128(sb + Q_OFF + c * CH + kk * 32, 16, 1024),
                                    sdesc_sw128(st + c * CH + kk * 32, 16, 1024), IDESC_S,
                                    (c | kk) != 0);
-                    tc_commit(s_full);
+                    tc_commit(s_full(s_next & 1));
                     ++s_next;
                     t_last = globaltimer_ns();
                     continue;
@@ -205,16 +213,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
         };
         for (int t = 0; ok && t < nkt; ++t) {
-            if (!(ok = wait_w(s_full, t & 1))) break;
+            if (!(ok = wait_w(s_full(t & 1), (t >> 1) & 1))) break;
             tc_fence_after();
             uint32_t raw_s[128];
+            const uint32_t ts = tl + TM_S + 128 * (t & 1);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                tmem_ld32(tl + TM_S + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&raw_s[32 * c]));
+                tmem_ld32(ts + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&raw_s[32 * c]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(s_free(t & 1));
             const int vis = min(KT, max(0, limit - t * KT + 1));  // visible keys of the tile
             float mx = -INFINITY;
 #pragma unroll
