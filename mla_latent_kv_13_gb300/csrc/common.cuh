@@ -1,6 +1,8 @@
 // common.cuh -- small device helpers shared by the libmla kernels (sm_103a).
 #pragma once
 
+#include <utility>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -42,6 +44,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Programmatic dependent launch. Every kernel of the library is launched with
+// launch_pdl, so it may start while its predecessor in the stream is still running: its
+// prologue (barriers, TMEM, tensor-map and weight prefetch) overlaps the predecessor's tail.
+// It calls grid_dependency_wait() before it reads anything a predecessor wrote (or writes
+// anything a predecessor may still read), and grid_launch_dependents() once its successor may
+// start -- in kernels that allocate TMEM only after the allocation, so that a successor CTA
+// can never hold columns a not yet started CTA of this kernel needs.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -135,28 +135,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
-    // ---- work: one (sequence, token range) per cluster, or, with the balanced
-    // schedule, the segments of this cluster's equal share of the concatenated tiles
-    const bool sched = p.tile_start != nullptr;
-    const int cl = blockIdx.x >> 1;
-    int P = gridDim.x >> 1;
-    long T = 0, r0 = 0, r1 = 0;
-    int seg_b = 0;
-    if (sched) {
-        T = p.tile_start[p.B];
-        if (T < P) P = static_cast<int>(T);  // as in the schedule: no empty ranges
-        if (cl < P) {
-            r0 = (cl * T) / P;
-            r1 = ((cl + 1) * T) / P;
-        }
-        int lo = 0, hi = p.B - 1;  // largest b with tile_start[b] <= r0
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.tile_start[mid] <= r0) lo = mid;
-            else hi = mid - 1;
-        }
-        seg_b = lo;
-    }
     auto init_barriers = [&]() {
         for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
@@ -185,6 +163,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     cluster_sync();  // the peer's barriers exist before any remote operation
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_launch_dependents();
+    grid_dependency_wait();  // q, the cache rows and the schedule come from predecessor kernels
+
+    // ---- work: one (sequence, token range) per cluster, or, with the balanced
+    // schedule, the segments of this cluster's equal share of the concatenated tiles
+    const bool sched = p.tile_start != nullptr;
+    const int cl = blockIdx.x >> 1;
+    int P = gridDim.x >> 1;
+    long T = 0, r0 = 0, r1 = 0;
+    int seg_b = 0;
+    if (sched) {
+        T = p.tile_start[p.B];
+        if (T < P) P = static_cast<int>(T);  // as in the schedule: no empty ranges
+        if (cl < P) {
+            r0 = (cl * T) / P;
+            r1 = ((cl + 1) * T) / P;
+        }
+        int lo = 0, hi = p.B - 1;  // largest b with tile_start[b] <= r0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.tile_start[mid] <= r0) lo = mid;
+            else hi = mid - 1;
+        }
+        seg_b = lo;
+    }
 
     for (int seg = 0;; ++seg) {
     // -------- this segment: sequence b, tiles [t_begin, t_end), output slot
@@ -646,8 +649,7 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t s
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * clusters);
-    decode_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mkv, p);
-    return cudaGetLastError();
+    return launch_pdl(decode_tc_kernel, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mkv, p);
 }
 
 }  // namespace mla

@@ -14,6 +14,8 @@ namespace {
 __global__ void __launch_bounds__(288) append_finalize_kernel(
     const float *part, int S, int B, const int32_t *pos, const int32_t *block_table,
     int max_blocks, uint16_t *cache, int num_blocks, RopeFreqs freqs, uint32_t *err) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int b = blockIdx.x, t = threadIdx.x;
     const int p = pos[b];
     if (p < 0 || p >= max_blocks * BLOCK) {
@@ -46,6 +48,8 @@ __global__ void __launch_bounds__(256) qrope_finalize_kernel(const float *part, 
                                                              int H, const int32_t *pos,
                                                              RopeFreqs freqs, uint16_t *q_rope) {
     __shared__ float cs[D_ROPE / 2], sn[D_ROPE / 2];
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int b = blockIdx.x;
     if (threadIdx.x < D_ROPE / 2)
         rope_cos_sin(pos[b], freqs.f[threadIdx.x], cs[threadIdx.x], sn[threadIdx.x]);
@@ -80,16 +84,15 @@ cudaError_t launch_append_finalize(const float *part, int S, int B, const int32_
                                    const int32_t *block_table, int max_blocks, uint16_t *cache,
                                    int num_blocks, float theta, uint32_t *err,
                                    cudaStream_t stream) {
-    append_finalize_kernel<<<B, 288, 0, stream>>>(part, S, B, pos, block_table, max_blocks, cache,
-                                                  num_blocks, make_freqs(theta), err);
-    return cudaGetLastError();
+    return launch_pdl(append_finalize_kernel, dim3(B), dim3(288), 0, stream, part, S, B, pos,
+                      block_table, max_blocks, cache, num_blocks, make_freqs(theta), err);
 }
 
 cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const int32_t *pos,
                                   float theta, uint16_t *q_rope, cudaStream_t stream) {
     const dim3 grid(B, (H * (D_ROPE / 2) + 255) / 256);
-    qrope_finalize_kernel<<<grid, 256, 0, stream>>>(part, S, B, H, pos, make_freqs(theta), q_rope);
-    return cudaGetLastError();
+    return launch_pdl(qrope_finalize_kernel, grid, dim3(256), 0, stream, part, S, B, H, pos,
+                      make_freqs(theta), q_rope);
 }
 
 }  // namespace mla

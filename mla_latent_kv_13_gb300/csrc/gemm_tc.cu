@@ -111,9 +111,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
+            // the weights (B) never come from a predecessor kernel: their first tiles head for
+            // L2 while the predecessor finishes; the activations (A) only after it has
+            for (int kb = 0; kb < min(nkb, ns); ++kb) {
+                const int k = k_begin + kb * BK;
+                if (!NN) {
+                    tma_prefetch_l2_2d(&map_b, batch * g.b_bx + k, batch * g.b_by + n0);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_prefetch_l2_2d(&map_b, n0 + 64 * j, batch * g.b_by + k);
+                }
+            }
+            grid_dependency_wait();
             int issued = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % ns;
@@ -256,8 +270,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    gemm_tc_kernel<NN, BN><<<grid, NTHREADS, smem, stream>>>(ma, mb, g);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tc_kernel<NN, BN>, grid, dim3(NTHREADS), smem, stream, ma, mb, g);
 }
 
 }  // namespace

@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_launch_dependents();
+    grid_dependency_wait();  // q, k, v and the gathered rows come from predecessor kernels
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -321,6 +323,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *cache,
                                                           const int32_t *block_table,
                                                           int max_blocks, int T, uint16_t *ckv,
                                                           uint16_t *kr, uint32_t *err) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int j = blockIdx.x;  // position
     const int blk = j / BLOCK < max_blocks ? block_table[j / BLOCK] : -1;
     const bool ok = blk >= 0 && blk < num_blocks;
@@ -383,9 +387,8 @@ bool map_2d_rows(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows)
 cudaError_t launch_gather_rows(const uint16_t *cache, int num_blocks, const int32_t *block_table,
                                int max_blocks, int T, uint16_t *ckv, uint16_t *kr, uint32_t *err,
                                cudaStream_t stream) {
-    gather_rows_kernel<<<T, 96, 0, stream>>>(cache, num_blocks, block_table, max_blocks, T, ckv, kr,
-                                             err);
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(T), dim3(96), 0, stream, cache, num_blocks,
+                      block_table, max_blocks, T, ckv, kr, err);
 }
 
 cudaError_t launch_prefill_tc(const uint16_t *q_nope, const uint16_t *q_rope,
@@ -405,8 +408,8 @@ cudaError_t launch_prefill_tc(const uint16_t *q_nope, const uint16_t *q_rope,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     dim3 grid((C + QT - 1) / QT, H);
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_TOTAL, stream>>>(mqn, mqr, mkn, mkr, mv, a);
-    return cudaGetLastError();
+    return launch_pdl(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mqn, mqr, mkn, mkr,
+                      mv, a);
 }
 
 }  // namespace mla

@@ -10,6 +10,8 @@ namespace {
 // One CTA per (h, b); 128 threads x 4 latent columns.
 __global__ void __launch_bounds__(128) combine_kernel(const float *o_part, const float *lse_part,
                                                       int S, int H, uint16_t *out, float *lse) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int h = blockIdx.x, b = blockIdx.y;
     float m = -INFINITY;
     for (int s = 0; s < S; ++s) m = fmaxf(m, lse_part[((size_t)b * S + s) * H + h]);
@@ -42,6 +44,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *o_part, const
 // Sum k-split partials [S][batch][M][N] into bf16 C (batch stride c_bstride, row ldc).
 __global__ void reduce_partials_bf16(const float *part, int S, int batch, int M, int N,
                                      uint16_t *C, long ldc, long c_bstride) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     long total = (long)batch * M * N / 2;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total;
          i += (long)gridDim.x * blockDim.x) {
@@ -110,6 +114,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
                                                                int32_t *part_begin,
                                                                int32_t *nparts, uint32_t *err) {
     __shared__ int v[4096], ex[4096], warp_tot[33];
+    grid_launch_dependents();
+    grid_dependency_wait();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seqlens[b];
         if (L < 0 || L > max_blocks * BLOCK) {
@@ -146,6 +152,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
 __global__ void __launch_bounds__(128) combine_sched_kernel(
     const float *o_part, const float *lse_part, const int32_t *tile_start,
     const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *lse) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int h = blockIdx.x, b = blockIdx.y;
     const int np = nparts[b];
     const bool empty = tile_start[b + 1] == tile_start[b];
@@ -186,9 +194,8 @@ __global__ void __launch_bounds__(128) combine_sched_kernel(
 cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
                                    int32_t *tile_start, int32_t *part_begin, int32_t *nparts,
                                    uint32_t *err, cudaStream_t stream) {
-    decode_schedule_kernel<<<1, 1024, 0, stream>>>(seqlens, B, max_blocks, P, tile_start,
-                                                   part_begin, nparts, err);
-    return cudaGetLastError();
+    return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
+                      max_blocks, P, tile_start, part_begin, nparts, err);
 }
 
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
@@ -196,16 +203,14 @@ cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
                                  const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
                                  cudaStream_t stream) {
     dim3 grid(H, B);
-    combine_sched_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, tile_start, part_begin,
-                                                   nparts, H, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(combine_sched_kernel, grid, dim3(128), 0, stream, o_part, lse_part,
+                      tile_start, part_begin, nparts, H, out, lse);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                            uint16_t *out, float *lse, cudaStream_t stream) {
     dim3 grid(H, B);
-    combine_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, S, H, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, o_part, lse_part, S, H, out, lse);
 }
 
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
@@ -213,8 +218,8 @@ cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N
     long pairs = (long)batch * M * N / 2;
     long nb = (pairs + 255) / 256;
     int blocks = (int)(nb < 4096 ? nb : 4096);
-    reduce_partials_bf16<<<blocks, 256, 0, stream>>>(part, S, batch, M, N, C, ldc, c_bstride);
-    return cudaGetLastError();
+    return launch_pdl(reduce_partials_bf16, dim3(blocks), dim3(256), 0, stream, part, S, batch, M,
+                      N, C, ldc, c_bstride);
 }
 
 }  // namespace mla
