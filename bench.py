@@ -51,7 +51,9 @@ def _measured_peaks():
 
 
 def step_costs(d):
-    """Algorithmic bytes and flops of one full step (see the design doc for the derivation)."""
+    """Algorithmic bytes and flops of one full step: every weight read once, every cached row
+    read once, the step's activations in and out; flops 2 per weight and batch row for the
+    projections, 2 x H x (576 + 512) per cached token for attention."""
     B, H, dm, ql = d["B"], d["H"], d["d_model"], d["q_lora"]
     L = d["seqlens_after"].astype(np.int64)
     weights = 2 * (576 * dm + ql * dm + H * 128 * ql + H * 64 * ql + H * 128 * 512 * 2 +
