@@ -2,36 +2,37 @@
 // (tcgen05 + TMEM), fed by TMA, one 2-CTA thread-block cluster per work item.
 //
 // Work item = (sequence b, token range s); with the balanced schedule a cluster runs the
-// segments of one equal share of all sequences' tiles in turn. All heads of a sequence score the same
-// latent cache rows [c_kv (512) | k_rope (64)], so the 128 head rows form the M=128
-// side of both products and a 64-token cache tile the N (scores) or K (output) side:
-//   S   = Q [128 x 576] . K^T [576 x 64]      (scores)
-//   O  += P [128 x 64]  . V   [64 x 512]      (latent output, V = c_kv part)
-// The fp32 accumulator O [128 x 512] alone fills a whole SM's tensor memory, so the
-// two CTAs of a cluster split the latent columns: CTA r stages only its columns of
-// each tile -- r = 0: c_kv[0:256); r = 1: c_kv[256:512) and k_rope -- computes the
-// partial scores over them, swaps the 128 x 64 fp32 partial with its peer through
-// distributed shared memory (bulk copies), and both CTAs then run the same softmax on
-// the same full scores (bit-identical, since fp32 addition commutes) and accumulate
-// their own 256 output columns. No cache byte is read twice and no product is
-// computed twice; the only duplicated work is the (cheap) softmax.
+// segments of one equal share of all sequences' tiles in turn. All heads of a sequence
+// score the same latent cache rows [c_kv (512) | k_rope (64)], so the 128 head rows form
+// the M = 128 side of both products:
+//   S   = Q [128 x 576] . K^T [576 x tokens]   (scores)
+//   O  += P [128 x tokens] . V [tokens x 512]  (latent output, V = c_kv part)
+// The fp32 accumulator O [128 x 512] alone would fill a whole SM's tensor memory, so the
+// two CTAs of a cluster split the output columns (CTA r keeps O[:, 256r : 256r+256]) and
+// split each 64-token cache tile by tokens for the scores: CTA r scores tokens
+// [32r, 32r+32) over all 576 columns. Each CTA therefore stages, per tile, its own 32
+// tokens in full (9 chunks of 64 columns) and the peer's 32 tokens in its own 256 output
+// columns (4 chunks); no partial score crosses the cluster. What does cross is the
+// probability half: each CTA turns its 128 x 32 scores into P (bf16) against a running
+// per-row reference, and ships P with (reference, row sum) to the peer through
+// distributed shared memory (9 KB per tile each way); both CTAs then agree on the larger
+// reference (rescaling whichever half was computed against the smaller one -- rare after
+// the first tile, since the reference is only raised when a score exceeds it by more
+// than 2^8) and run P . V over all 64 tokens for their own columns.
 //
-// Roles per CTA (192 threads): warp 0 issues TMA loads (one elected lane); warp 1
-// allocates TMEM and issues tcgen05.mma / tcgen05.commit (one elected lane); warps
-// 2-5 (thread = head row = TMEM lane) load Q into TMEM, combine the two partial
-// scores, run the online softmax in the exp2 domain, write P (bf16) into TMEM and
-// finish the output. The exchange is a ping-pong over two 32 KB buffers per CTA: the
-// peer's partial of tile k lands in buffer (k+1) % 2; once a warp has read its 32 rows
-// of it, it overwrites them with its own partial of tile k+1 and bulk-copies them into
-// the peer's buffer k % 2 -- which the peer emptied before it sent tile k. Arrival of
-// data is the only signal: a buffer is always free by the time a copy targets it. The
-// exchange (64 fp32 per head row per tile, ~20 B/clk of distributed shared memory per
-// SM) thus runs one tile ahead on the copy engine, overlapping the softmax of the
-// current tile, and each warp ships its own rows without waiting for the others.
-// Both products read their A operand (Q, P) from TMEM and their B operand (the
-// cache tile, 128-byte swizzled as TMA wrote it) from shared memory. The running maximum
-// is only raised (and O rescaled in TMEM) when a score exceeds it by more than 2^8,
-// so after the first tile of a sequence O is almost never touched between MMAs.
+// Tensor memory (512 columns): O fp32 [0, 256), S fp32 [256, 288), Q bf16 pairs of
+// column chunks 0..6 [288, 512). Q chunks 7 (c_kv[448:512]) and 8 (k_rope) are read from
+// shared memory. Shared memory: three cache stages of 52 KB, the two Q chunks, and the
+// P halves (double-buffered: the local half doubles as the source of the copy and as
+// the A operand of P . V; the received half is the A operand of the second K half).
+//
+// Roles per CTA (192 threads): warp 0 issues TMA loads (one lane); warp 1 allocates
+// TMEM and issues tcgen05.mma / tcgen05.commit: the whole warp runs the issue loop,
+// polls the barriers with the non-suspending test_wait and one elected lane issues (a
+// tcgen05.mma issued by a lone lane of a diverged warp costs that thread several times
+// the tensor pipe's own time per instruction at these small N); warps 2-5 (thread = head
+// row = TMEM lane) load Q, run the online softmax in the exp2 domain, exchange P and
+// finish the output.
 // Every mbarrier wait is bounded (about one second); a wait that gives up records
 // MLA_ERR_TIMEOUT in the error word and the CTA drains and exits.
 #include "common.cuh"
@@ -45,45 +46,55 @@ namespace {
 using namespace sm100;
 
 #ifndef MLA_DECODE_STAGES
-#define MLA_DECODE_STAGES 4
+#define MLA_DECODE_STAGES 3
 #endif
 
-constexpr int TOK = 64;
-constexpr int NS = MLA_DECODE_STAGES;        // cache-tile stages
-constexpr int KVCH = 64 * 128;               // one tile chunk: 64 tokens x 64 bf16 (8 KB)
-constexpr int MAXCH = 5;                     // rank 1 stages 5 chunks (4 latent + rope)
+constexpr int TOK = 64;                       // tokens per cache tile (one page)
+constexpr int HALF = 32;                      // tokens of a tile scored by each CTA
+constexpr int NS = MLA_DECODE_STAGES;         // cache-tile stages
+constexpr int CH = HALF * 128;                // one chunk: 32 tokens x 64 bf16 (4 KB)
+constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_rope
+constexpr int NPEER = 4;                      // peer tokens: this CTA's 4 output chunks
+constexpr int STAGE = (NOWN + NPEER) * CH;    // 53248
+constexpr int NQT = 7;                        // Q chunks held in TMEM (the rest in smem)
+constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
+constexpr int PBUF = 128 * 64;                // P half: 128 rows x 32 bf16 (8 KB)
+constexpr int PWARP = 32 * 64;                // the 32 rows of one warp (2 KB, contiguous)
+constexpr int MBUF = 128 * 8;                 // (reference, row sum) per row
 constexpr int KV_OFF = 0;
-constexpr int KV_STAGE = MAXCH * KVCH;       // 40960
-constexpr int XROW = 256;                    // exchange row: 64 fp32, 16-byte chunks XOR-swizzled
-constexpr int XQ = 32 * XROW;                // the 32 rows of one warp (8 KB)
-constexpr int XBUF = 4 * XQ;                 // 32768
-constexpr int X_OFF = KV_OFF + NS * KV_STAGE;  // two exchange buffers (ping-pong)
-constexpr int BAR_OFF = X_OFF + 2 * XBUF;
-constexpr int NBAR = 24;
+constexpr int QS_OFF = KV_OFF + NS * STAGE;
+constexpr int SEND_OFF = QS_OFF + 2 * QCH;    // local P half, x2
+constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
+constexpr int SMETA_OFF = RECV_OFF + 2 * PBUF;
+constexpr int RMETA_OFF = SMETA_OFF + 2 * MBUF;
+constexpr int BAR_OFF = RMETA_OFF + 2 * MBUF;
+constexpr int NBAR = 32;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
-constexpr int NTHREADS = 192;                // 6 warps
+constexpr int NTHREADS = 192;                 // 6 warps
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0;                 // O: fp32 columns [0, 256)
-constexpr uint32_t TM_S = 256;               // S: fp32 columns [256, 320)
-constexpr uint32_t TM_Q = 320;               // Q: bf16 pairs, columns [320, 480)
-constexpr uint32_t TM_P = 480;               // P: bf16 pairs, columns [480, 512)
-constexpr uint64_t WAIT_NS = 1000000000ull;  // bounded waits: 1 s
+constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
+constexpr uint32_t TM_S = 256;                // S: fp32 columns [256, 288)
+constexpr uint32_t TM_Q = 288;                // Q chunks 0..6: bf16 pairs, [288, 512)
+constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
-constexpr float TAU = 8.0f;                  // lazy-rescale threshold (log2 units)
-constexpr int PF_DIST = 4;                   // tiles prefetched into L2 beyond the stage ring
+constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
+constexpr int PF_DIST = 4;                    // tiles prefetched into L2 beyond the stage ring
+constexpr uint32_t XBYTES = PWARP + 32 * 8;   // one warp's message: P rows + (reference, sum)
 
-constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false, false);
+constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(X_OFF >= KV_OFF + NS * KV_STAGE && BAR_OFF >= X_OFF + 2 * XBUF &&
-                  MISC_OFF >= BAR_OFF + NBAR * 8,
-              "shared-memory regions must not overlap");
-static_assert(X_OFF % 16 == 0 && XQ % 16 == 0, "bulk-copy alignment");
-static_assert((BAR_OFF % 8) == 0, "mbarrier alignment");
+static_assert(QS_OFF % 1024 == 0 && STAGE % 1024 == 0 && CH % 1024 == 0,
+              "128-byte-swizzled operands need 1024-byte-aligned atoms");
+static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && SMETA_OFF % 16 == 0 &&
+                  RMETA_OFF % 16 == 0,
+              "bulk-copy alignment");
+static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
+static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -91,16 +102,28 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  "r"(d)
                  : "memory");
 }
-__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+// bf16 pair (lo, hi) scaled by f, rounded back to bf16 (round to nearest even)
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float f) {
+    return pack_bf16x2(__uint_as_float(v << 16) * f, __uint_as_float(v & 0xFFFF0000u) * f);
+}
 
-// Wait that ignores the abort flag: used only to drain copies before exit.
+// Wait that ignores the abort flag: used only to drain copies and signals before exit.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (mbar_test(bar, parity)) return;
     uint64_t t0 = globaltimer_ns();
@@ -119,7 +142,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int H = p.H;
-    const int nch = rank == 0 ? 4 : 5;  // 64-column chunks of Q and of each tile owned here
 
     const uint32_t bar = sb + BAR_OFF;
     auto kv_full = [&](int s) { return bar + 8u * s; };
@@ -127,11 +149,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t q_ready = bar + 8u * (2 * NS);
     const uint32_t s_full = q_ready + 8;
     const uint32_t s_free = q_ready + 16;
-    const uint32_t p_full = q_ready + 24;
-    const uint32_t pv_done = q_ready + 32;
-    const uint32_t mma_drain = q_ready + 40;
-    // the peer's partial scores of the rows of warp quadrant q have landed in buffer x
-    auto recv_full = [&](int q, int x) { return q_ready + 48 + 8u * (2 * q + x); };
+    auto p_ready = [&](int x) { return q_ready + 24 + 8u * x; };  // both P halves of tile parity x
+    auto pv_done = [&](int x) { return q_ready + 40 + 8u * x; };  // P.V of tile parity x finished
+    // the peer's P.V of tile parity x finished (its copy of our P half may be overwritten);
+    // arrived on by the peer's tcgen05.commit
+    auto rfree = [&](int x) { return q_ready + 56 + 8u * x; };
+    const uint32_t mma_drain = q_ready + 72;
+    // the peer's P half of the rows of warp quadrant q has landed in buffer x
+    auto recv_full = [&](int q, int x) { return q_ready + 80 + 8u * (2 * q + x); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
@@ -143,8 +168,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mbar_init(q_ready, 4);
         mbar_init(s_full, 1);
         mbar_init(s_free, 4);
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(p_ready(x), 4);
+            mbar_init(pv_done(x), 1);
+            mbar_init(rfree(x), 1);
+        }
         mbar_init(mma_drain, 1);
         for (int k = 0; k < 8; ++k) mbar_init(recv_full(k >> 1, k & 1), 1);
         fence_mbar_init();
@@ -226,14 +254,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
-            // Tiles beyond the shared-memory ring are prefetched into L2, so that a load
-            // issued when a stage frees up is served from L2 rather than from HBM.
+            // Tiles beyond the shared-memory ring are prefetched into L2 (each CTA its own
+            // 32 tokens, all columns), so that a load issued when a stage frees up is
+            // served from L2 rather than from HBM.
             auto prefetch = [&](int t) {
                 if (t >= n) return;
                 const int blk = btab[t_begin + t];
                 if (blk < 0 || blk >= p.num_blocks) return;
-                for (int c = 0; c < nch; ++c)
-                    tma_prefetch_l2_2d(&map_kv, 64 * (4 * rank + c), blk * TOK);
+                for (int d = 0; d < NOWN; ++d)
+                    tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
             };
             for (int t = NS; t < NS + PF_DIST; ++t) prefetch(t);
             int issued = 0;
@@ -241,11 +270,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const int s = i % NS;
                 if (!mbar_wait(kv_empty(s), ((i / NS) & 1) ^ 1, abort_flag, WAIT_NS)) break;
                 const int blk = btab[t_begin + i];
+                const uint32_t st = sb + KV_OFF + s * STAGE;
                 if (blk >= 0 && blk < p.num_blocks) {
-                    mbar_arrive_expect_tx(kv_full(s), nch * KVCH);
-                    for (int c = 0; c < nch; ++c)
-                        tma_load_2d(sb + KV_OFF + s * KV_STAGE + c * KVCH, &map_kv, kv_full(s),
-                                    64 * (4 * rank + c), blk * TOK);
+                    mbar_arrive_expect_tx(kv_full(s), STAGE);
+                    const int y_own = blk * TOK + HALF * rank, y_peer = blk * TOK + HALF * peer;
+                    for (int d = 0; d < NOWN; ++d)
+                        tma_load_2d(st + d * CH, &map_kv, kv_full(s), 64 * d, y_own);
+                    for (int k = 0; k < NPEER; ++k)
+                        tma_load_2d(st + (NOWN + k) * CH, &map_kv, kv_full(s),
+                                    64 * (4 * rank + k), y_peer);
                 } else {
                     if (rank == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
                     mbar_arrive(kv_full(s));  // no data: the consumers mask the tile
@@ -259,61 +292,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA
-        if (lane == 0 && n > 0) {
+        if (n > 0) {
+            const bool leader = elect_one();
+            auto lane0 = [&](bool v) { return __shfl_sync(0xffffffffu, v, 0); };
+            const uint32_t qs = sb + QS_OFF;
+            // scores of this CTA's 32 tokens of tile i over all 576 columns
             auto issue_s = [&](int i) {
-                const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
-                for (int c = 0; c < nch; ++c)
+                const uint32_t own = sb + KV_OFF + (i % NS) * STAGE;
+                for (int d = 0; d < NOWN; ++d)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(tmem + TM_S, tmem + TM_Q + 32 * c + 8 * kk,
-                                  sdesc_sw128(kv + c * KVCH + kk * 32, 16, 1024), IDESC_S,
-                                  (c | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bdesc = sdesc_sw128(own + d * CH + kk * 32, 16, 1024);
+                        if (d < NQT)
+                            tc_mma_ts(tmem + TM_S, tmem + TM_Q + 32 * d + 8 * kk, bdesc, IDESC_S,
+                                      (d | kk) != 0);
+                        else
+                            tc_mma(tmem + TM_S, sdesc_sw128(qs + (d - NQT) * QCH + kk * 32, 16, 1024),
+                                   bdesc, IDESC_S, 1);
+                    }
                 tc_commit(s_full);
             };
-            // Scores of tile k need its cache tile (kv_full) and the S columns back from
-            // the softmax (s_free of tile k-1); the output product of tile i needs P(i)
-            // (p_full). Issue whichever is ready first, so that a tile still in flight
-            // from HBM never holds up the output product of an earlier tile.
-            bool ok = mbar_wait(q_ready, 0, abort_flag, WAIT_NS);
+            // O[:, own columns] += P [128 x 64] . V [64 x 256]: tokens [32h, 32h+32) come from
+            // the local P half and the own-token chunks when h is this CTA's half, else from
+            // the received half and the peer-token chunks
+            auto issue_pv = [&](int i) {
+                const uint32_t st = sb + KV_OFF + (i % NS) * STAGE;
+                const int x = i & 1;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const bool mine = h == static_cast<int>(rank);
+                    const uint32_t a = sb + (mine ? SEND_OFF : RECV_OFF) + x * PBUF;
+                    const uint32_t v = st + (mine ? 4 * rank * CH : NOWN * CH);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc_mma(tmem + TM_O, sdesc_kmajor_plain(a + kk * 256, 128, 512),
+                               sdesc_sw128(v + kk * 2048, CH, 1024), IDESC_PV,
+                               (i > 0 || h > 0 || kk > 0));
+                }
+                tc_commit(kv_empty(i % NS));
+                tc_commit(pv_done(x));
+                tc_commit_multicast(rfree(x), static_cast<uint16_t>(1u << peer));
+            };
+            // Scores of tile k need its cache tile (kv_full) and the S columns back from the
+            // softmax (s_free of tile k-1); the output product of tile i needs both P halves
+            // (p_ready). Issue whichever is ready first.
+            bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, WAIT_NS));
             if (ok) tc_fence_after();
             int s_next = 0, pv_next = 0;
             uint64_t t_last = globaltimer_ns();
             uint32_t spins = 0;
             while (ok && pv_next < n) {
-                if (s_next < n && mbar_test(kv_full(s_next % NS), (s_next / NS) & 1) &&
-                    (s_next == 0 || mbar_test(s_free, (s_next - 1) & 1))) {
+                if (lane0(s_next < n && mbar_poll(kv_full(s_next % NS), (s_next / NS) & 1) &&
+                          (s_next == 0 || mbar_poll(s_free, (s_next - 1) & 1)))) {
                     tc_fence_after();
-                    issue_s(s_next);
+                    if (leader) issue_s(s_next);
+                    __syncwarp();
                     ++s_next;
                     t_last = globaltimer_ns();
                     continue;
                 }
-                if (pv_next < s_next && mbar_test(p_full, pv_next & 1)) {
+                if (lane0(pv_next < s_next && mbar_poll(p_ready(pv_next & 1), (pv_next >> 1) & 1))) {
                     tc_fence_after();
-                    const int i = pv_next;
-                    const uint32_t kv = sb + KV_OFF + (i % NS) * KV_STAGE;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_ts(tmem + TM_O, tmem + TM_P + 8 * kk,
-                                  sdesc_sw128(kv + kk * 2048, KVCH, 1024), IDESC_PV,
-                                  (i > 0 || kk > 0));
-                    tc_commit(kv_empty(i % NS));
-                    tc_commit(pv_done);
+                    if (leader) issue_pv(pv_next);
+                    __syncwarp();
                     ++pv_next;
                     t_last = globaltimer_ns();
                     continue;
                 }
                 if ((++spins & 63) == 0) {
-                    if (*abort_flag) ok = false;
-                    else if (globaltimer_ns() - t_last > WAIT_NS) {
-                        *abort_flag = 1;
-                        ok = false;
+                    bool stop = *abort_flag != 0;
+                    if (!stop && globaltimer_ns() - t_last > WAIT_NS) {
+                        if (lane == 0) *abort_flag = 1;
+                        stop = true;
                     }
+                    ok = !lane0(stop);
                 }
             }
             // every MMA this thread issued has finished before TMEM is released
-            tc_commit(mma_drain);
-            drain_wait(mma_drain, 0);
+            if (leader) {
+                tc_commit(mma_drain);
+                drain_wait(mma_drain, 0);
+            }
         }
         __syncwarp();
     } else {
@@ -324,13 +383,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         // row = (query token t, head): token t of s_q sees the rows j < L - (s_q - 1 - t)
         const int back = live_row ? p.s_q - 1 - row / p.hq : 0;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t xrow = row * XROW;
-        // rows of this warp that hold a head: only those are exchanged (both CTAs agree)
-        const int nlive = min(32, max(0, H - wq * 32));
-        const uint32_t xbytes = static_cast<uint32_t>(nlive) * XROW;
-        const uint32_t xq = sb + X_OFF + wq * XQ;            // + XBUF for buffer 1
-        const uint32_t xq_peer = mapa(xq, peer);
-        const uint32_t recv_peer = mapa(recv_full(wq, 0), peer);  // + 8 for buffer 1
+        // warps with at least one head row exchange their P rows (both CTAs agree)
+        const bool wlive = wq * 32 < H;
+        // this row in a P half: K-major 8 x 16-byte core matrices, no swizzle
+        // (next 8 K elements +128 B, next 8 rows +512 B)
+        const uint32_t prow = (row >> 3) * 512 + (row & 7) * 16;
+        const uint32_t send = sb + SEND_OFF, recv = sb + RECV_OFF;
+        const uint32_t smeta = sb + SMETA_OFF, rmeta = sb + RMETA_OFF;
+        const uint32_t recv_peer = mapa(recv, peer), rmeta_peer = mapa(rmeta, peer);
+        const uint32_t rbar_peer = mapa(recv_full(wq, 0), peer);  // + 8 for buffer 1
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         // waits are warp-uniform: a lane that gives up takes its whole warp with it
@@ -342,113 +403,155 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         };
 
         if (n > 0) {
-            // Q rows of this CTA's columns into TMEM (A operand of the score product):
-            // rank 0: q_lat[0:256); rank 1: q_lat[256:512) and q_rope. Rows >= H are 0.
+            // Q rows: chunks 0..6 into TMEM (A operand of the score product), chunks 7..8
+            // (c_kv columns 448..511 and k_rope) into shared memory, 128-byte swizzled as
+            // the cache tiles are. Rows >= H are 0.
             const uint4 *qsrc =
-                reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + row) * D_C + 256 * rank);
+                reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + row) * D_C);
             const uint4 *rsrc =
                 reinterpret_cast<const uint4 *>(p.q_rope + ((size_t)b * H + row) * D_ROPE);
-            for (int c = 0; c < nch; ++c) {
+            const uint32_t qrow = sb + QS_OFF + (row >> 3) * 1024 + (row & 7) * 128;
+            for (int c = 0; c < NOWN; ++c) {
                 uint32_t r[32];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (live_row) v = c < 4 ? qsrc[8 * c + k] : rsrc[k];
+                    if (live_row) v = c < 8 ? qsrc[8 * c + k] : rsrc[k];
                     r[4 * k] = v.x;
                     r[4 * k + 1] = v.y;
                     r[4 * k + 2] = v.z;
                     r[4 * k + 3] = v.w;
                 }
-                tmem_st32(tl + TM_Q + 32 * c, r);
+                if (c < NQT) {
+                    tmem_st32(tl + TM_Q + 32 * c, r);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(qrow + (c - NQT) * QCH + ((k ^ (row & 7)) << 4), r[4 * k],
+                                     r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                }
             }
             tmem_st_wait();
+            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
         }
 
-        // Read this CTA's partial scores of tile k out of TMEM (releasing the S buffer),
-        // stage this warp's rows of them in buffer k % 2 (the peer's tile k-1 there has
-        // been read) and copy them into the peer's buffer (k+1) % 2.
-        uint32_t own[64];
-        auto stage_partial = [&](int k) -> bool {
-            if (!wait_w(s_full, k & 1)) return false;
-            tc_fence_after();
-            tmem_ld32(tl + TM_S, *reinterpret_cast<uint32_t(*)[32]>(&own[0]));
-            tmem_ld32(tl + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&own[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
-            if (nlive > 0) {
-                const uint32_t buf = (k & 1) * XBUF;
-                const uint32_t dst = sb + X_OFF + buf + xrow;
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    st_shared_v4(dst + ((c ^ (row & 7)) << 4), own[4 * c], own[4 * c + 1],
-                                 own[4 * c + 2], own[4 * c + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t nb = XBUF - buf;  // the peer's buffer (k+1) % 2
-                    bulk_copy_to_peer(xq_peer + nb, xq + buf, xbytes,
-                                      recv_peer + 8u * ((k + 1) & 1));
-                    bulk_commit();
-                }
-            }
-            return true;
-        };
-
-        if (n > 0) ok = stage_partial(0);
         int blk_next = n > 0 ? btab[t_begin] : 0;  // block ids are fetched one tile ahead
         for (int i = 0; ok && i < n; ++i) {
             const int tile = t_begin + i;
             const int blk = blk_next;
             if (i + 1 < n) blk_next = btab[tile + 1];
-            float s[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) s[j] = __uint_as_float(own[j]);
-            // the peer's partial of tile i (buffer (i+1) % 2) -> full scores
-            if (nlive > 0) {
-                const int x = (i + 1) & 1;
-                if (lane == 0) mbar_arrive_expect_tx(recv_full(wq, x), xbytes);
-                if (!(ok = wait_wc(recv_full(wq, x), (i >> 1) & 1))) break;
-                const uint32_t src = sb + X_OFF + x * XBUF + xrow;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float4 v = ld_shared_v4f(src + ((k ^ (row & 7)) << 4));
-                    s[4 * k + 0] += v.x;
-                    s[4 * k + 1] += v.y;
-                    s[4 * k + 2] += v.z;
-                    s[4 * k + 3] += v.w;
-                }
-                __syncwarp();
-            }
-            // then the next tile's partial into the rows just read, so its transfer
-            // overlaps this softmax
-            if (i + 1 < n && !(ok = stage_partial(i + 1))) break;
+            const int x = i & 1;
+            const uint32_t st = sb + KV_OFF + (i % NS) * STAGE;
 
-            // online softmax of tile i on this head row
+            // ---- scores of this CTA's 32 tokens, out of TMEM (releasing S)
+            if (!(ok = wait_w(s_full, i & 1))) break;
+            tc_fence_after();
+            uint32_t sr[32];
+            tmem_ld32(tl + TM_S, sr);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int tvalid = blk_ok ? min(TOK, L - tile * TOK) : 0;  // valid tokens of the tile
-            // columns this row keeps
+            // tokens of the tile this row keeps, and how many of them are this CTA's
             const int valid = live_row ? min(tvalid, max(0, L - back - tile * TOK)) : 0;
-            if (valid < TOK) {
+            const int ov = min(HALF, max(0, valid - HALF * static_cast<int>(rank)));
+            float s[32];
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j >= valid) s[j] = -INFINITY;
-            }
+            for (int j = 0; j < 32; ++j) s[j] = j < ov ? __uint_as_float(sr[j]) : -INFINITY;
             float mx = s[0];
 #pragma unroll
-            for (int j = 1; j < 64; ++j) mx = fmaxf(mx, s[j]);
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, s[j]);
             mx *= p.scale_log2;  // scale > 0: the max of the scaled scores
-            const bool raise = mx > m + TAU;
+            // local reference: raised only when a score exceeds it by more than TAU
+            const float m_new = mx > m + TAU ? mx : m;
+
+            // P (local half) = exp2(scale * s - reference), bf16 pairs
+            auto make_p = [&](float ref, uint32_t (&pk)[16]) {
+                const float nm = ref != -INFINITY ? -ref : 0.f;
+                float es = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = fast_exp2(fmaf(s[2 * j], p.scale_log2, nm));
+                    const float p1 = fast_exp2(fmaf(s[2 * j + 1], p.scale_log2, nm));
+                    pk[j] = pack_bf16x2(p0, p1);
+                    es += p0 + p1;
+                }
+                return ref != -INFINITY ? es : 0.f;
+            };
+            auto put_p = [&](const uint32_t (&pk)[16]) {
+                const uint32_t dst = send + x * PBUF + prow;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    st_shared_v4(dst + k * 128, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                 pk[4 * k + 3]);
+            };
+            uint32_t pk[16];
+            float e_own = make_p(m_new, pk);
+
+            // buffer x (local half) is free once P.V of tile i-2 has read it and its copy
+            // to the peer has been read out
+            if (i >= 2 && !(ok = wait_w(pv_done(x), ((i >> 1) - 1) & 1))) break;
+            float m_peer = -INFINITY, e_peer = 0.f;
+            if (wlive) {
+                if (i >= 2 && lane == 0) bulk_wait_read_but_one();
+                __syncwarp();
+                put_p(pk);
+                st_shared_v2f(smeta + x * MBUF + row * 8, m_new, e_own);
+                fence_proxy_async_smem();
+                // the peer's buffer x is free once its P.V of tile i-2 is done
+                if (i >= 2 && !(ok = wait_wc(rfree(x), ((i >> 1) - 1) & 1))) break;
+                if (lane == 0) {
+                    const uint32_t off = x * PBUF + wq * PWARP, moff = x * MBUF + wq * 256;
+                    bulk_copy_to_peer(recv_peer + off, send + off, PWARP, rbar_peer + 8u * x);
+                    bulk_copy_to_peer(rmeta_peer + moff, smeta + moff, 256, rbar_peer + 8u * x);
+                    bulk_commit();
+                    mbar_arrive_expect_tx(recv_full(wq, x), XBYTES);
+                }
+                // ---- the peer's half of tile i
+                if (!(ok = wait_wc(recv_full(wq, x), (i >> 1) & 1))) break;
+                const float2 pm = ld_shared_v2f(rmeta + x * MBUF + row * 8);
+                m_peer = pm.x;
+                e_peer = pm.y;
+            }
+
+            // ---- common reference: the larger of the two; the half computed against the
+            // smaller one is brought to it (the local half recomputed from the scores, the
+            // received half rescaled)
+            const float m_fin = fmaxf(m_new, m_peer);
+            const bool fix_own = m_new != m_fin, fix_peer = m_peer != m_fin;
+            if (__any_sync(0xffffffffu, fix_own)) {
+                if (lane == 0) bulk_wait_read_all();  // the copy has read the local half
+                __syncwarp();
+                if (fix_own) {
+                    e_own = make_p(m_fin, pk);
+                    put_p(pk);
+                }
+            }
+            if (fix_peer) {
+                const float f = fast_exp2(m_peer - m_fin);
+                const uint32_t src = recv + x * PBUF + prow;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 v = ld_shared_v4(src + k * 128);
+                    st_shared_v4(src + k * 128, scale_bf16x2(v.x, f), scale_bf16x2(v.y, f),
+                                 scale_bf16x2(v.z, f), scale_bf16x2(v.w, f));
+                }
+                e_peer *= f;
+            }
+
+            // ---- O and l follow the reference
+            const bool raise = m_fin != m;
             if (__any_sync(0xffffffffu, raise)) {
-                const float m_new = raise ? mx : m;
-                const float alpha = raise ? fast_exp2(m - m_new) : 1.f;
+                const float alpha = raise ? fast_exp2(m - m_fin) : 1.f;
                 if (i > 0) {
                     // O holds tiles < i: wait until P.V of tile i-1 has landed, then rescale
-                    if (!(ok = wait_w(pv_done, (i - 1) & 1))) break;
+                    if (!(ok = wait_w(pv_done(x ^ 1), ((i - 1) >> 1) & 1))) break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
@@ -463,44 +566,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     tmem_st_wait();
                 }
                 l *= alpha;
-                m = m_new;
+                m = m_fin;
             }
-            // P = exp2(scale * s - m) as bf16 pairs for the P.V product
-            uint32_t pk[32];
-            const bool live = m != -INFINITY;
-            const float nm = live ? -m : 0.f;
-            float es = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(fmaf(s[2 * j], p.scale_log2, nm));
-                const float p1 = fast_exp2(fmaf(s[2 * j + 1], p.scale_log2, nm));
-                pk[j] = pack_bf16x2(p0, p1);
-                es += p0 + p1;
-            }
-            l += live ? es : 0.f;
-            if (i > 0 && !(ok = wait_w(pv_done, (i - 1) & 1))) break;  // P columns free
-            tmem_st32(tl + TM_P, pk);
-            // rows past the valid tokens (the whole tile if its block is bad) may hold
-            // stale or poisoned data: zero them in the four chunks P.V reads, since
-            // 0 * NaN would still poison the product
+            // tokens in order (low half first) in both CTAs: the same l bit for bit
+            l += rank == 0 ? e_own + e_peer : e_peer + e_own;
+
+            // rows past the valid tokens (the whole tile if its block is bad) may hold stale
+            // or poisoned data: zero them in the chunks P.V reads, since 0 * NaN would
+            // still poison the product
             if (tvalid < TOK) {
-                const uint32_t st = sb + KV_OFF + (i % NS) * KV_STAGE;
-                const int nchunks = (TOK - tvalid) * 32;  // 16-byte chunks: rows x 4 x 8
-                for (int e = row; e < nchunks; e += 128) {
-                    const int r = tvalid + (e >> 5), c = (e >> 3) & 3, k = e & 7;
-                    st_shared_v4(st + c * KVCH + r * 128 + k * 16, 0u, 0u, 0u, 0u);
+                const int own_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(rank)));
+                const int peer_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(peer)));
+                const int n_own = (HALF - own_from) * 32;  // 16-byte pieces: rows x 4 x 8
+                const int n_all = n_own + (HALF - peer_from) * 32;
+                for (int e = row; e < n_all; e += 128) {
+                    const bool o = e < n_own;
+                    const int ee = o ? e : e - n_own;
+                    const int r = (o ? own_from : peer_from) + (ee >> 5), c = (ee >> 3) & 3,
+                              k = ee & 7;
+                    const uint32_t base = st + (o ? (4 * static_cast<int>(rank) + c) : (NOWN + c)) * CH;
+                    st_shared_v4(base + r * 128 + k * 16, 0u, 0u, 0u, 0u);
                 }
-                fence_proxy_async_smem();
             }
-            tmem_st_wait();
+            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_ready(x));
         }
-
         // ------------------------------------------------------------- output
         const int col0 = 256 * rank;
-        if (n > 0 && ok && wait_w(pv_done, (n - 1) & 1)) {
+        if (n > 0 && ok && wait_w(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -557,8 +652,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
 
     // -------- end of segment: every copy into this CTA has landed (each was waited for),
-    // our own copies have read their rows, every role is idle; then barriers restart
+    // our own copies have read their rows, the peer's signals that its P.V has read our
+    // halves have all arrived, every role is idle; then barriers restart
     if (warp >= 2 && lane == 0) bulk_wait_read_all();
+    if (tid == 64 && n > 0) {
+        for (int x = 0; x < 2; ++x) {
+            const int cnt = (n + 1 - x) / 2;  // tiles of parity x
+            if (cnt > 0) drain_wait(rfree(x), (cnt - 1) & 1);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync();
@@ -643,7 +745,7 @@ int decode_tc_cluster_slots() {
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream) {
     CUtensorMap mkv;
-    if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, TOK))
+    if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, HALF))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);

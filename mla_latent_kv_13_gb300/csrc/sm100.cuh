@@ -42,6 +42,16 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t
         : "memory");
 }
 
+// one lane of a converged warp (the same one every time), the others false
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n .reg .b32 rx;\n .reg .pred px;\n elect.sync rx|px, %1;\n selp.u32 %0, 1, 0, px;\n}\n"
+        : "=r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // --------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -72,6 +82,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// non-blocking test (test_wait never suspends the thread)
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -125,6 +146,10 @@ __device__ __forceinline__ void bulk_commit() {
 // wait until the bulk copies committed by this thread have finished reading their source
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the same for all but the most recently committed group
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- proxies
@@ -190,6 +215,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                      bar)
                  : "memory");
 }
+// arrive (once) on the mbarrier at the same shared-memory offset in every CTA of the
+// cluster named in `mask` when all prior tcgen05 async ops of this thread finish
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 inputs here), fp32 accumulate
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -243,6 +277,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= static_cast<uint64_t>(1) << 46;  // descriptor version for the sm_100 family
     d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
     return d;
+}
+// Shared-memory matrix descriptor for a K-major operand without swizzle: 8-row x
+// 16-byte core matrices (each 128 contiguous bytes); lbo = byte distance to the core
+// matrix holding the next 8 elements of K, sbo = to the one holding the next 8 rows.
+__device__ __forceinline__ uint64_t sdesc_kmajor_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for the sm_100 family
+    return d;                             // layout type 0: no swizzle
 }
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
