@@ -14,25 +14,30 @@
 // tokens in full (9 chunks of 64 columns) and the peer's 32 tokens in its own 256 output
 // columns (4 chunks); no partial score crosses the cluster. What does cross is the
 // probability half: each CTA turns its 128 x 32 scores into P (bf16) against a running
-// per-row reference, and ships P with (reference, row sum) to the peer through
-// distributed shared memory (9 KB per tile each way); both CTAs then agree on the larger
-// reference (rescaling whichever half was computed against the smaller one -- rare after
-// the first tile, since the reference is only raised when a score exceeds it by more
-// than 2^8) and run P . V over all 64 tokens for their own columns.
+// per-row reference and stores P with (reference, row sum) straight from registers into
+// the peer's shared memory (st.async, completing bytes on the peer's mbarrier: 9 KB per
+// tile each way); both CTAs then agree on the larger reference (rescaling whichever half
+// was computed against the smaller one -- rare after the first tile, since the
+// reference is only raised when a score exceeds it by more than 2^8) and run P . V over
+// all 64 tokens for their own columns.
 //
 // Tensor memory (512 columns): O fp32 [0, 256), S fp32 [256, 288), Q bf16 pairs of
 // column chunks 0..6 [288, 512). Q chunks 7 (c_kv[448:512]) and 8 (k_rope) are read from
-// shared memory. Shared memory: three cache stages of 52 KB, the two Q chunks, and the
-// P halves (double-buffered: the local half doubles as the source of the copy and as
-// the A operand of P . V; the received half is the A operand of the second K half).
+// shared memory. The chunks of a tile sit in three rings sized by how long they are held:
+// the own tokens' own output columns (both products, 5 slots), the own tokens' other
+// columns and k_rope (scores only, 2 slots) and the peer tokens' own output columns
+// (P . V only, loaded late, 2 slots). P halves are double-buffered: the local half is the
+// A operand of P . V for the own tokens, the received half for the peer's.
 //
-// Roles per CTA (192 threads): warp 0 issues TMA loads (one lane); warp 1 allocates
-// TMEM and issues tcgen05.mma / tcgen05.commit: the whole warp runs the issue loop,
-// polls the barriers with the non-suspending test_wait and one elected lane issues (a
+// Roles per CTA (224 threads): warp 0 loads the own tokens' chunks (TMA, one lane);
+// warp 1 allocates TMEM and issues the score MMAs; warp 6 issues P . V and loads the
+// peer tokens' chunks; warps 2-5 (thread = head row = TMEM lane) load Q, run the online
+// softmax in the exp2 domain, exchange P and finish the output. Each MMA warp runs its
+// loop converged and issues from one elected lane with a predicated instruction: a
 // tcgen05.mma issued by a lone lane of a diverged warp costs that thread several times
-// the tensor pipe's own time per instruction at these small N); warps 2-5 (thread = head
-// row = TMEM lane) load Q, run the online softmax in the exp2 domain, exchange P and
-// finish the output.
+// the tensor pipe's own time per instruction at these small N. P . V has its own warp
+// because a warp issuing the 36 small score MMAs of a tile stays busy for about their
+// execution time.
 // Every mbarrier wait is bounded (about one second); a wait that gives up records
 // MLA_ERR_TIMEOUT in the error word and the CTA drains and exits.
 #include "common.cuh"
@@ -45,35 +50,34 @@ namespace {
 
 using namespace sm100;
 
-#ifndef MLA_DECODE_STAGES
-#define MLA_DECODE_STAGES 3
-#endif
-
 constexpr int TOK = 64;                       // tokens per cache tile (one page)
 constexpr int HALF = 32;                      // tokens of a tile scored by each CTA
-constexpr int NS = MLA_DECODE_STAGES;         // cache-tile stages
 constexpr int CH = HALF * 128;                // one chunk: 32 tokens x 64 bf16 (4 KB)
 constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_rope
-constexpr int NPEER = 4;                      // peer tokens: this CTA's 4 output chunks
-constexpr int STAGE = (NOWN + NPEER) * CH;    // 53248
+// The chunks of a tile live in three rings, by how long they are needed:
+//   KV: own tokens x own output columns (4 chunks) -- both products, until P.V
+//   K : own tokens x the other 4 c_kv chunks and k_rope (5 chunks) -- scores only
+//   V : peer tokens x own output columns (4 chunks) -- P.V only, loaded later
+constexpr int NKV = 5, NK = 2, NV = 2;        // slots per ring
+constexpr int KV_SLOT = 4 * CH, K_SLOT = 5 * CH, V_SLOT = 4 * CH;
 constexpr int NQT = 7;                        // Q chunks held in TMEM (the rest in smem)
 constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
-constexpr int PBUF = 128 * 64;                // P half: 128 rows x 32 bf16 (8 KB)
-constexpr int PWARP = 32 * 64;                // the 32 rows of one warp (2 KB, contiguous)
-constexpr int MBUF = 128 * 8;                 // (reference, row sum) per row
+constexpr int PGRP = 8 * 64 + 8 * 8;          // 8 rows: their 32 bf16 of P, then (reference, sum)
+constexpr int PBUF = 16 * PGRP;               // P half of 128 rows with its row data (9 KB)
+constexpr int PWARP = 4 * PGRP;               // the 32 rows of one warp (contiguous)
 constexpr int KV_OFF = 0;
-constexpr int QS_OFF = KV_OFF + NS * STAGE;
+constexpr int K_OFF = KV_OFF + NKV * KV_SLOT;
+constexpr int V_OFF = K_OFF + NK * K_SLOT;
+constexpr int QS_OFF = V_OFF + NV * V_SLOT;
 constexpr int SEND_OFF = QS_OFF + 2 * QCH;    // local P half, x2
 constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
-constexpr int SMETA_OFF = RECV_OFF + 2 * PBUF;
-constexpr int RMETA_OFF = SMETA_OFF + 2 * MBUF;
-constexpr int BAR_OFF = RMETA_OFF + 2 * MBUF;
-constexpr int NBAR = 32;
+constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
+constexpr int NBAR = 40;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_USED = MISC_OFF + 64;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
-constexpr int NTHREADS = 192;                 // 6 warps
+constexpr int NTHREADS = 224;                 // 7 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
 constexpr uint32_t TM_S = 256;                // S: fp32 columns [256, 288)
@@ -82,18 +86,17 @@ constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
 constexpr int PF_DIST = 4;                    // tiles prefetched into L2 beyond the stage ring
-constexpr uint32_t XBYTES = PWARP + 32 * 8;   // one warp's message: P rows + (reference, sum)
+constexpr uint32_t XBYTES = PWARP;            // one warp's message: P rows + (reference, sum)
 
 constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(QS_OFF % 1024 == 0 && STAGE % 1024 == 0 && CH % 1024 == 0,
+static_assert(QS_OFF % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && CH % 1024 == 0,
               "128-byte-swizzled operands need 1024-byte-aligned atoms");
-static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && SMETA_OFF % 16 == 0 &&
-                  RMETA_OFF % 16 == 0,
-              "bulk-copy alignment");
+static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "bulk-copy alignment");
 static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
+static_assert(2 * (NKV + NK + NV) + 19 <= NBAR, "mbarrier count");
 static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -145,8 +148,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
     const uint32_t bar = sb + BAR_OFF;
     auto kv_full = [&](int s) { return bar + 8u * s; };
-    auto kv_empty = [&](int s) { return bar + 8u * (NS + s); };
-    const uint32_t q_ready = bar + 8u * (2 * NS);
+    auto kv_empty = [&](int s) { return bar + 8u * (NKV + s); };
+    auto k_full = [&](int s) { return bar + 8u * (2 * NKV + s); };
+    auto k_empty = [&](int s) { return bar + 8u * (2 * NKV + NK + s); };
+    auto v_full = [&](int s) { return bar + 8u * (2 * NKV + 2 * NK + s); };
+    auto v_empty = [&](int s) { return bar + 8u * (2 * NKV + 2 * NK + NV + s); };
+    const uint32_t q_ready = bar + 8u * (2 * NKV + 2 * NK + 2 * NV);
     const uint32_t s_full = q_ready + 8;
     const uint32_t s_free = q_ready + 16;
     auto p_ready = [&](int x) { return q_ready + 24 + 8u * x; };  // both P halves of tile parity x
@@ -155,15 +162,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // arrived on by the peer's tcgen05.commit
     auto rfree = [&](int x) { return q_ready + 56 + 8u * x; };
     const uint32_t mma_drain = q_ready + 72;
+    const uint32_t pv_drain = q_ready + 144;
     // the peer's P half of the rows of warp quadrant q has landed in buffer x
     auto recv_full = [&](int q, int x) { return q_ready + 80 + 8u * (2 * q + x); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
     auto init_barriers = [&]() {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NKV; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
+        }
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
         }
         mbar_init(q_ready, 4);
         mbar_init(s_full, 1);
@@ -174,6 +190,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             mbar_init(rfree(x), 1);
         }
         mbar_init(mma_drain, 1);
+        mbar_init(pv_drain, 1);
         for (int k = 0; k < 8; ++k) mbar_init(recv_full(k >> 1, k & 1), 1);
         fence_mbar_init();
     };
@@ -254,9 +271,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
-            // Tiles beyond the shared-memory ring are prefetched into L2 (each CTA its own
-            // 32 tokens, all columns), so that a load issued when a stage frees up is
-            // served from L2 rather than from HBM.
+            // Tiles beyond the shared-memory rings are prefetched into L2 (each CTA its own
+            // 32 tokens, all columns: the peer's value chunks of them included), so that a
+            // load issued when a slot frees up is served from L2 rather than from HBM.
             auto prefetch = [&](int t) {
                 if (t >= n) return;
                 const int blk = btab[t_begin + t];
@@ -264,111 +281,191 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 for (int d = 0; d < NOWN; ++d)
                     tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
             };
-            for (int t = NS; t < NS + PF_DIST; ++t) prefetch(t);
-            int issued = 0;
-            for (int i = 0; i < n; ++i) {
-                const int s = i % NS;
-                if (!mbar_wait(kv_empty(s), ((i / NS) & 1) ^ 1, abort_flag, WAIT_NS)) break;
-                const int blk = btab[t_begin + i];
-                const uint32_t st = sb + KV_OFF + s * STAGE;
-                if (blk >= 0 && blk < p.num_blocks) {
-                    mbar_arrive_expect_tx(kv_full(s), STAGE);
-                    const int y_own = blk * TOK + HALF * rank, y_peer = blk * TOK + HALF * peer;
+            for (int t = NKV; t < NKV + PF_DIST; ++t) prefetch(t);
+            // Near the end of a scheduled segment, warm L2 with the next segment's Q rows
+            // and first tiles, so that its start does not wait on HBM round trips.
+            auto prefetch_next = [&]() {
+                int nb = seg_b;  // first sequence after b that has tiles
+                while (nb < p.B && p.tile_start[nb + 1] == p.tile_start[nb]) ++nb;
+                if (nb >= p.B || p.tile_start[nb] >= r1) return;
+                bulk_prefetch_l2(p.q_lat + (size_t)nb * H * D_C, static_cast<uint32_t>(H * D_C * 2));
+                bulk_prefetch_l2(p.q_rope + (size_t)nb * H * D_ROPE,
+                                 static_cast<uint32_t>(H * D_ROPE * 2));
+                const long ts = p.tile_start[nb], te = p.tile_start[nb + 1];
+                const long nt = min(static_cast<long>(NKV + PF_DIST), min(r1, te) - ts);
+                const int32_t *bt = p.block_table + (size_t)nb * p.max_blocks;
+                for (int t = 0; t < nt; ++t) {
+                    const int blk = bt[t];
+                    if (blk < 0 || blk >= p.num_blocks) continue;
                     for (int d = 0; d < NOWN; ++d)
-                        tma_load_2d(st + d * CH, &map_kv, kv_full(s), 64 * d, y_own);
-                    for (int k = 0; k < NPEER; ++k)
-                        tma_load_2d(st + (NOWN + k) * CH, &map_kv, kv_full(s),
-                                    64 * (4 * rank + k), y_peer);
-                } else {
-                    if (rank == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
-                    mbar_arrive(kv_full(s));  // no data: the consumers mask the tile
+                        tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
                 }
-                issued = i + 1;
-                if (i >= NS) prefetch(i + PF_DIST);
+            };
+            const int next_at = sched ? max(0, n - (NKV + PF_DIST + 4)) : -1;
+            int issued_kv = 0, issued_k = 0;
+            for (int i = 0; i < n; ++i) {
+                const int skv = i % NKV, sk = i % NK;
+                const int blk = btab[t_begin + i];
+                const bool blk_ok = blk >= 0 && blk < p.num_blocks;
+                if (!blk_ok && rank == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
+                const int y_own = blk * TOK + HALF * rank;
+                // own tokens x own output columns
+                if (!mbar_wait(kv_empty(skv), ((i / NKV) & 1) ^ 1, abort_flag, WAIT_NS)) break;
+                if (blk_ok) {
+                    const uint32_t dst = sb + KV_OFF + skv * KV_SLOT;
+                    mbar_arrive_expect_tx(kv_full(skv), KV_SLOT);
+                    for (int k = 0; k < 4; ++k)
+                        tma_load_2d(dst + k * CH, &map_kv, kv_full(skv), 64 * (4 * rank + k), y_own);
+                } else {
+                    mbar_arrive(kv_full(skv));  // no data: the consumers mask the tile
+                }
+                issued_kv = i + 1;
+                // own tokens x the other c_kv columns and k_rope
+                if (!mbar_wait(k_empty(sk), ((i / NK) & 1) ^ 1, abort_flag, WAIT_NS)) break;
+                if (blk_ok) {
+                    const uint32_t dst = sb + K_OFF + sk * K_SLOT;
+                    mbar_arrive_expect_tx(k_full(sk), K_SLOT);
+                    for (int k = 0; k < 4; ++k)
+                        tma_load_2d(dst + k * CH, &map_kv, k_full(sk), 64 * (4 * peer + k), y_own);
+                    tma_load_2d(dst + 4 * CH, &map_kv, k_full(sk), D_C, y_own);
+                } else {
+                    mbar_arrive(k_full(sk));
+                }
+                issued_k = i + 1;
+                if (i >= NKV) prefetch(i + PF_DIST);
+                if (i == next_at) prefetch_next();
             }
             // copies still in flight must land before this CTA may exit
-            for (int i = max(0, issued - NS); i < issued; ++i)
-                drain_wait(kv_full(i % NS), (i / NS) & 1);
+            for (int i = max(0, issued_kv - NKV); i < issued_kv; ++i)
+                drain_wait(kv_full(i % NKV), (i / NKV) & 1);
+            for (int i = max(0, issued_k - NK); i < issued_k; ++i)
+                drain_wait(k_full(i % NK), (i / NK) & 1);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA
+    } else if (warp == 6) {
+        // ------------------------------------ output product and its value chunks
+        // P . V is issued by its own warp: a warp issuing the 36 small score MMAs of a
+        // tile stays busy for about their execution time, and P . V must not queue
+        // behind that. The peer's tokens of a tile in this CTA's output columns are needed
+        // only here, so this warp also loads them, into a short ring whose slot frees when
+        // the P . V that read it is done.
         if (n > 0) {
             const bool leader = elect_one();
-            auto lane0 = [&](bool v) { return __shfl_sync(0xffffffffu, v, 0); };
-            const uint32_t qs = sb + QS_OFF;
-            // scores of this CTA's 32 tokens of tile i over all 576 columns
-            auto issue_s = [&](int i) {
-                const uint32_t own = sb + KV_OFF + (i % NS) * STAGE;
-                for (int d = 0; d < NOWN; ++d)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bdesc = sdesc_sw128(own + d * CH + kk * 32, 16, 1024);
-                        if (d < NQT)
-                            tc_mma_ts(tmem + TM_S, tmem + TM_Q + 32 * d + 8 * kk, bdesc, IDESC_S,
-                                      (d | kk) != 0);
-                        else
-                            tc_mma(tmem + TM_S, sdesc_sw128(qs + (d - NQT) * QCH + kk * 32, 16, 1024),
-                                   bdesc, IDESC_S, 1);
-                    }
-                tc_commit(s_full);
+            auto wait_all = [&](uint32_t bar_, uint32_t par) {
+                return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
+            };
+            auto load_v = [&](int j) {
+                const int sv = j % NV;
+                const int blk = btab[t_begin + j];
+                if (blk >= 0 && blk < p.num_blocks) {
+                    const uint32_t dst = sb + V_OFF + sv * V_SLOT;
+                    mbar_arrive_expect_tx(v_full(sv), V_SLOT);
+                    for (int k = 0; k < 4; ++k)
+                        tma_load_2d(dst + k * CH, &map_kv, v_full(sv), 64 * (4 * rank + k),
+                                    blk * TOK + HALF * peer);
+                } else {
+                    mbar_arrive(v_full(sv));  // no data: the softmax zeroes the slot
+                }
             };
             // O[:, own columns] += P [128 x 64] . V [64 x 256]: tokens [32h, 32h+32) come from
             // the local P half and the own-token chunks when h is this CTA's half, else from
             // the received half and the peer-token chunks
             auto issue_pv = [&](int i) {
-                const uint32_t st = sb + KV_OFF + (i % NS) * STAGE;
+                const uint32_t kv = sb + KV_OFF + (i % NKV) * KV_SLOT;
+                const uint32_t vv = sb + V_OFF + (i % NV) * V_SLOT;
                 const int x = i & 1;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const bool mine = h == static_cast<int>(rank);
                     const uint32_t a = sb + (mine ? SEND_OFF : RECV_OFF) + x * PBUF;
-                    const uint32_t v = st + (mine ? 4 * rank * CH : NOWN * CH);
+                    const uint32_t v = mine ? kv : vv;
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
-                        tc_mma(tmem + TM_O, sdesc_kmajor_plain(a + kk * 256, 128, 512),
-                               sdesc_sw128(v + kk * 2048, CH, 1024), IDESC_PV,
-                               (i > 0 || h > 0 || kk > 0));
+                        tc_mma_if(leader, tmem + TM_O, sdesc_kmajor_plain(a + kk * 256, 128, PGRP),
+                                  sdesc_sw128(v + kk * 2048, CH, 1024), IDESC_PV,
+                                  (i > 0 || h > 0 || kk > 0));
                 }
-                tc_commit(kv_empty(i % NS));
-                tc_commit(pv_done(x));
-                tc_commit_multicast(rfree(x), static_cast<uint16_t>(1u << peer));
+                tc_commit_if(leader, kv_empty(i % NKV));
+                tc_commit_if(leader, v_empty(i % NV));
+                tc_commit_if(leader, pv_done(x));
+                tc_commit_multicast_if(leader, rfree(x), static_cast<uint16_t>(1u << peer));
             };
-            // Scores of tile k need its cache tile (kv_full) and the S columns back from the
-            // softmax (s_free of tile k-1); the output product of tile i needs both P halves
-            // (p_ready). Issue whichever is ready first.
-            bool ok = __all_sync(0xffffffffu, mbar_wait(q_ready, 0, abort_flag, WAIT_NS));
-            if (ok) tc_fence_after();
-            int s_next = 0, pv_next = 0;
-            uint64_t t_last = globaltimer_ns();
-            uint32_t spins = 0;
-            while (ok && pv_next < n) {
-                if (lane0(s_next < n && mbar_poll(kv_full(s_next % NS), (s_next / NS) & 1) &&
-                          (s_next == 0 || mbar_poll(s_free, (s_next - 1) & 1)))) {
-                    tc_fence_after();
-                    if (leader) issue_s(s_next);
-                    __syncwarp();
-                    ++s_next;
-                    t_last = globaltimer_ns();
-                    continue;
+            int loaded = min(n, NV);
+            if (lane == 0)
+                for (int j = 0; j < loaded; ++j) load_v(j);
+            bool ok = true;
+            for (int i = 0; ok && i < n; ++i) {
+                // refill the slot of tile i-1 once its P . V is done
+                if (i >= 1 && loaded < n) {
+                    if (!(ok = wait_all(v_empty((i - 1) % NV), ((i - 1) / NV) & 1))) break;
+                    if (lane == 0) load_v(loaded);
+                    ++loaded;
                 }
-                if (lane0(pv_next < s_next && mbar_poll(p_ready(pv_next & 1), (pv_next >> 1) & 1))) {
-                    tc_fence_after();
-                    if (leader) issue_pv(pv_next);
-                    __syncwarp();
-                    ++pv_next;
-                    t_last = globaltimer_ns();
-                    continue;
-                }
-                if ((++spins & 63) == 0) {
-                    bool stop = *abort_flag != 0;
-                    if (!stop && globaltimer_ns() - t_last > WAIT_NS) {
-                        if (lane == 0) *abort_flag = 1;
-                        stop = true;
-                    }
-                    ok = !lane0(stop);
-                }
+                if (!(ok = wait_all(p_ready(i & 1), (i >> 1) & 1))) break;
+                if (!(ok = wait_all(v_full(i % NV), (i / NV) & 1))) break;
+                tc_fence_after();
+                issue_pv(i);
+                __syncwarp();
             }
-            // every MMA this thread issued has finished before TMEM is released
+            // every MMA this warp issued has finished, every copy it started has landed
+            if (leader) {
+                tc_commit(pv_drain);
+                drain_wait(pv_drain, 0);
+            }
+            if (lane == 0)
+                for (int j = max(0, loaded - NV); j < loaded; ++j)
+                    drain_wait(v_full(j % NV), (j / NV) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA
+        // The whole warp runs the issue loop and one elected lane issues (the instruction
+        // is predicated, not branched to): a tcgen05.mma issued by a lone lane of a
+        // diverged warp costs that thread several times the tensor pipe's own time per
+        // instruction at these small N.
+        if (n > 0) {
+            const bool leader = elect_one();
+            auto wait_all = [&](uint32_t bar_, uint32_t par) {
+                return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
+            };
+            const uint32_t qs = sb + QS_OFF;
+            // scores of this CTA's 32 tokens of tile i over all 576 columns
+            auto issue_s = [&](int i) {
+                const uint32_t kv = sb + KV_OFF + (i % NKV) * KV_SLOT;
+                const uint32_t ko = sb + K_OFF + (i % NK) * K_SLOT;
+#pragma unroll
+                for (int d = 0; d < NOWN; ++d)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // column chunk d of the own tokens: in the KV ring if it is one of
+                        // this CTA's output chunks, else in the K ring (k_rope last)
+                        const int o = d - 4 * static_cast<int>(rank);
+                        const uint32_t src =
+                            (o >= 0 && o < 4) ? kv + o * CH
+                                              : ko + (d < 8 ? d - 4 * static_cast<int>(peer) : 4) * CH;
+                        const uint64_t bdesc = sdesc_sw128(src + kk * 32, 16, 1024);
+                        if (d < NQT)
+                            tc_mma_ts_if(leader, tmem + TM_S, tmem + TM_Q + 32 * d + 8 * kk, bdesc,
+                                         IDESC_S, (d | kk) != 0);
+                        else
+                            tc_mma_if(leader, tmem + TM_S,
+                                      sdesc_sw128(qs + (d - NQT) * QCH + kk * 32, 16, 1024), bdesc,
+                                      IDESC_S, 1);
+                    }
+                tc_commit_if(leader, s_full);
+                tc_commit_if(leader, k_empty(i % NK));
+            };
+            // scores of tile k need its cache chunks and the S columns back from the
+            // softmax (s_free of tile k-1)
+            bool ok = wait_all(q_ready, 0);
+            for (int k = 0; ok && k < n; ++k) {
+                if (!(ok = wait_all(kv_full(k % NKV), (k / NKV) & 1))) break;
+                if (!(ok = wait_all(k_full(k % NK), (k / NK) & 1))) break;
+                if (k > 0 && !(ok = wait_all(s_free, (k - 1) & 1))) break;
+                tc_fence_after();
+                issue_s(k);
+                __syncwarp();
+            }
+            // every MMA this warp issued has finished before TMEM is released
             if (leader) {
                 tc_commit(mma_drain);
                 drain_wait(mma_drain, 0);
@@ -385,12 +482,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         // warps with at least one head row exchange their P rows (both CTAs agree)
         const bool wlive = wq * 32 < H;
-        // this row in a P half: K-major 8 x 16-byte core matrices, no swizzle
-        // (next 8 K elements +128 B, next 8 rows +512 B)
-        const uint32_t prow = (row >> 3) * 512 + (row & 7) * 16;
+        // this row in a P half: K-major 8 x 16-byte core matrices, no swizzle (next 8 K
+        // elements +128 B, next 8 rows +PGRP B); each 8-row group ends with the rows'
+        // (reference, row sum)
+        const uint32_t prow = (row >> 3) * PGRP + (row & 7) * 16;
+        const uint32_t mrow = (row >> 3) * PGRP + 512 + (row & 7) * 8;
         const uint32_t send = sb + SEND_OFF, recv = sb + RECV_OFF;
-        const uint32_t smeta = sb + SMETA_OFF, rmeta = sb + RMETA_OFF;
-        const uint32_t recv_peer = mapa(recv, peer), rmeta_peer = mapa(rmeta, peer);
+        const uint32_t recv_peer = mapa(recv, peer);
         const uint32_t rbar_peer = mapa(recv_full(wq, 0), peer);  // + 8 for buffer 1
         float m = -INFINITY, l = 0.f;
         bool ok = true;
@@ -411,24 +509,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const uint4 *rsrc =
                 reinterpret_cast<const uint4 *>(p.q_rope + ((size_t)b * H + row) * D_ROPE);
             const uint32_t qrow = sb + QS_OFF + (row >> 3) * 1024 + (row & 7) * 128;
-            for (int c = 0; c < NOWN; ++c) {
-                uint32_t r[32];
+            // three chunks' loads in flight at a time: three memory round trips, not nine
+            for (int c0 = 0; c0 < NOWN; c0 += 3) {
+                uint4 v[3][8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (live_row) v = c < 8 ? qsrc[8 * c + k] : rsrc[k];
-                    r[4 * k] = v.x;
-                    r[4 * k + 1] = v.y;
-                    r[4 * k + 2] = v.z;
-                    r[4 * k + 3] = v.w;
-                }
-                if (c < NQT) {
-                    tmem_st32(tl + TM_Q + 32 * c, r);
-                } else {
+                for (int u = 0; u < 3; ++u)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        st_shared_v4(qrow + (c - NQT) * QCH + ((k ^ (row & 7)) << 4), r[4 * k],
-                                     r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                    for (int k = 0; k < 8; ++k) {
+                        const int c = c0 + u;
+                        v[u][k] = make_uint4(0u, 0u, 0u, 0u);
+                        if (live_row) v[u][k] = c < 8 ? qsrc[8 * c + k] : rsrc[k];
+                    }
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    const int c = c0 + u;
+                    if (c < NQT) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            r[4 * k] = v[u][k].x;
+                            r[4 * k + 1] = v[u][k].y;
+                            r[4 * k + 2] = v[u][k].z;
+                            r[4 * k + 3] = v[u][k].w;
+                        }
+                        tmem_st32(tl + TM_Q + 32 * c, r);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(qrow + (c - NQT) * QCH + ((k ^ (row & 7)) << 4), v[u][k].x,
+                                         v[u][k].y, v[u][k].z, v[u][k].w);
+                    }
                 }
             }
             tmem_st_wait();
@@ -444,7 +554,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const int blk = blk_next;
             if (i + 1 < n) blk_next = btab[tile + 1];
             const int x = i & 1;
-            const uint32_t st = sb + KV_OFF + (i % NS) * STAGE;
+            const uint32_t kvs = sb + KV_OFF + (i % NKV) * KV_SLOT;
+            const uint32_t vs = sb + V_OFF + (i % NV) * V_SLOT;
 
             // ---- scores of this CTA's 32 tokens, out of TMEM (releasing S)
             if (!(ok = wait_w(s_full, i & 1))) break;
@@ -464,10 +575,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             float s[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) s[j] = j < ov ? __uint_as_float(sr[j]) : -INFINITY;
-            float mx = s[0];
+            float mx;
+            {
+                float t[16];
 #pragma unroll
-            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, s[j]);
-            mx *= p.scale_log2;  // scale > 0: the max of the scaled scores
+                for (int j = 0; j < 16; ++j) t[j] = fmaxf(s[j], s[j + 16]);
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+                mx = t[0] * p.scale_log2;  // scale > 0: the max of the scaled scores
+            }
             // local reference: raised only when a score exceeds it by more than TAU
             const float m_new = mx > m + TAU ? mx : m;
 
@@ -499,23 +617,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (i >= 2 && !(ok = wait_w(pv_done(x), ((i >> 1) - 1) & 1))) break;
             float m_peer = -INFINITY, e_peer = 0.f;
             if (wlive) {
-                if (i >= 2 && lane == 0) bulk_wait_read_but_one();
-                __syncwarp();
                 put_p(pk);
-                st_shared_v2f(smeta + x * MBUF + row * 8, m_new, e_own);
-                fence_proxy_async_smem();
-                // the peer's buffer x is free once its P.V of tile i-2 is done
+                // the peer's buffer x is free once its P.V of tile i-2 is done; the P row
+                // and its (reference, sum) go straight from registers into it
                 if (i >= 2 && !(ok = wait_wc(rfree(x), ((i >> 1) - 1) & 1))) break;
-                if (lane == 0) {
-                    const uint32_t off = x * PBUF + wq * PWARP, moff = x * MBUF + wq * 256;
-                    bulk_copy_to_peer(recv_peer + off, send + off, PWARP, rbar_peer + 8u * x);
-                    bulk_copy_to_peer(rmeta_peer + moff, smeta + moff, 256, rbar_peer + 8u * x);
-                    bulk_commit();
-                    mbar_arrive_expect_tx(recv_full(wq, x), XBYTES);
+                {
+                    const uint32_t dst = recv_peer + x * PBUF + prow, rb = rbar_peer + 8u * x;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_async_v4(dst + k * 128, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2],
+                                    pk[4 * k + 3], rb);
+                    st_async_v2(recv_peer + x * PBUF + mrow, __float_as_uint(m_new),
+                                __float_as_uint(e_own), rb);
                 }
+                if (lane == 0) mbar_arrive_expect_tx(recv_full(wq, x), XBYTES);
                 // ---- the peer's half of tile i
                 if (!(ok = wait_wc(recv_full(wq, x), (i >> 1) & 1))) break;
-                const float2 pm = ld_shared_v2f(rmeta + x * MBUF + row * 8);
+                const float2 pm = ld_shared_v2f(recv + x * PBUF + mrow);
                 m_peer = pm.x;
                 e_peer = pm.y;
             }
@@ -525,13 +643,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // received half rescaled)
             const float m_fin = fmaxf(m_new, m_peer);
             const bool fix_own = m_new != m_fin, fix_peer = m_peer != m_fin;
-            if (__any_sync(0xffffffffu, fix_own)) {
-                if (lane == 0) bulk_wait_read_all();  // the copy has read the local half
-                __syncwarp();
-                if (fix_own) {
-                    e_own = make_p(m_fin, pk);
-                    put_p(pk);
-                }
+            if (fix_own) {
+                e_own = make_p(m_fin, pk);
+                put_p(pk);
             }
             if (fix_peer) {
                 const float f = fast_exp2(m_peer - m_fin);
@@ -575,6 +689,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // or poisoned data: zero them in the chunks P.V reads, since 0 * NaN would
             // still poison the product
             if (tvalid < TOK) {
+                // the value chunks of the peer's tokens may still be in flight
+                if (!(ok = wait_w(v_full(i % NV), (i / NV) & 1))) break;
                 const int own_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(rank)));
                 const int peer_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(peer)));
                 const int n_own = (HALF - own_from) * 32;  // 16-byte pieces: rows x 4 x 8
@@ -584,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const int ee = o ? e : e - n_own;
                     const int r = (o ? own_from : peer_from) + (ee >> 5), c = (ee >> 3) & 3,
                               k = ee & 7;
-                    const uint32_t base = st + (o ? (4 * static_cast<int>(rank) + c) : (NOWN + c)) * CH;
+                    const uint32_t base = (o ? kvs : vs) + c * CH;
                     st_shared_v4(base + r * 128 + k * 16, 0u, 0u, 0u, 0u);
                 }
             }

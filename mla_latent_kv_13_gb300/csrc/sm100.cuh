@@ -52,6 +52,15 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// 8-byte store into a peer CTA's shared memory that completes 8 bytes on its mbarrier
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, uint32_t a, uint32_t b, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+            raddr),
+        "r"(a), "r"(b), "r"(rbar)
+        : "memory");
+}
+
 // --------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -111,13 +120,25 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait for the phase of parity `parity`. Gives up after `limit_ns` (or at
+__device__ __forceinline__ bool mbar_poll_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], "
+        "%2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` (a non-suspending test first, then
+// suspending tests). Gives up after `limit_ns` (or at
 // once when another thread of the CTA already gave up, *abort != 0); returns false
 // then, after raising *abort.
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t limit_ns) {
-    if (CLUSTER ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    if (CLUSTER ? mbar_poll_cluster(bar, parity) : mbar_poll(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (CLUSTER ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
@@ -131,25 +152,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Bulk copy from this CTA's shared memory into a peer CTA's shared memory (both
-// 16-byte aligned, size a multiple of 16); completes `bytes` on the peer's mbarrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes,
-                                                  uint32_t rbar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];" ::"r"(rdst), "r"(src), "r"(bytes), "r"(rbar)
-        : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 // wait until the bulk copies committed by this thread have finished reading their source
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// the same for all but the most recently committed group
-__device__ __forceinline__ void bulk_wait_read_but_one() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- proxies
@@ -182,6 +190,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte-aligned address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)),
+                 "r"(bytes)
+                 : "memory");
+}
 // Prefetch the box at (x, y) of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void *map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
@@ -215,15 +229,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                      bar)
                  : "memory");
 }
-// arrive (once) on the mbarrier at the same shared-memory offset in every CTA of the
-// cluster named in `mask` when all prior tcgen05 async ops of this thread finish
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-}
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 inputs here), fp32 accumulate
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -241,6 +246,42 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Predicated forms of the MMA and commit instructions, executed by every lane of a
+// converged warp and performed only where `issue` is set (the warp does not branch):
+// the operands stay warp-uniform, which keeps each issue near the tensor pipe's own
+// rate. The multicast commit arrives on the mbarrier at the same shared-memory offset
+// in every CTA of the cluster named in `mask`.
+__device__ __forceinline__ void tc_mma_ts_if(bool issue, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+        " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(issue))
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_if(bool issue, uint32_t d_tmem, uint64_t adesc,
+                                          uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+        " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(issue))
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_if(bool issue, uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+        " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar),
+        "r"(static_cast<uint32_t>(issue))
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_multicast_if(bool issue, uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+        " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;\n}\n" ::"r"(bar),
+        "h"(mask), "r"(static_cast<uint32_t>(issue))
         : "memory");
 }
 // 32 consecutive 32-bit columns of this thread's TMEM lane
