@@ -58,7 +58,7 @@ constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_r
 //   KV: own tokens x own output columns (4 chunks) -- both products, until P.V
 //   K : own tokens x the other 4 c_kv chunks and k_rope (5 chunks) -- scores only
 //   V : peer tokens x own output columns (4 chunks) -- P.V only, loaded later
-constexpr int NKV = 5, NK = 2, NV = 2;        // slots per ring
+constexpr int NKV = 4, NK = 2, NV = 3;        // slots per ring
 constexpr int KV_SLOT = 4 * CH, K_SLOT = 5 * CH, V_SLOT = 4 * CH;
 constexpr int NQT = 7;                        // Q chunks held in TMEM (the rest in smem)
 constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
@@ -234,6 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         seg_b = lo;
     }
 
+    int q_for = -1;  // softmax warps: the sequence whose Q rows are in TMEM / shared memory
     for (int seg = 0;; ++seg) {
     // -------- this segment: sequence b, tiles [t_begin, t_end), output slot
     int b, t_begin, t_end, part;
@@ -281,7 +282,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 for (int d = 0; d < NOWN; ++d)
                     tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
             };
-            for (int t = NKV; t < NKV + PF_DIST; ++t) prefetch(t);
             // Near the end of a scheduled segment, warm L2 with the next segment's Q rows
             // and first tiles, so that its start does not wait on HBM round trips.
             auto prefetch_next = [&]() {
@@ -332,6 +332,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     mbar_arrive(k_full(sk));
                 }
                 issued_k = i + 1;
+                if (i == 0)  // after the first tile's loads are on their way
+                    for (int t = NKV; t < NKV + PF_DIST; ++t) prefetch(t);
                 if (i >= NKV) prefetch(i + PF_DIST);
                 if (i == next_at) prefetch_next();
             }
@@ -499,17 +501,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         auto wait_wc = [&](uint32_t bar_, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait<true>(bar_, par, abort_flag, WAIT_NS));
         };
-
-        if (n > 0) {
-            // Q rows: chunks 0..6 into TMEM (A operand of the score product), chunks 7..8
-            // (c_kv columns 448..511 and k_rope) into shared memory, 128-byte swizzled as
-            // the cache tiles are. Rows >= H are 0.
+        // Q rows of sequence bq: chunks 0..6 into TMEM (A operand of the score product),
+        // chunks 7..8 (c_kv columns 448..511 and k_rope) into shared memory, 128-byte
+        // swizzled as the cache tiles are. Rows >= H are 0. Three chunks per memory round
+        // trip (more in flight at once costs the main loop registers).
+        auto load_q = [&](int bq) {
             const uint4 *qsrc =
-                reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)b * H + row) * D_C);
+                reinterpret_cast<const uint4 *>(p.q_lat + ((size_t)bq * H + row) * D_C);
             const uint4 *rsrc =
-                reinterpret_cast<const uint4 *>(p.q_rope + ((size_t)b * H + row) * D_ROPE);
+                reinterpret_cast<const uint4 *>(p.q_rope + ((size_t)bq * H + row) * D_ROPE);
             const uint32_t qrow = sb + QS_OFF + (row >> 3) * 1024 + (row & 7) * 128;
-            // three chunks' loads in flight at a time: three memory round trips, not nine
             for (int c0 = 0; c0 < NOWN; c0 += 3) {
                 uint4 v[3][8];
 #pragma unroll
@@ -518,11 +519,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     for (int k = 0; k < 8; ++k) {
                         const int c = c0 + u;
                         v[u][k] = make_uint4(0u, 0u, 0u, 0u);
-                        if (live_row) v[u][k] = c < 8 ? qsrc[8 * c + k] : rsrc[k];
+                        if (live_row && c < NOWN) v[u][k] = c < 8 ? qsrc[8 * c + k] : rsrc[k];
                     }
 #pragma unroll
                 for (int u = 0; u < 3; ++u) {
                     const int c = c0 + u;
+                    if (c >= NOWN) break;
                     if (c < NQT) {
                         uint32_t r[32];
 #pragma unroll
@@ -541,6 +543,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
+        };
+
+        if (n > 0) {
+            if (q_for != b) load_q(b);
+            q_for = b;
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
@@ -708,6 +715,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_ready(x));
+        }
+        // The last score product of this segment is done (its scores were read): load the
+        // next scheduled segment's Q rows now, so that they are in place when it starts.
+        if (sched && ok && n > 0) {
+            int nb = seg_b;
+            while (nb < p.B && p.tile_start[nb + 1] == p.tile_start[nb]) ++nb;
+            if (nb < p.B && p.tile_start[nb] < r1) {
+                load_q(nb);
+                q_for = nb;
+            }
         }
         // ------------------------------------------------------------- output
         const int col0 = 256 * rank;
