@@ -7,38 +7,73 @@ namespace mla {
 
 namespace {
 
-// One CTA per (h, b); 128 threads x 4 latent columns.
-__global__ void __launch_bounds__(128) combine_kernel(const float *o_part, const float *lse_part,
-                                                      int S, int H, uint16_t *out, float *lse) {
-    grid_launch_dependents();
-    grid_dependency_wait();
-    const int h = blockIdx.x, b = blockIdx.y;
+// Merge np partial rows (fp32 [512], each with its log-sum-exp) into one bf16 row and its
+// log-sum-exp, with one warp: lane l holds columns 4l + 128k (k < 4), so every part row is
+// read as four coalesced 512-byte segments; the parts' log-sum-exps are read in parallel
+// across lanes (part s on lane s % 32) and their weights shared by shuffles. Parts are
+// accumulated in order. A part with lse = -inf (an empty range) contributes nothing.
+__device__ __forceinline__ void merge_row_warp(const float *o0, size_t ostride, const float *l0,
+                                               size_t lstride, int np, uint16_t *orow,
+                                               float *lse_out, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
     float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, lse_part[((size_t)b * S + s) * H + h]);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = lane; s < np; s += 32) m = fmaxf(m, l0[s * lstride]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
     float tot = -INFINITY;
     if (m != -INFINITY) {
         float den = 0.f;
-        for (int s = 0; s < S; ++s) {
-            float l = lse_part[((size_t)b * S + s) * H + h];
+        for (int s = lane; s < np; s += 32) {
+            const float l = l0[s * lstride];
             if (l != -INFINITY) den += __expf(l - m);
         }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(FULL, den, o);
         tot = m + __logf(den);
-        for (int s = 0; s < S; ++s) {
-            float l = lse_part[((size_t)b * S + s) * H + h];
-            if (l == -INFINITY) continue;
-            float w = __expf(l - tot);
-            float4 v = *reinterpret_cast<const float4 *>(
-                o_part + (((size_t)b * S + s) * H + h) * D_C + threadIdx.x * 4);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
+        for (int s0 = 0; s0 < np; s0 += 32) {
+            const float lmine = s0 + lane < np ? l0[(s0 + lane) * lstride] : -INFINITY;
+            const float wmine = lmine != -INFINITY ? __expf(lmine - tot) : 0.f;
+            const int cnt = min(32, np - s0);
+            for (int j = 0; j < cnt; ++j) {
+                if (__shfl_sync(FULL, lmine, j) == -INFINITY) continue;
+                const float w = __shfl_sync(FULL, wmine, j);
+                const float *row = o0 + (size_t)(s0 + j) * ostride + lane * 4;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 v = *reinterpret_cast<const float4 *>(row + 128 * k);
+                    acc[4 * k] += w * v.x;
+                    acc[4 * k + 1] += w * v.y;
+                    acc[4 * k + 2] += w * v.z;
+                    acc[4 * k + 3] += w * v.w;
+                }
+            }
         }
     }
-    uint2 pk = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
-    *reinterpret_cast<uint2 *>(out + ((size_t)b * H + h) * D_C + threadIdx.x * 4) = pk;
-    if (threadIdx.x == 0) lse[(size_t)b * H + h] = tot;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint2 *>(orow + lane * 4 + 128 * k) =
+            make_uint2(pack_bf16x2(acc[4 * k], acc[4 * k + 1]),
+                       pack_bf16x2(acc[4 * k + 2], acc[4 * k + 3]));
+    if (lane == 0) *lse_out = tot;
+}
+
+constexpr int MERGE_ROWS = 8;  // head rows (one warp each) per CTA of the merge kernels
+
+// Fixed split: rows (b, h) of S token ranges each. Grid (ceil(H / 8), B), 256 threads.
+__global__ void __launch_bounds__(32 * MERGE_ROWS) combine_kernel(const float *o_part,
+                                                                 const float *lse_part, int S,
+                                                                 int H, uint16_t *out,
+                                                                 float *lse) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), b = blockIdx.y;
+    if (h >= H) return;
+    merge_row_warp(o_part + ((size_t)b * S * H + h) * D_C, (size_t)H * D_C,
+                   lse_part + (size_t)b * S * H + h, H, S, out + ((size_t)b * H + h) * D_C,
+                   lse + (size_t)b * H + h, threadIdx.x & 31);
 }
 
 // Sum k-split partials [S][batch][M][N] into bf16 C (batch stride c_bstride, row ldc).
@@ -149,44 +184,22 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
 
 // Merge of the parts of each cut sequence; empty sequences get out = 0, lse = -inf;
 // sequences finished inside one cluster were written by the attention kernel itself.
-__global__ void __launch_bounds__(128) combine_sched_kernel(
+// Balanced schedule: only sequences cut between clusters (nparts > 0) and empty ones are
+// written here; the decode kernel wrote the others. Grid (ceil(H / 8), B), 256 threads.
+__global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
     const float *o_part, const float *lse_part, const int32_t *tile_start,
     const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *lse) {
     grid_launch_dependents();
     grid_dependency_wait();
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), b = blockIdx.y;
+    if (h >= H) return;
     const int np = nparts[b];
     const bool empty = tile_start[b + 1] == tile_start[b];
     if (np == 0 && !empty) return;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float tot = -INFINITY;
-    if (np > 0) {
-        const int p0 = part_begin[b];
-        float m = -INFINITY;
-        for (int s = 0; s < np; ++s) m = fmaxf(m, lse_part[(size_t)(p0 + s) * H + h]);
-        if (m != -INFINITY) {
-            float den = 0.f;
-            for (int s = 0; s < np; ++s) {
-                const float l = lse_part[(size_t)(p0 + s) * H + h];
-                if (l != -INFINITY) den += __expf(l - m);
-            }
-            tot = m + __logf(den);
-            for (int s = 0; s < np; ++s) {
-                const float l = lse_part[(size_t)(p0 + s) * H + h];
-                if (l == -INFINITY) continue;
-                const float w = __expf(l - tot);
-                const float4 x = *reinterpret_cast<const float4 *>(
-                    o_part + ((size_t)(p0 + s) * H + h) * D_C + threadIdx.x * 4);
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-                acc[2] += w * x.z;
-                acc[3] += w * x.w;
-            }
-        }
-    }
-    const uint2 pk = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
-    *reinterpret_cast<uint2 *>(out + ((size_t)b * H + h) * D_C + threadIdx.x * 4) = pk;
-    if (threadIdx.x == 0) lse[(size_t)b * H + h] = tot;
+    const int p0 = np > 0 ? part_begin[b] : 0;
+    merge_row_warp(o_part + ((size_t)p0 * H + h) * D_C, (size_t)H * D_C,
+                   lse_part + (size_t)p0 * H + h, H, np, out + ((size_t)b * H + h) * D_C,
+                   lse + (size_t)b * H + h, threadIdx.x & 31);
 }
 
 }  // namespace
@@ -202,15 +215,16 @@ cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
                                  const int32_t *tile_start, const int32_t *part_begin,
                                  const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
                                  cudaStream_t stream) {
-    dim3 grid(H, B);
-    return launch_pdl(combine_sched_kernel, grid, dim3(128), 0, stream, o_part, lse_part,
-                      tile_start, part_begin, nparts, H, out, lse);
+    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, B);
+    return launch_pdl(combine_sched_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part,
+                      lse_part, tile_start, part_begin, nparts, H, out, lse);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
                            uint16_t *out, float *lse, cudaStream_t stream) {
-    dim3 grid(H, B);
-    return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, o_part, lse_part, S, H, out, lse);
+    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, B);
+    return launch_pdl(combine_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part, lse_part, S,
+                      H, out, lse);
 }
 
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
