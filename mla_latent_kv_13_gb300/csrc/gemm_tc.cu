@@ -281,7 +281,10 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
 int gemm_block_n(int N, int K) { return (N >= 4096 && K >= 4096 && N % 256 == 0) ? 256 : 128; }
 int gemm_block_n(int M, int N, int K) {
     // many row tiles (prefill up-projections): fewer, longer-lived CTAs at width 256
-    return (M >= 1024 && N >= 4096 && N % 256 == 0) ? 256 : gemm_block_n(N, K);
+    if (M >= 1024 && N >= 4096 && N % 256 == 0) return 256;
+    // short products (per-head W_UK, K = 128): half as many CTAs, A read half as often
+    if (K <= 256 && N >= 512 && N % 256 == 0) return 256;
+    return gemm_block_n(N, K);
 }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column
