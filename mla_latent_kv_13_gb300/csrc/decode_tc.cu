@@ -113,9 +113,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "memory");
     return v;
 }
-__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
 __device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");

@@ -76,17 +76,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  "r"(bytes)
                  : "memory");
 }
-// arrive on an mbarrier of another CTA of the cluster (shared::cluster address)
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
-                 : "memory");
-}
-// relaxed variant: orders nothing; for flow-control signals whose data dependences
-// are already satisfied in program order (the loads they protect have been consumed)
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cbar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
-                 : "memory");
-}
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
