@@ -209,3 +209,26 @@ def test_balanced_schedule_matches_fixed_split(mla):
     b = _run(mla, d, num_splits=1)
     np.testing.assert_allclose(a[0], b[0], rtol=1e-2, atol=2e-3)
     np.testing.assert_allclose(a[1], b[1], atol=1e-4)
+
+
+@pytest.mark.parametrize("splits", [1, 0])
+def test_reference_raised_by_one_half_mid_sequence(mla, splits):
+    """The k_rope part of a few cached rows is scaled by 40, so that for many heads one
+    token's score jumps far above the running reference in the middle of a sequence, inside
+    one CTA's 32-token half of a tile (tokens 40 and 5 of their tiles lie in different
+    halves); the rows' values (c_kv) keep their scale. The other half of the tile, the
+    received half and the running output must all be brought to the new reference; results
+    must still match the oracle."""
+    d = _case(3, 128, (700, 333, 1000), seed=21)
+    cache = d["kv_cache"].copy()
+    bt = d["block_table"]
+    spikes = [(0, 3 * 64 + 40), (1, 2 * 64 + 5), (2, 1 * 64 + 50), (2, 10 * 64 + 3)]
+    for b, t in spikes:
+        blk, r = bt[b][t // 64], t % 64
+        rope = synth.bf16_bits_to_f64(cache[blk, r, 512:]) * 40.0
+        cache[blk, r, 512:] = synth.f32_to_bf16_bits(rope.astype(np.float32))
+    out, lse, st = _run(mla, d, num_splits=splits, cache=dev_bf16(cache))
+    assert st == 0
+    ref, lref = _oracle(d, cache=cache)
+    assert_close_rows(out, ref)
+    assert_lse(lse, lref)
