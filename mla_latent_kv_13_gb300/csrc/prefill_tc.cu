@@ -151,54 +151,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA
-        if (lane == 0) {
-            bool ok = mbar_wait(q_full, 0, abort_flag, WAIT_NS);
+        // The whole warp runs the issue loop (decisions from lane 0's view of the barriers,
+        // non-suspending polls) and one elected lane issues through predicated
+        // instructions: a tcgen05.mma issued by a lone lane of a diverged warp costs that
+        // thread more than the tensor pipe's own time per instruction.
+        {
+            const bool leader = elect_one();
+            auto lane0 = [&](bool v) { return __shfl_sync(0xffffffffu, v, 0); };
+            bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, WAIT_NS));
             if (ok) tc_fence_after();
             int s_next = 0, pv_next = 0;
-            uint64_t t_last = globaltimer_ns();
+            uint64_t t_idle = 0;  // start of the current idle stretch (0: progress since)
             uint32_t spins = 0;
             while (ok && pv_next < nkt) {
                 // S(t) into buffer t % 2 once the softmax has read tile t-2 out of it
-                if (s_next < nkt && mbar_test(kv_full(s_next % NSTG), (s_next / NSTG) & 1) &&
-                    (s_next < 2 || mbar_test(s_free(s_next & 1), ((s_next >> 1) - 1) & 1))) {
+                if (lane0(s_next < nkt && mbar_poll(kv_full(s_next % NSTG), (s_next / NSTG) & 1) &&
+                          (s_next < 2 || mbar_poll(s_free(s_next & 1), ((s_next >> 1) - 1) & 1)))) {
                     tc_fence_after();
                     const uint32_t st = sb + STG_OFF + (s_next % NSTG) * STG;
                     const uint32_t ts = tmem + TM_S + 128 * (s_next & 1);
+#pragma unroll
                     for (int c = 0; c < K_CH; ++c)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(ts, sdesc_sw128(sb + Q_OFF + c * CH + kk * 32, 16, 1024),
-                                   sdesc_sw128(st + c * CH + kk * 32, 16, 1024), IDESC_S,
-                                   (c | kk) != 0);
-                    tc_commit(s_full(s_next & 1));
+                            tc_mma_if(leader, ts, sdesc_sw128(sb + Q_OFF + c * CH + kk * 32, 16, 1024),
+                                      sdesc_sw128(st + c * CH + kk * 32, 16, 1024), IDESC_S,
+                                      (c | kk) != 0);
+                    tc_commit_if(leader, s_full(s_next & 1));
+                    __syncwarp();
                     ++s_next;
-                    t_last = globaltimer_ns();
+                    t_idle = 0;
                     continue;
                 }
-                if (pv_next < s_next && mbar_test(p_full, pv_next & 1)) {
+                if (lane0(pv_next < s_next && mbar_poll(p_full, pv_next & 1))) {
                     tc_fence_after();
                     const uint32_t vt = sb + STG_OFF + (pv_next % NSTG) * STG + 3 * CH;
 #pragma unroll
                     for (int kk = 0; kk < KT / 16; ++kk)
-                        tc_mma_ts(tmem + TM_O, tmem + TM_P + 8 * kk,
-                                  sdesc_sw128(vt + kk * 2048, CH, 1024), IDESC_PV,
-                                  (pv_next > 0 || kk > 0));
-                    tc_commit(kv_empty(pv_next % NSTG));
-                    tc_commit(pv_done);
+                        tc_mma_ts_if(leader, tmem + TM_O, tmem + TM_P + 8 * kk,
+                                     sdesc_sw128(vt + kk * 2048, CH, 1024), IDESC_PV,
+                                     (pv_next > 0 || kk > 0));
+                    tc_commit_if(leader, kv_empty(pv_next % NSTG));
+                    tc_commit_if(leader, pv_done);
+                    __syncwarp();
                     ++pv_next;
-                    t_last = globaltimer_ns();
+                    t_idle = 0;
                     continue;
                 }
                 if ((++spins & 63) == 0) {
-                    if (*abort_flag) ok = false;
-                    else if (globaltimer_ns() - t_last > WAIT_NS) {
-                        *abort_flag = 1;
-                        ok = false;
+                    const uint64_t now = globaltimer_ns();
+                    if (t_idle == 0) t_idle = now;
+                    bool stop = *abort_flag != 0;
+                    if (!stop && now - t_idle > WAIT_NS) {
+                        if (lane == 0) *abort_flag = 1;
+                        stop = true;
                     }
+                    ok = !lane0(stop);
                 }
             }
-            tc_commit(mma_drain);
-            drain(mma_drain, 0);
+            if (leader) {
+                tc_commit(mma_drain);
+                drain(mma_drain, 0);
+            }
         }
         __syncwarp();
     } else {
