@@ -149,22 +149,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int kb = max(0, issued - ns); kb < issued; ++kb) drain(full(kb % ns), (kb / ns) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            bool ok = true;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % ns;
-                if (!(ok = mbar_wait(full(s), (kb / ns) & 1, abort_flag, WAIT_NS))) break;
-                tc_fence_after();
-                const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
+        // The whole warp waits and one elected lane issues through predicated instructions:
+        // a tcgen05.mma issued by a lone lane of a diverged warp costs that thread more than
+        // the tensor pipe's own time per instruction.
+        const bool leader = elect_one();
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % ns;
+            if (!__all_sync(0xffffffffu, mbar_wait(full(s), (kb / ns) & 1, abort_flag, WAIT_NS)))
+                break;
+            tc_fence_after();
+            const uint32_t sa = sb + s * STAGE, sbb = sa + TILE_A;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t bd = NN ? sdesc_sw128(sbb + kk * 2048, NN_GROUP, 1024)
-                                           : sdesc_sw128(sbb + kk * 32, 16, 1024);
-                    tc_mma(tmem, ad, bd, IDESC, (kb | kk) != 0);
-                }
-                tc_commit(empty(s));
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+                const uint64_t bd = NN ? sdesc_sw128(sbb + kk * 2048, NN_GROUP, 1024)
+                                       : sdesc_sw128(sbb + kk * 32, 16, 1024);
+                tc_mma_if(leader, tmem, ad, bd, IDESC, (kb | kk) != 0);
             }
+            tc_commit_if(leader, empty(s));
+            __syncwarp();
+        }
+        if (leader) {
             tc_commit(done);  // arrives once every MMA above has finished
             drain(done, 0);
         }
