@@ -271,6 +271,11 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM, p.batch * p.k_splits);
     const int kblocks = (p.k_per_split + BK - 1) / BK;
     g.ns = kblocks < 1 ? 1 : (kblocks < T::NS ? kblocks : T::NS);
+    // Many output tiles of a short product (the prefill up-projections: K = 512, thousands
+    // of 128 x 256 tiles): two stages, so that two CTAs share an SM and one's epilogue
+    // overlaps the other's loads and MMAs.
+    if (BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() && kblocks <= 16)
+        g.ns = g.ns < 2 ? g.ns : 2;
     const int smem = g.ns * T::STAGE + SMEM_EXTRA;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
