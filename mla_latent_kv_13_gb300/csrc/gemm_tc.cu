@@ -14,11 +14,13 @@
 // the split keeps every SM streaming weights even when there are few output tiles.
 //
 // Roles (192 threads): warp 0 issues TMA (one lane), warp 1 owns TMEM and issues the
-// MMAs (one lane), warps 2-5 read the accumulator out of TMEM and store it. Waits are
-// bounded (one second); a wait that gives up records MLA_ERR_TIMEOUT.
-// The stage ring holds min(6, k-blocks of a CTA) stages and shared memory is sized to
-// it, so products with little K per tile (the per-head absorptions) run several CTAs
-// per SM instead of one.
+// MMAs (the whole warp waits, one elected lane issues through predicated instructions),
+// warps 2-5 read the accumulator out of TMEM and store it. Waits are bounded (one
+// second); a wait that gives up records MLA_ERR_TIMEOUT.
+// The stage ring holds min(6, k-blocks of a CTA) stages (4 at width 256) and shared
+// memory is sized to it, so products with little K per tile (the per-head absorptions)
+// run several CTAs per SM instead of one; products with many 256-wide tiles and short K
+// take two stages for the same reason.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"

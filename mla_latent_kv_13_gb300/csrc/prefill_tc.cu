@@ -13,8 +13,9 @@
 // with the online softmax (exp2 domain, lazy rescale as in decode) between them. S is
 // double-buffered in TMEM, so the scores of tile t+1 are computed while the softmax works
 // on tile t.
-// Roles (192 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-5 softmax/output
-// (thread = query row = TMEM lane). Every wait is bounded (one second).
+// Roles (192 threads): warp 0 TMA, warp 1 TMEM + MMA issue (converged, one elected lane
+// issues through predicated instructions), warps 2-5 softmax/output (thread = query row =
+// TMEM lane). Every wait is bounded (one second).
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
