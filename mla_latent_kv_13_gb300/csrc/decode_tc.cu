@@ -85,7 +85,7 @@ constexpr uint32_t TM_Q = 288;                // Q chunks 0..6: bf16 pairs, [288
 constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
-constexpr int PF_DIST = 4;                    // tiles prefetched into L2 beyond the stage ring
+constexpr int PF_DIST = 4;                    // tiles prefetched into L2 beyond the rings
 constexpr uint32_t XBYTES = PWARP;            // one warp's message: P rows + (reference, sum)
 
 constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
@@ -94,7 +94,7 @@ constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 static_assert(QS_OFF % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && CH % 1024 == 0,
               "128-byte-swizzled operands need 1024-byte-aligned atoms");
-static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "bulk-copy alignment");
+static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
 static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
 static_assert(2 * (NKV + NK + NV) + 19 <= NBAR, "mbarrier count");
 static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
@@ -155,8 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t s_free = q_ready + 16;
     auto p_ready = [&](int x) { return q_ready + 24 + 8u * x; };  // both P halves of tile parity x
     auto pv_done = [&](int x) { return q_ready + 40 + 8u * x; };  // P.V of tile parity x finished
-    // the peer's P.V of tile parity x finished (its copy of our P half may be overwritten);
-    // arrived on by the peer's tcgen05.commit
+    // the peer's P.V of tile parity x finished (our P half in its buffer x may be
+    // overwritten); arrived on by the peer's tcgen05.commit
     auto rfree = [&](int x) { return q_ready + 56 + 8u * x; };
     const uint32_t mma_drain = q_ready + 72;
     const uint32_t pv_drain = q_ready + 144;
@@ -616,8 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             uint32_t pk[16];
             float e_own = make_p(m_new, pk);
 
-            // buffer x (local half) is free once P.V of tile i-2 has read it and its copy
-            // to the peer has been read out
+            // buffer x (local half) is free once P.V of tile i-2 has read it
             if (i >= 2 && !(ok = wait_w(pv_done(x), ((i >> 1) - 1) & 1))) break;
             float m_peer = -INFINITY, e_peer = 0.f;
             if (wlive) {
