@@ -118,8 +118,9 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  * ranges each sequence is cut into (1..256), merged exactly by their log-sum-exps
  * (split-KV combine); 0 = chosen by the library: such a fixed split when it fits the
  * GPU in one pass, else a balanced schedule (the concatenated token blocks of all
- * sequences cut into one equal share per resident work unit, sequences cut between
- * shares merged the same way).
+ * sequences, each sequence weighted with a fixed start-up cost, cut into one equal
+ * share of the weight per resident work unit; sequences cut between shares merged the
+ * same way; mla_decode_schedule shows the shares).
  * Workspace: mla_decode_workspace_size(B, H, max_seqlen, num_splits) with the
  * same B, H and num_splits; max_seqlen is an upper bound of seqlens.
  */
@@ -135,6 +136,22 @@ mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_spl
  */
 mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *splits,
                              int *launches);
+/*
+ * The balanced schedule for these sequence lengths, computed on the host with the
+ * arithmetic the device uses (no counterpart on the pages; no device memory is touched).
+ * seqlens [B] host int32, clamped to [0, 64 * max_blocks] as on the device; clusters =
+ * the number of work units (the device's resident count in mla_decode_attention; any
+ * value >= 1 here). A sequence with v > 0 token blocks weighs v plus a fixed start-up
+ * cost; work unit c takes the weight range [c*W/P, (c+1)*W/P) of the total W
+ * (P = min(clusters, W)) and the token blocks inside it. Writes the first `capacity`
+ * segments as 5 int32 each: (work unit, sequence, first block, end block, part index or
+ * -1 when the unit writes the sequence's output itself), in work-unit order;
+ * *count = the number of segments (it may exceed capacity; nothing past capacity is
+ * written); *parts (may be null) = the number of fp32 parts merged afterwards.
+ * MLA_ERR_INVALID_ARG on null pointers, B outside 1..4096, max_blocks < 1, clusters < 1.
+ */
+mla_status_t mla_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int clusters,
+                                 int32_t *segs, int capacity, int *count, int *parts);
 mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                                   const mla_bf16_t *kv_cache, int num_blocks,
                                   const int32_t *block_table, int max_blocks,

@@ -1,7 +1,11 @@
 // api.cu -- the C ABI of libmla (declared in include/mla.h): host-side validation,
 // workspace layout, split planning and kernel launches.
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -83,7 +87,7 @@ int sched_clusters(int B, int max_seqlen) {
 }
 
 struct DecodeLayout {
-    size_t tile_start, part_begin, nparts, o_part, lse_part, total;
+    size_t tile_start, wpos, part_begin, nparts, o_part, lse_part, total;
 };
 
 DecodeLayout decode_layout(int B, int H, int max_seqlen, int splits) {
@@ -101,7 +105,8 @@ DecodeLayout decode_layout(int B, int H, int max_seqlen, int splits) {
     const int P = sched_clusters(B, max_seqlen);
     const size_t parts = 2 * (size_t)P;  // each cluster cuts at most two sequences
     L.tile_start = HDR;
-    L.part_begin = L.tile_start + align256((size_t)(B + 1) * 4);
+    L.wpos = L.tile_start + align256((size_t)(B + 1) * 4);
+    L.part_begin = L.wpos + align256((size_t)(B + 1) * 4);
     L.nparts = L.part_begin + align256((size_t)B * 4);
     L.o_part = L.nparts + align256((size_t)B * 4);
     L.lse_part = L.o_part + align256(parts * H * D_C * sizeof(float));
@@ -200,6 +205,58 @@ mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *
     return MLA_OK;
 }
 
+mla_status_t mla_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int clusters,
+                                 int32_t *segs, int capacity, int *count, int *parts) {
+    if (!seqlens || !count || B < 1 || B > 4096 || max_blocks < 1 || clusters < 1 ||
+        capacity < 0 || (capacity > 0 && !segs))
+        return MLA_ERR_INVALID_ARG;
+    // the same arithmetic as the schedule kernel, on the host
+    std::vector<int32_t> tile_start(B + 1), wpos(B + 1), part_begin(B), v(B);
+    long T = 0, W = 0;
+    for (int b = 0; b < B; ++b) {
+        const int L = seqlens[b] < 0 ? 0 : std::min(seqlens[b], max_blocks * BLOCK);
+        v[b] = (L + BLOCK - 1) / BLOCK;
+        tile_start[b] = static_cast<int32_t>(T);
+        wpos[b] = static_cast<int32_t>(W + (v[b] > 0 ? SEG_COST : 0));
+        T += v[b];
+        W += v[b] > 0 ? v[b] + SEG_COST : 0;
+    }
+    if (W > INT32_MAX) return MLA_ERR_INVALID_ARG;
+    tile_start[B] = static_cast<int32_t>(T);
+    wpos[B] = static_cast<int32_t>(W);
+    const int P = W < clusters ? static_cast<int>(W) : clusters;
+    int np_total = 0;
+    for (int b = 0; b < B; ++b) {
+        part_begin[b] = np_total;
+        if (v[b] > 0) {
+            const int c0 = cluster_of_tile(wpos[b], W, P);
+            const int c1 = cluster_of_tile(wpos[b] + v[b] - 1, W, P);
+            if (c1 > c0) np_total += c1 - c0 + 1;
+        }
+    }
+    int n = 0;
+    for (int cl = 0; cl < P; ++cl) {
+        const long r0 = (cl * W) / P, r1 = ((cl + 1) * W) / P;
+        int cursor = sched_first(wpos.data(), B, r0);
+        SchedSegment sg;
+        while (sched_next(tile_start.data(), wpos.data(), part_begin.data(), B, r0, r1, W, P, cl,
+                          &cursor, &sg)) {
+            if (n < capacity) {
+                int32_t *e = segs + 5 * (size_t)n;
+                e[0] = cl;
+                e[1] = sg.b;
+                e[2] = sg.t_begin;
+                e[3] = sg.t_end;
+                e[4] = sg.direct ? -1 : sg.part;
+            }
+            ++n;
+        }
+    }
+    *count = n;
+    if (parts) *parts = np_total;
+    return MLA_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -251,17 +308,19 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     // balanced schedule: tile offsets on the device, P persistent clusters, merge of cut sequences
     const int P = sched_clusters(B, max_seqlen);
     int32_t *tile_start = reinterpret_cast<int32_t *>(w + lay.tile_start);
+    int32_t *wpos = reinterpret_cast<int32_t *>(w + lay.wpos);
     int32_t *part_begin = reinterpret_cast<int32_t *>(w + lay.part_begin);
     int32_t *nparts = reinterpret_cast<int32_t *>(w + lay.nparts);
     p.num_splits = 1;
     p.tiles_per_split = T;
     p.tile_start = tile_start;
+    p.wpos = wpos;
     p.part_begin = part_begin;
     p.nparts = nparts;
     p.o_part = reinterpret_cast<float *>(w + lay.o_part);
     p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
-    if (launch_decode_schedule(seqlens, B, max_blocks, P, tile_start, part_begin, nparts, p.err,
-                               st) != cudaSuccess)
+    if (launch_decode_schedule(seqlens, B, max_blocks, P, tile_start, wpos, part_begin, nparts,
+                               p.err, st) != cudaSuccess)
         return MLA_ERR_CUDA;
     if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_status(launch_combine_sched(p.o_part, p.lse_part, tile_start, part_begin, nparts,

@@ -96,7 +96,11 @@ static_assert(QS_OFF % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && CH
               "128-byte-swizzled operands need 1024-byte-aligned atoms");
 static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
 static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
-static_assert(2 * (NKV + NK + NV) + 19 <= NBAR, "mbarrier count");
+static_assert(2 * (NKV + NK + NV) + 20 <= NBAR, "mbarrier count");
+// Q rows staged in the idle rings between segments: one row (q_lat then q_rope) per
+// 1168 bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
+constexpr int QSTG = 2 * (D_C + D_ROPE) + 16;
+static_assert(128 * QSTG <= QS_OFF - KV_OFF && QSTG % 16 == 0, "Q staging area");
 static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -160,6 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     auto rfree = [&](int x) { return q_ready + 56 + 8u * x; };
     const uint32_t mma_drain = q_ready + 72;
     const uint32_t pv_drain = q_ready + 144;
+    const uint32_t qs_full = q_ready + 152;  // the next segment's Q rows staged
     // the peer's P half of the rows of warp quadrant q has landed in buffer x
     auto recv_full = [&](int q, int x) { return q_ready + 80 + 8u * (2 * q + x); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
@@ -188,6 +193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         mbar_init(mma_drain, 1);
         mbar_init(pv_drain, 1);
+        mbar_init(qs_full, 4);
         for (int k = 0; k < 8; ++k) mbar_init(recv_full(k >> 1, k & 1), 1);
         fence_mbar_init();
     };
@@ -209,26 +215,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     grid_dependency_wait();  // q, the cache rows and the schedule come from predecessor kernels
 
     // ---- work: one (sequence, token range) per cluster, or, with the balanced
-    // schedule, the segments of this cluster's equal share of the concatenated tiles
+    // schedule, the segments of this cluster's equal share of the weighted tile list
     const bool sched = p.tile_start != nullptr;
     const int cl = blockIdx.x >> 1;
     int P = gridDim.x >> 1;
-    long T = 0, r0 = 0, r1 = 0;
+    long W = 0, r0 = 0, r1 = 0;
     int seg_b = 0;
     if (sched) {
-        T = p.tile_start[p.B];
-        if (T < P) P = static_cast<int>(T);  // as in the schedule: no empty ranges
+        W = p.wpos[p.B];
+        if (W < P) P = static_cast<int>(W);  // as in the schedule: no empty ranges
         if (cl < P) {
-            r0 = (cl * T) / P;
-            r1 = ((cl + 1) * T) / P;
+            r0 = (cl * W) / P;
+            r1 = ((cl + 1) * W) / P;
         }
-        int lo = 0, hi = p.B - 1;  // largest b with tile_start[b] <= r0
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.tile_start[mid] <= r0) lo = mid;
-            else hi = mid - 1;
-        }
-        seg_b = lo;
+        seg_b = sched_first(p.wpos, p.B, r0);
     }
 
     int q_for = -1;  // softmax warps: the sequence whose Q rows are in TMEM / shared memory
@@ -246,14 +246,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         direct = p.num_splits == 1;
         part = b * p.num_splits + split;
     } else {
-        while (seg_b < p.B && p.tile_start[seg_b + 1] == p.tile_start[seg_b]) ++seg_b;
-        if (seg_b >= p.B || p.tile_start[seg_b] >= r1 || r0 >= r1) break;
-        b = seg_b++;
-        const long ts = p.tile_start[b], te = p.tile_start[b + 1];
-        t_begin = static_cast<int>((r0 > ts ? r0 : ts) - ts);
-        t_end = static_cast<int>((r1 < te ? r1 : te) - ts);
-        direct = ts >= r0 && te <= r1;
-        part = direct ? 0 : p.part_begin[b] + (cl - cluster_of_tile(ts, T, P));
+        SchedSegment sg;
+        if (!sched_next(p.tile_start, p.wpos, p.part_begin, p.B, r0, r1, W, P, cl, &seg_b, &sg))
+            break;
+        b = sg.b;
+        t_begin = sg.t_begin;
+        t_end = sg.t_end;
+        direct = sg.direct;
+        part = sg.part;
     }
     int L = p.seqlens[b];
     if (L < 0 || L > p.max_blocks * TOK) {
@@ -282,14 +282,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // Near the end of a scheduled segment, warm L2 with the next segment's Q rows
             // and first tiles, so that its start does not wait on HBM round trips.
             auto prefetch_next = [&]() {
-                int nb = seg_b;  // first sequence after b that has tiles
-                while (nb < p.B && p.tile_start[nb + 1] == p.tile_start[nb]) ++nb;
-                if (nb >= p.B || p.tile_start[nb] >= r1) return;
+                const int nb = sched_peek(p.tile_start, p.wpos, p.B, r1, seg_b);
+                if (nb < 0) return;  // no further sequence in this cluster's share
                 bulk_prefetch_l2(p.q_lat + (size_t)nb * H * D_C, static_cast<uint32_t>(H * D_C * 2));
                 bulk_prefetch_l2(p.q_rope + (size_t)nb * H * D_ROPE,
                                  static_cast<uint32_t>(H * D_ROPE * 2));
-                const long ts = p.tile_start[nb], te = p.tile_start[nb + 1];
-                const long nt = min(static_cast<long>(NKV + PF_DIST), min(r1, te) - ts);
+                const long ws = p.wpos[nb], we = ws + (p.tile_start[nb + 1] - p.tile_start[nb]);
+                const long nt = min(static_cast<long>(NKV + PF_DIST), min(r1, we) - ws);
                 const int32_t *bt = p.block_table + (size_t)nb * p.max_blocks;
                 for (int t = 0; t < nt; ++t) {
                     const int blk = bt[t];
@@ -712,20 +711,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_ready(x));
         }
-        // The last score product of this segment is done (its scores were read): load the
-        // next scheduled segment's Q rows now, so that they are in place when it starts.
-        if (sched && ok && n > 0) {
-            int nb = seg_b;
-            while (nb < p.B && p.tile_start[nb + 1] == p.tile_start[nb]) ++nb;
-            if (nb < p.B && p.tile_start[nb] < r1) {
-                load_q(nb);
-                q_for = nb;
-            }
-        }
         // ------------------------------------------------------------- output
+        const int nb = sched && ok && n > 0 ? sched_peek(p.tile_start, p.wpos, p.B, r1, seg_b)
+                                            : -1;
         const int col0 = 256 * rank;
         if (n > 0 && ok && wait_w(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1)) {
             tc_fence_after();
+            // Every product of this segment is done, so the rings are idle: the next
+            // scheduled segment's Q rows are copied into them (one bulk copy per row and
+            // array) while the output rows are written, then moved to their places.
+            if (nb >= 0) {
+                const int live = min(max(H - 32 * wq, 0), 32);
+                if (lane == 0) mbar_arrive_expect_tx(qs_full, live * 2 * (D_C + D_ROPE));
+                __syncwarp();
+                if (live_row) {
+                    const uint32_t dst = sb + KV_OFF + row * QSTG;
+                    bulk_load(dst, p.q_lat + ((size_t)nb * H + row) * D_C, 2 * D_C, qs_full);
+                    bulk_load(dst + 2 * D_C, p.q_rope + ((size_t)nb * H + row) * D_ROPE,
+                              2 * D_ROPE, qs_full);
+                }
+            }
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
@@ -757,6 +762,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                                  __uint_as_float(r[4 * k + 2]) * inv,
                                                  __uint_as_float(r[4 * k + 3]) * inv);
                     }
+                }
+            }
+            if (nb >= 0) {
+                if ((ok = wait_w(qs_full, 0))) {
+                    const uint32_t src = sb + KV_OFF + row * QSTG;
+                    const uint32_t qrow = sb + QS_OFF + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll 1
+                    for (int c = 0; c < NOWN; ++c) {
+                        uint4 v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            v[k] = live_row ? ld_shared_v4(src + 128 * c + 16 * k)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                        if (c < NQT) {
+                            uint32_t r[32];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                r[4 * k] = v[k].x;
+                                r[4 * k + 1] = v[k].y;
+                                r[4 * k + 2] = v[k].z;
+                                r[4 * k + 3] = v[k].w;
+                            }
+                            tmem_st32(tl + TM_Q + 32 * c, r);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                st_shared_v4(qrow + (c - NQT) * QCH + ((k ^ (row & 7)) << 4),
+                                             v[k].x, v[k].y, v[k].z, v[k].w);
+                        }
+                    }
+                    q_for = nb;
+                } else if (lane == 0) {
+                    drain_wait(qs_full, 0);  // copies still in flight land before exit
                 }
             }
         } else if (row < H) {

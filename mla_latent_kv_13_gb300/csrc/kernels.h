@@ -51,23 +51,85 @@ struct DecodeParams {
     float *lse_part;           // [B][S][H]      (num_splits > 1); [2P][H]      if scheduled
     uint32_t *err;
     // Balanced schedule (num_splits == 0): P clusters each take an equal contiguous range
-    // of the concatenated tile list; sequences cut between clusters become parts.
+    // of the weighted tile list; sequences cut between clusters become parts.
     const int32_t *tile_start;  // [B+1] exclusive prefix of tiles per sequence
+    const int32_t *wpos;        // [B+1] weight position of each sequence's first tile; [B] = W
     const int32_t *part_begin;  // [B]   first part index of a sequence that is cut
     const int32_t *nparts;      // [B]   number of parts (0 = whole in one cluster)
 };
 
-// The cluster (of P) whose tile range [c*T/P, (c+1)*T/P) holds global tile t.
-__host__ __device__ inline int cluster_of_tile(long t, long T, int P) {
-    long c = (t * P) / T;
-    while (c + 1 < P && ((c + 1) * T) / P <= t) ++c;
-    while (c > 0 && (c * T) / P > t) --c;
+// Balanced schedule. A sequence with v > 0 tiles weighs SEG_COST + v: a segment (the
+// piece of one sequence that one cluster processes) costs about as much to start and to
+// finish -- Q rows loaded, rings filled, the output rows written -- as SEG_COST tiles of
+// the steady loop. With the weights laid end to end, sequence b owns the weight range
+// [wpos[b] - SEG_COST, wpos[b] + v): its start-up first, then one position per tile.
+// Cluster c of P takes the weight range [c*W/P, (c+1)*W/P) (W = total weight) and
+// processes the tiles that fall inside it, so a cluster that starts many short sequences
+// gets fewer tiles than one that streams a long one.
+constexpr int SEG_COST = 12;
+
+// The cluster (of P) whose range [c*W/P, (c+1)*W/P) holds weight position t.
+__host__ __device__ inline int cluster_of_tile(long t, long W, int P) {
+    long c = (t * P) / W;
+    while (c + 1 < P && ((c + 1) * W) / P <= t) ++c;
+    while (c > 0 && (c * W) / P > t) --c;
     return static_cast<int>(c);
 }
 
+// One segment of a cluster's share: tiles [t_begin, t_end) of sequence b, written straight
+// to the output (direct) or as fp32 part `part` of a sequence cut between clusters.
+struct SchedSegment {
+    int b, t_begin, t_end, part;
+    bool direct;
+};
+
+// Largest b with wpos[b] <= r0 (the first sequence that may have tiles in [r0, r1)).
+__host__ __device__ inline int sched_first(const int32_t *wpos, int B, long r0) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wpos[mid] <= r0) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The next segment of cluster cl (range [r0, r1) of W, P ranges) at or after sequence
+// *cursor, which advances past it; false when the share has no further tiles.
+__host__ __device__ inline bool sched_next(const int32_t *tile_start, const int32_t *wpos,
+                                           const int32_t *part_begin, int B, long r0, long r1,
+                                           long W, int P, int cl, int *cursor,
+                                           SchedSegment *s) {
+    int b = *cursor;
+    while (b < B) {  // skip empty sequences and one whose tiles end before the range
+        const int v = tile_start[b + 1] - tile_start[b];
+        if (v > 0 && wpos[b] + v > r0) break;
+        ++b;
+    }
+    if (b >= B || wpos[b] >= r1 || r0 >= r1) {
+        *cursor = b;
+        return false;
+    }
+    *cursor = b + 1;
+    const long ws = wpos[b], we = ws + (tile_start[b + 1] - tile_start[b]);
+    s->b = b;
+    s->t_begin = static_cast<int>((r0 > ws ? r0 : ws) - ws);
+    s->t_end = static_cast<int>((r1 < we ? r1 : we) - ws);
+    s->direct = ws >= r0 && we <= r1;
+    s->part = s->direct ? 0 : part_begin[b] + (cl - cluster_of_tile(ws, W, P));
+    return true;
+}
+
+// The first sequence at or after b with tiles, if its first tile lies before r1; else -1.
+__host__ __device__ inline int sched_peek(const int32_t *tile_start, const int32_t *wpos, int B,
+                                          long r1, int b) {
+    while (b < B && tile_start[b + 1] == tile_start[b]) ++b;
+    return b < B && wpos[b] < r1 ? b : -1;
+}
+
 cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
-                                   int32_t *tile_start, int32_t *part_begin, int32_t *nparts,
-                                   uint32_t *err, cudaStream_t stream);
+                                   int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
+                                   int32_t *nparts, uint32_t *err, cudaStream_t stream);
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
                                  const int32_t *tile_start, const int32_t *part_begin,
                                  const int32_t *nparts, int B, int H, uint16_t *out, float *lse,

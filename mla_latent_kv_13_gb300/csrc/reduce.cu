@@ -141,11 +141,13 @@ __device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_to
     return total;
 }
 
-// One CTA of 1024 threads (B <= 4096): tiles per sequence -> tile_start; parts of the
-// sequences that the equal split of the tile list cuts between clusters.
+// One CTA of 1024 threads (B <= 4096): tiles per sequence -> tile_start; weighted
+// positions (SEG_COST + tiles per sequence with tiles) -> wpos; parts of the sequences that
+// the equal split of the total weight cuts between clusters.
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seqlens, int B,
                                                                int max_blocks, int P,
                                                                int32_t *tile_start,
+                                                               int32_t *wpos,
                                                                int32_t *part_begin,
                                                                int32_t *nparts, uint32_t *err) {
     __shared__ int v[4096], ex[4096], warp_tot[33];
@@ -161,20 +163,27 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
     }
     __syncthreads();
     const int T = block_exclusive_scan4(v, B, ex, warp_tot);
-    // never more ranges than tiles, so that every range is non-empty and a sequence cut
-    // between clusters c0..c1 gets exactly one part from each of them
-    const int Pe = T < P ? T : P;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) tile_start[b] = ex[b];
+    if (threadIdx.x == 0) tile_start[B] = T;
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) ex[b] = v[b] > 0 ? v[b] + SEG_COST : 0;
+    __syncthreads();
+    const int W = block_exclusive_scan4(ex, B, ex, warp_tot);  // in place
+    // never more ranges than weight positions, so that every range is non-empty and a
+    // sequence cut between clusters c0..c1 gets exactly one part from each of them
+    const int Pe = W < P ? W : P;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        tile_start[b] = ex[b];
+        const int w0 = ex[b] + (v[b] > 0 ? SEG_COST : 0);
+        wpos[b] = w0;
         int np = 0;
-        if (v[b] > 0 && T > 0) {
-            const int c0 = cluster_of_tile(ex[b], T, Pe);
-            const int c1 = cluster_of_tile(ex[b] + v[b] - 1, T, Pe);
+        if (v[b] > 0) {
+            const int c0 = cluster_of_tile(w0, W, Pe);
+            const int c1 = cluster_of_tile(w0 + v[b] - 1, W, Pe);
             np = c1 > c0 ? c1 - c0 + 1 : 0;
         }
         nparts[b] = np;
     }
-    if (threadIdx.x == 0) tile_start[B] = T;
+    if (threadIdx.x == 0) wpos[B] = W;
     __syncthreads();
     for (int b = threadIdx.x; b < B; b += blockDim.x) v[b] = nparts[b];
     __syncthreads();
@@ -205,10 +214,10 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
 }  // namespace
 
 cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
-                                   int32_t *tile_start, int32_t *part_begin, int32_t *nparts,
-                                   uint32_t *err, cudaStream_t stream) {
+                                   int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
+                                   int32_t *nparts, uint32_t *err, cudaStream_t stream) {
     return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
-                      max_blocks, P, tile_start, part_begin, nparts, err);
+                      max_blocks, P, tile_start, wpos, part_begin, nparts, err);
 }
 
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,

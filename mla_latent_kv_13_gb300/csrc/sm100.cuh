@@ -179,6 +179,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// Copy `bytes` (a multiple of 16) from global memory into this CTA's shared memory, both
+// addresses 16-byte aligned; completes `bytes` of transaction count on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 // Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte-aligned address into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *addr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)),

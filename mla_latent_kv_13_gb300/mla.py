@@ -48,6 +48,8 @@ _SIGS = {
     "mla_append_kv": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _f, _vp, _sz, _vp], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _szp], _i),
     "mla_decode_plan": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
+    "mla_decode_schedule": ([_vp, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
+                            _i),
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
@@ -140,6 +142,27 @@ def decode_plan(B, H, max_seqlen, num_splits=0):
     if rc != 0:
         raise MLAError(rc, "mla_decode_plan")
     return s.value, n.value
+
+
+def decode_schedule(seqlens, max_blocks, clusters):
+    """The balanced schedule for these lengths, computed on the host: a list of segments
+    (work unit, sequence, first block, end block, part or -1 when written directly) and
+    the number of fp32 parts."""
+    import numpy as np
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    cnt, parts = _i(0), _i(0)
+
+    def call(buf, cap):
+        rc = _lib.mla_decode_schedule(sl.ctypes.data_as(ctypes.c_void_p), len(sl), max_blocks,
+                                      clusters, buf.ctypes.data_as(ctypes.c_void_p), cap,
+                                      ctypes.byref(cnt), ctypes.byref(parts))
+        if rc != 0:
+            raise MLAError(rc, "mla_decode_schedule")
+
+    call(np.zeros((1, 5), dtype=np.int32), 0)  # count only
+    buf = np.zeros((max(cnt.value, 1), 5), dtype=np.int32)
+    call(buf, cnt.value)
+    return [tuple(int(x) for x in r) for r in buf[:cnt.value]], parts.value
 
 
 def absorb_q_workspace_size(B, d_model, q_lora, H):

@@ -116,3 +116,86 @@ def test_prefill_validation_before_launch(lib):
     assert lib.mla_prefill_workspace_size(48, 0, 64, ctypes.byref(sz)) == 2
     assert lib.mla_prefill_workspace_size(16, -1, 64, ctypes.byref(sz)) == 1
     assert lib.mla_prefill_workspace_size(16, 0, 0, ctypes.byref(sz)) == 1
+
+
+def _check_schedule(seqlens, max_blocks, clusters, seg_cost=12):
+    """Invariants of the balanced schedule (host arithmetic shared with the device)."""
+    import numpy as np
+    from mla_latent_kv_13_gb300 import mla
+    segs, parts = mla.decode_schedule(seqlens, max_blocks, clusters)
+    tiles = [(min(max(int(L), 0), 64 * max_blocks) + 63) // 64 for L in seqlens]
+    W = sum(v + seg_cost for v in tiles if v > 0)
+    P = min(clusters, W)
+    covered = [np.zeros(v, dtype=np.int32) for v in tiles]
+    by_cluster, parts_of = {}, {}
+    for cl, b, t0, t1, part in segs:
+        assert 0 <= cl < P and 0 <= t0 < t1 <= tiles[b]
+        covered[b][t0:t1] += 1
+        by_cluster.setdefault(cl, []).append((b, t0, t1))
+        if part < 0:
+            assert (t0, t1) == (0, tiles[b])  # written directly: the whole sequence
+        else:
+            parts_of.setdefault(b, []).append((cl, part))
+    for c in covered:  # every tile of every sequence exactly once
+        assert (c == 1).all()
+    # a cluster's segments run in sequence order; only its first and last may be cut
+    for cl, ss in by_cluster.items():
+        assert [s[0] for s in ss] == sorted(s[0] for s in ss)
+        for k, (b, t0, t1) in enumerate(ss):
+            if 0 < k < len(ss) - 1:
+                assert (t0, t1) == (0, tiles[b])
+    # the parts of a cut sequence: consecutive clusters, consecutive indices in token order
+    idx = sorted(p for ps in parts_of.values() for _, p in ps)
+    assert idx == list(range(parts)) and parts <= 2 * max(P, 1)
+    for b, ps in parts_of.items():
+        assert len(ps) >= 2
+        cls = [c for c, _ in ps]
+        assert cls == list(range(cls[0], cls[0] + len(ps)))
+        assert [p for _, p in ps] == list(range(ps[0][1], ps[0][1] + len(ps)))
+    # balance: no cluster costs more than its share of the weight plus one start-up
+    share = -(-W // P) if P else 0
+    for ss in by_cluster.values():
+        assert sum(seg_cost + t1 - t0 for _, t0, t1 in ss) <= share + seg_cost
+    return segs, parts, by_cluster
+
+
+def test_balanced_schedule_covers_every_tile_once(lib):
+    import numpy as np
+    from mla_latent_kv_13_gb300 import synth
+    rng = np.random.default_rng(5)
+    cases = [
+        (synth.draw_seqlens(synth.WORKLOADS["mixed"]), 128, 76),   # lengths 1024..8192
+        (np.full(128, 8192), 128, 76),                             # equal lengths
+        (np.full(76, 8192), 128, 76),
+        ([0, 0, 64, 0, 1, 4096, 0], 64, 76),                       # empties, fewer tiles than units
+        ([100, 5000, 0, 70000, 1, 65, 640], 1200, 13),             # one dominant sequence
+        (rng.integers(0, 3000, 1000), 47, 152),                    # many short ones
+        ([8192], 128, 1),
+        ([0, 0, 0], 4, 76),                                        # nothing to do
+        ([-5, 10 ** 6, 128], 4, 3),                                # clamped like the device
+    ]
+    for seqlens, mb, clusters in cases:
+        _check_schedule(np.asarray(seqlens, dtype=np.int32), mb, clusters)
+
+
+def test_balanced_schedule_weights_segment_starts(lib):
+    """A unit that starts several short sequences gets fewer tiles than one that streams a
+    long one: on the mixed-length batch no unit carries more than its share of tiles plus
+    start-ups, where equal tile counts would give units of 2 and 5 segments alike."""
+    import numpy as np
+    from mla_latent_kv_13_gb300 import mla, synth
+    seqlens = synth.draw_seqlens(synth.WORKLOADS["mixed"])
+    segs, parts, by_cluster = _check_schedule(seqlens, 128, 76)
+    tiles = {cl: sum(t1 - t0 for _, t0, t1 in ss) for cl, ss in by_cluster.items()}
+    nseg = {cl: len(ss) for cl, ss in by_cluster.items()}
+    few = [tiles[c] for c in tiles if nseg[c] == min(nseg.values())]
+    many = [tiles[c] for c in tiles if nseg[c] == max(nseg.values())]
+    assert min(few) > max(many)
+    with pytest.raises(mla.MLAError):
+        mla.decode_schedule(seqlens, 128, 0)
+    n = ctypes.c_int(0)
+    assert lib.mla_decode_schedule(None, 4, 4, 4, None, 0, ctypes.byref(n), None) == 1
+    sl = (ctypes.c_int32 * 2)(64, 64)
+    assert lib.mla_decode_schedule(sl, 2, 4, 4, None, 0, ctypes.byref(n), None) == 0
+    assert n.value >= 1
+    assert lib.mla_decode_schedule(sl, 2, 4, 4, None, 3, ctypes.byref(n), None) == 1
