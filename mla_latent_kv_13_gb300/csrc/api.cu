@@ -54,8 +54,8 @@ void plan_ksplit(int M, int N, int K, int batch, int &splits, int &per) {
 // fixed split (fewest waves x tiles per range, plus the partials' traffic, assuming all
 // sequences are max_seqlen long) is used when it fits in one wave of clusters; when it
 // would not, 0 is returned: the balanced schedule (equal shares of the concatenated
-// tiles) avoids the partly empty last wave, at the price of restarting the pipeline at
-// every sequence boundary inside a share.
+// tiles, each sequence weighted with its start-up cost) avoids the partly empty last wave,
+// at the price of restarting the pipeline at every sequence boundary inside a share.
 int plan_decode_splits(int B, int H, int max_seqlen, int requested) {
     if (requested > 0) return requested;
     int T = (max_seqlen + BLOCK - 1) / BLOCK;

@@ -2,7 +2,8 @@
 // (tcgen05 + TMEM), fed by TMA, one 2-CTA thread-block cluster per work item.
 //
 // Work item = (sequence b, token range s); with the balanced schedule a cluster runs the
-// segments of one equal share of all sequences' tiles in turn. All heads of a sequence
+// segments of its share of all sequences' tiles in turn (shares equal in tiles plus a fixed
+// start-up cost per sequence). All heads of a sequence
 // score the same latent cache rows [c_kv (512) | k_rope (64)], so the 128 head rows form
 // the M = 128 side of both products:
 //   S   = Q [128 x 576] . K^T [576 x tokens]   (scores)

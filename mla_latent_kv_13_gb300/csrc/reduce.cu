@@ -1,5 +1,6 @@
 // reduce.cu -- the two reductions of the path: the split-KV merge of decode partials
-// (exact log-sum-exp weighting) and the sum of split-K GEMM partials into bf16.
+// (exact log-sum-exp weighting) and the sum of split-K GEMM partials into bf16; and the
+// balanced decode schedule's device-side offsets, weights and part counts.
 #include "common.cuh"
 #include "kernels.h"
 
