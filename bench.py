@@ -11,9 +11,11 @@ needed between steps.
 
 `value` is the step's algorithmic bytes (latent cache rows read once, weights read
 once, q/out/new-row traffic) per second, summed over all ranks. `e2e` is the same
-metric through the public Python API with the step's per-token inputs (hidden
-states, positions, lengths) copied from pinned host memory and the output y copied
-back inside the timed region; the cache and weights are device-resident state.
+metric through the public Python API (DecodeStep) with every step's per-token
+inputs (hidden states, positions, lengths) copied from pinned host memory and its
+output y copied back inside the timed region, on a copy stream with double buffers
+so that the transfers overlap the neighbouring steps' kernels, as a serving loop
+would; the cache and weights are device-resident state.
 
 --impl reference times the fp64 CPU oracle (the only other implementation) on a
 bounded sample of the same workload on this machine's host cores.
@@ -288,9 +290,15 @@ def run_gpu(args, d, costs, metric, unit):
     start.record(stream)
     w = step.w
     for i in range(args.steps):
-        mla.append_kv(h, w["w_dkr"], pos, bt, cache, step.theta, step.ws_append)
+        # the same launches and streams as DecodeStep (the append on its side stream, next
+        # to the query projections), with events around the attention launch
+        step.ev_fork.record(stream)
+        step.side.wait_event(step.ev_fork)
+        mla.append_kv(h, w["w_dkr"], pos, bt, cache, step.theta, step.ws_append, step.side)
+        step.ev_join.record(step.side)
         mla.absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, step.theta,
-                     step.q_lat, step.q_rope, step.ws_q)
+                     step.q_lat, step.q_rope, step.ws_q, stream)
+        stream.wait_event(step.ev_join)
         ev[i][0].record(stream)
         mla.decode_attention(step.q_lat, step.q_rope, cache, bt, L, max_len, step.scale,
                              step.num_splits, step.o_lat, step.lse, step.ws_att)
@@ -318,14 +326,47 @@ def run_gpu(args, d, costs, metric, unit):
         step(h_dev.view(torch.bfloat16), pos, L, bt, cache)
     torch.cuda.synchronize(dev)
     _barrier(world)
+    # A serving loop: each step's inputs go up and its result comes down on a copy stream,
+    # double-buffered, so that the transfers overlap the neighbouring steps' kernels; every
+    # step's copies are still inside the timed region.
+    copy_s = torch.cuda.Stream(dev)
+    ins = [(torch.empty_like(h_dev), torch.empty_like(pos_dev), torch.empty_like(L_dev))
+           for _ in range(2)]
+    ys = [torch.empty((B, d["d_model"]), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    y_done = [torch.cuda.Event() for _ in range(2)]
+    y_read = [torch.cuda.Event() for _ in range(2)]
+
+    def upload(i):
+        k = i % 2
+        with torch.cuda.stream(copy_s):
+            if i >= 2:
+                copy_s.wait_event(in_free[k])  # step i-2 has read this buffer
+            ins[k][0].copy_(h_host, non_blocking=True)
+            ins[k][1].copy_(pos_host, non_blocking=True)
+            ins[k][2].copy_(L_host, non_blocking=True)
+            in_ready[k].record(copy_s)
+
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        h_dev.copy_(h_host, non_blocking=True)
-        pos_dev.copy_(pos_host, non_blocking=True)
-        L_dev.copy_(L_host, non_blocking=True)
-        y = step(h_dev.view(torch.bfloat16), pos_dev, L_dev, bt, cache)
-        y_host.copy_(y.view(torch.int16), non_blocking=True)
+    copy_s.wait_event(e0)
+    upload(0)
+    for i in range(args.steps):
+        k = i % 2
+        if i + 1 < args.steps:
+            upload(i + 1)
+        stream.wait_event(in_ready[k])
+        if i >= 2:
+            stream.wait_event(y_read[k])  # the result of step i-2 has left this buffer
+        step(ins[k][0].view(torch.bfloat16), ins[k][1], ins[k][2], bt, cache, out=ys[k])
+        in_free[k].record(stream)
+        y_done[k].record(stream)
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(y_done[k])
+            y_host.copy_(ys[k].view(torch.int16), non_blocking=True)
+            y_read[k].record(copy_s)
+    stream.wait_event(y_read[(args.steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)

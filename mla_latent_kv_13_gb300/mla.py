@@ -380,8 +380,11 @@ class DecodeStep:
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()
 
-    def __call__(self, h, pos, seqlens_after, block_table, kv_cache, stream=None):
+    def __call__(self, h, pos, seqlens_after, block_table, kv_cache, stream=None, out=None):
+        """One step; the result y [B, d_model] bf16 goes to `out` if given, else to the
+        step's own buffer (returned either way)."""
         w = self.w
+        y = self.y if out is None else out
         main = torch.cuda.current_stream() if stream is None else stream
         self.ev_fork.record(main)
         self.side.wait_event(self.ev_fork)
@@ -394,8 +397,8 @@ class DecodeStep:
         decode_attention(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
                          self.max_seqlen, self.scale, self.num_splits, self.o_lat, self.lse,
                          self.ws_att, main)
-        out_absorb(self.o_lat, w["w_uv"], w["w_o"], self.y, self.ws_out, main)
-        return self.y
+        out_absorb(self.o_lat, w["w_uv"], w["w_o"], y, self.ws_out, main)
+        return y
 
     def check(self, stream=None) -> int:
         codes = [check_device_status(ws, stream) for ws in
