@@ -49,6 +49,7 @@ template <int BN> struct Tile {
 struct TcGemmArgs {
     int M, N, K, batch, k_splits, k_per_split;
     int ns;     // stages in the ring (1..NS)
+    int tma_c;  // bf16 output written from shared memory by TMA stores (map_c)
     int a_bx;   // A column offset per batch
     int b_bx;   // B (TN) column offset per batch
     int b_by;   // B row offset per batch (TN: rows of N; NN: rows of K)
@@ -57,6 +58,21 @@ struct TcGemmArgs {
     long ldc, c_bstride;
     uint32_t *err;
 };
+
+// Store the box at (x, y) of a tensor map from this CTA's shared memory (bulk async-group;
+// x * element size a multiple of 16 bytes, x and y not negative).
+__device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     uint64_t t0 = globaltimer_ns();
@@ -67,7 +83,8 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 template <bool NN, int BN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, TcGemmArgs g) {
+                   const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_c, TcGemmArgs g) {
     constexpr int STAGE = Tile<BN>::STAGE;
     constexpr uint32_t TMEM_COLS = BN;
     constexpr uint32_t IDESC = idesc_bf16(BM, BN, false, NN);
@@ -104,6 +121,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
+        if (g.tma_c) tma_prefetch_map(&map_c);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -183,7 +201,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const bool ok =
             __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
-        if (ok) {
+        if (ok && g.tma_c) {
+            // bf16 tile through shared memory: every product is done, so the stage ring is
+            // idle; each 64-column group becomes one 128-byte-swizzled 128 x 64 box (row r at
+            // r * 128 bytes, its 16-byte chunks permuted by r % 8), written by one TMA store
+            tc_fence_after();
+            const int r = wq * 32 + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tl + 32 * c, v);
+                tmem_ld_wait();
+                const uint32_t rowp = sb + (c >> 1) * (BM * 128) + r * 128;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int ch = (c & 1) * 4 + k;
+                    st_shared_v4(rowp + ((ch ^ (r & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+                }
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+            if (warp == 2 && lane == 0) {
+                for (int j = 0; j < BN / 64 && n0 + 64 * j < g.N; ++j)
+                    tma_store_2d(&map_c, sb + j * (BM * 128),
+                                 static_cast<int>(batch * g.c_bstride) + n0 + 64 * j, m0);
+                bulk_commit();
+                bulk_wait_read_all();  // the boxes have left shared memory before exit
+            }
+        } else if (ok) {
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -279,10 +328,19 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     if (BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() && kblocks <= 16)
         g.ns = g.ns < 2 ? g.ns : 2;
     const int smem = g.ns * T::STAGE + SMEM_EXTRA;
+    // bf16 output through TMA stores when every batch's slice is a column range of one
+    // [M][ldc] matrix (x offsets multiples of 64 elements) and the ring holds the tile
+    CUtensorMap mc = ma;
+    g.tma_c = 0;
+    if (p.c_bf16 && !p.c_part && p.N % 64 == 0 && p.c_bstride % 64 == 0 && p.ldc % 8 == 0 &&
+        (reinterpret_cast<uintptr_t>(p.c_bf16) & 15) == 0 &&
+        (long)(p.batch - 1) * p.c_bstride + p.N <= p.ldc && g.ns * T::STAGE >= BM * BN * 2 &&
+        map_2d(&mc, p.c_bf16, (uint64_t)p.ldc, (uint64_t)p.M, (uint64_t)p.ldc, BM))
+        g.tma_c = 1;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tc_kernel<NN, BN>, grid, dim3(NTHREADS), smem, stream, ma, mb, g);
+    return launch_pdl(gemm_tc_kernel<NN, BN>, grid, dim3(NTHREADS), smem, stream, ma, mb, mc, g);
 }
 
 }  // namespace
