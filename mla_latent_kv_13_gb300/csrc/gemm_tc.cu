@@ -49,7 +49,8 @@ template <int BN> struct Tile {
 struct TcGemmArgs {
     int M, N, K, batch, k_splits, k_per_split;
     int ns;     // stages in the ring (1..NS)
-    int tma_c;  // bf16 output written from shared memory by TMA stores (map_c)
+    int tma_c;  // output written from shared memory by TMA stores (map_c): 1 = bf16 C,
+                //   2 = fp32 split-K partials (3-D map: columns, rows, split x batch)
     int a_bx;   // A column offset per batch
     int b_bx;   // B (TN) column offset per batch
     int b_by;   // B row offset per batch (TN: rows of N; NN: rows of K)
@@ -66,6 +67,13 @@ __device__ __forceinline__ void tma_store_2d(const void *map, uint32_t src, int 
                      reinterpret_cast<uint64_t>(map)),
                  "r"(src), "r"(x), "r"(y)
                  : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -201,7 +209,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const bool ok =
             __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
-        if (ok && g.tma_c) {
+        if (ok && g.tma_c == 2) {
+            // fp32 partials the same way: each 32-column chunk is one 128-byte-swizzled
+            // 128 x 32 box of the [split x batch][M][N] partial array
+            tc_fence_after();
+            const int r = wq * 32 + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tl + 32 * c, v);
+                tmem_ld_wait();
+                const uint32_t rowp = sb + c * (BM * 128) + r * 128;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(rowp + ((k ^ (r & 7)) << 4), v[4 * k], v[4 * k + 1], v[4 * k + 2],
+                                 v[4 * k + 3]);
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+            if (warp == 2 && lane == 0) {
+                for (int c = 0; c < BN / 32 && n0 + 32 * c < g.N; ++c)
+                    tma_store_3d(&map_c, sb + c * (BM * 128), n0 + 32 * c, m0,
+                                 split * g.batch + batch);
+                bulk_commit();
+                bulk_wait_read_all();  // the boxes have left shared memory before exit
+            }
+        } else if (ok && g.tma_c) {
             // bf16 tile through shared memory: every product is done, so the stage ring is
             // idle; each 64-column group becomes one 128-byte-swizzled 128 x 64 box (row r at
             // r * 128 bytes, its 16-byte chunks permuted by r % 8), written by one TMA store
@@ -315,6 +348,21 @@ bool map_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 array [slices][rows][cols] (contiguous) as a 3-D map with 128-byte-swizzled boxes of
+// 32 columns x 128 rows x 1 slice.
+bool map_3d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t slices) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, rows, slices};
+    cuuint64_t strides[2] = {cols * 4, cols * rows * 4};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool NN, int BN>
 cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs g,
                         const GemmParams &p, cudaStream_t stream) {
@@ -337,6 +385,11 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
         (long)(p.batch - 1) * p.c_bstride + p.N <= p.ldc && g.ns * T::STAGE >= BM * BN * 2 &&
         map_2d(&mc, p.c_bf16, (uint64_t)p.ldc, (uint64_t)p.M, (uint64_t)p.ldc, BM))
         g.tma_c = 1;
+    else if (p.c_part && p.N % 32 == 0 && (reinterpret_cast<uintptr_t>(p.c_part) & 15) == 0 &&
+             g.ns * T::STAGE >= BM * BN * 4 &&
+             map_3d_f32(&mc, p.c_part, (uint64_t)p.N, (uint64_t)p.M,
+                        (uint64_t)p.k_splits * p.batch))
+        g.tma_c = 2;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
