@@ -15,8 +15,11 @@
 //
 // Roles (192 threads): warp 0 issues TMA (one lane), warp 1 owns TMEM and issues the
 // MMAs (the whole warp waits, one elected lane issues through predicated instructions),
-// warps 2-5 read the accumulator out of TMEM and store it. Waits are bounded (one
-// second); a wait that gives up records MLA_ERR_TIMEOUT.
+// warps 2-5 read the accumulator out of TMEM and write it: into the stage ring, idle once
+// the products are done, as 128-byte-swizzled boxes that one thread stores with TMA (whole
+// lines instead of one row per thread), or directly where the output layout does not fit
+// one tensor map. Waits are bounded (one second); a wait that gives up records
+// MLA_ERR_TIMEOUT.
 // The stage ring holds min(6, k-blocks of a CTA) stages (4 at width 256) and shared
 // memory is sized to it, so products with little K per tile (the per-head absorptions)
 // run several CTAs per SM instead of one; products with many 256-wide tiles and short K
