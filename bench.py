@@ -17,8 +17,15 @@ output y copied back inside the timed region, on a copy stream with double buffe
 so that the transfers overlap the neighbouring steps' kernels, as a serving loop
 would; the cache and weights are device-resident state.
 
+The same line carries `configs`: decode attention alone, timed in the same process
+after the step, on the V3-shaped (16 x 4096), mixed-length (128 x U[1024, 8192]) and
+long-context (32 x 32768, 64 heads) workloads, each with its time, GB/s, TFLOP/s and
+fraction of the roofline.
+
 --impl reference times the fp64 CPU oracle (the only other implementation) on a
-bounded sample of the same workload on this machine's host cores.
+bounded sample of the same workload on this machine's host cores; its value and
+ms_per_step are the sample's own (an estimate for the whole batch is reported in a
+separate field).
 
 Multi-GPU: the decode step shards by sequence with no exchange, so N ranks run N
 independent replicas of the batch (weak scaling) and rank 0 reports the total.
@@ -155,6 +162,25 @@ def _max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def _line_config(d, args, world):
+    """The `config` object of both arms' lines (the same keys for the GPU and the reference)."""
+    return dict(d["_cfg"], parallelism=f"replicas{world}" if world > 1 else "single",
+                l2="inputs larger than L2 (1.21 GB cache + 374 MB weights); no flush",
+                num_splits=args.num_splits or "auto")
+
+
+def sample_bytes(d, n_seq: int, heads: int) -> int:
+    """Algorithmic bytes of the oracle's sample: the full step of n_seq sequences restricted
+    to `heads` heads (the weights of those heads once, the sequences' cached rows once, their
+    activations)."""
+    H, dm, ql = heads, d["d_model"], d["q_lora"]
+    L = d["seqlens_after"][:n_seq].astype(np.int64)
+    weights = 2 * (576 * dm + ql * dm + H * 128 * ql + H * 64 * ql + H * 128 * 512 * 2 +
+                   dm * H * 128)
+    act = n_seq * dm * 2 * 2 + n_seq * 576 * 2 + n_seq * H * (576 * 2 + 512 * 2 + 4)
+    return int(weights + int(L.sum()) * 576 * 2 + act)
+
+
 # --------------------------------------------------------------- CPU oracle leg
 
 def time_oracle(d, n_seq: int):
@@ -205,10 +231,13 @@ def time_oracle_heads(d, ws, seq: int = 0) -> float:
 
 
 def run_reference(args, d, costs, metric, unit):
-    """The fp64 oracle on the host cores. Each step is one sequence of the full step with a
-    head subset sized so that warm-up + all steps take about two minutes; its time is
-    scaled to the whole batch: 128 x (per-sequence part + 128 x per-head part), with the
-    two parts calibrated from a 1-head and an all-head run of one sequence."""
+    """The fp64 oracle on the host cores. Each step is a sample of the full step sized so
+    that warm-up + all steps take about two minutes: the whole step for the first n_seq
+    sequences (every head) when one sequence fits the per-step budget, else one sequence
+    restricted to a head subset. `value` and `ms_per_step` are the sample's own (its
+    algorithmic bytes over its measured time); the whole batch's time, scaled from
+    per-sequence and per-head parts calibrated on a 1-head and an all-head run of one
+    sequence, is reported separately as an estimate."""
     world, rank, _ = _dist_init()
     if rank != 0:
         return
@@ -220,25 +249,35 @@ def run_reference(args, d, costs, metric, unit):
     t_head = max((t_all - t_one) / (H - 1), 1e-9)
     t_seq = max(t_one - t_head, 0.0)
     budget = 120.0 / max(1, args.steps + args.warmup)
-    hs = H
-    while hs > 1 and t_seq + hs * t_head > budget:
-        hs //= 2
-    ws = _head_slice(d, hs)
+    if t_all <= budget:
+        n_seq, hs = max(1, min(B, int(budget / t_all))), H
+        run = lambda: time_oracle(d, n_seq)  # noqa: E731
+        what = f"the full step of {n_seq} of {B} sequences (every head)"
+    else:
+        n_seq, hs = 1, H
+        while hs > 1 and t_seq + hs * t_head > budget:
+            hs //= 2
+        ws = _head_slice(d, hs)
+        run = lambda: time_oracle_heads(d, ws)  # noqa: E731
+        what = (f"1 of {B} sequences x {hs} of {H} heads of the full step (its whole "
+                f"8192-token attention and the projections of those heads)")
     for _ in range(args.warmup):
-        time_oracle_heads(d, ws)
-    ts = [time_oracle_heads(d, ws) for _ in range(args.steps)]
+        run()
+    ts = [run() for _ in range(args.steps)]
     t_sample = statistics.median(ts)
-    # measured sample (1 sequence, hs heads) -> whole step
-    t_step = B * (t_sample + (H - hs) * t_head)
-    value = costs["bytes"] / t_step / 1e9
-    sample = (f"1 of {B} sequences x {hs} of {H} heads per step (full 8192-token attention, "
-              f"its projections); scaled to the batch with per-sequence {t_seq*1e3:.1f} ms and "
-              f"per-head {t_head*1e3:.2f} ms parts calibrated on the same host")
+    value = sample_bytes(d, n_seq, hs) / t_sample / 1e9
+    # estimate only: the whole step scaled from the calibrated per-sequence and per-head parts
+    t_step_est = B * (t_seq + H * t_head)
+    sample = f"each step: {what}, timed as run; value = its algorithmic bytes / its time"
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_sample * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": dict(d["_cfg"], impl="fp64 CPU oracle"),
+            "data": "synthetic", "config": _line_config(d, args, 1),
+            "implementation": "fp64 CPU oracle",
+            "full_step_estimate": {
+                "ms": t_step_est * 1e3, "value": costs["bytes"] / t_step_est / 1e9, "unit": unit,
+                "how": (f"{B} x (per-sequence {t_seq*1e3:.1f} ms + {H} x per-head "
+                        f"{t_head*1e3:.2f} ms), parts calibrated on the same host")},
             "cpu_baseline": {"value": value, "unit": unit, "cores": _host_cores(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
@@ -373,6 +412,11 @@ def run_gpu(args, d, costs, metric, unit):
     h2d = h_host.numel() * 2 + pos_host.numel() * 4 + L_host.numel() * 4
     d2h = y_host.numel() * 2
 
+    # ---- decode attention alone on the other attention workloads (same process)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = time_attention_configs(cache, dev, max(args.steps, 50), args.num_splits)
+
     if rank != 0:
         return
     peaks = _measured_peaks()
@@ -396,9 +440,7 @@ def run_gpu(args, d, costs, metric, unit):
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(d["_cfg"], parallelism=f"replicas{world}" if world > 1 else "single",
-                       l2="inputs larger than L2 (1.21 GB cache + 374 MB weights); no flush",
-                       num_splits=args.num_splits or "auto"),
+        "config": _line_config(d, args, world),
         "tflops": tflops,
         "tokens_per_s": B * world * args.steps / (t_ms * 1e-3),
         "roofline_frac_step": roof_s / (ms_step * 1e-3),
@@ -413,13 +455,16 @@ def run_gpu(args, d, costs, metric, unit):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if configs:
+        line["configs"] = configs
     if world == 1 and not args.no_cpu_baseline:
         t_s = time_oracle(d, args.cpu_sample)
-        t_step = t_s * B / args.cpu_sample
         line["cpu_baseline"] = {
-            "value": costs["bytes"] / t_step / 1e9, "unit": unit, "cores": _host_cores(),
-            "kind": "oracle",
-            "sample": f"{args.cpu_sample} of {B} sequences of the full step, scaled linearly"}
+            "value": sample_bytes(d, args.cpu_sample, H) / t_s / 1e9, "unit": unit,
+            "cores": _host_cores(), "kind": "oracle", "seconds": t_s,
+            "sample": (f"the full step of {args.cpu_sample} of {B} sequences (all heads, "
+                       f"all weights), timed as run; value = that sample's algorithmic "
+                       f"bytes / its time")}
     print(json.dumps(line), flush=True)
 
 
@@ -574,6 +619,88 @@ def run_gpu_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+ATTN_CONFIGS = ("v3", "mixed", "long")
+ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70}
+
+
+def time_attention_configs(pool, dev, launches: int, num_splits: int):
+    """mla_decode_attention alone on the v3-shaped, mixed-length and long-context workloads,
+    in this process after the step: their seqlens, block tables and queries follow the
+    seeded recipe of each workload; their cache rows are the step's resident pool (the same
+    N(0, 1) bf16 values; every block table indexes into it). Launches back to back on one
+    stream between CUDA events; a workload whose cache is under twice the L2 size reads a
+    different block range of the pool at each launch (its table shifted by a multiple of its
+    block count), so every launch starts from a cold L2."""
+    import torch
+    from mla_latent_kv_13_gb300 import mla, synth
+    peaks = _measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    nb_pool = pool.shape[0]
+    out_all = {}
+    for name in ATTN_CONFIGS:
+        w = synth.WORKLOADS[name]
+        L = synth.draw_seqlens(w, 0)
+        bt, nblk = synth.make_block_table(L, w.shuffled, 0)
+        if nblk > nb_pool:
+            continue
+        ql, qr = synth.make_attention_queries(w, seed=0)
+        B, H = w.batch, w.heads
+        max_len = int(L.max())
+
+        def dbf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(
+                torch.bfloat16)
+
+        q_lat, q_rope = dbf(ql), dbf(qr)
+        cache_bytes = int(L.sum()) * 576 * 2
+        rot = 1
+        if 2 * cache_bytes < (256 << 20):
+            rot = max(1, min(nb_pool // nblk, 16))
+        bts = []
+        for k in range(rot):
+            b2 = bt.copy()
+            b2[b2 >= 0] += k * nblk
+            bts.append(torch.from_numpy(b2).to(dev))
+        Ld = torch.from_numpy(L).to(dev)
+        ws = mla.alloc_workspace(mla.decode_workspace_size(B, H, max_len, num_splits))
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+
+        def attend(i):
+            mla.decode_attention(q_lat, q_rope, pool, bts[i % rot], Ld, max_len,
+                                 synth.SCALE_192, num_splits, out, lse, ws)
+
+        for i in range(3):
+            attend(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(launches):
+            attend(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if mla.check_device_status(ws) != 0:
+            raise RuntimeError(f"device error in the {name} attention timing")
+        ms = e0.elapsed_time(e1) / launches
+        byts = synth.algorithmic_attention_bytes(L, H)
+        flops = synth.attention_flops(L, H)
+        roof_s = max(byts / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+        out_all[name] = {
+            "batch": B, "heads": H,
+            "seqlens": w.seqlens[0] if w.seqlens else f"U{list(w.seqlen_range)} seed 0",
+            "tokens": int(L.sum()), "ms": ms, "GB/s": byts / (ms * 1e-3) / 1e9,
+            "TFLOP/s": flops / (ms * 1e-3) / 1e12, "frac": roof_s / (ms * 1e-3),
+            "bound": "hbm" if byts / (peaks["hbm_gbs"] * 1e9) >=
+            flops / (peaks["bf16_tflops"] * 1e12) else "tensor",
+            "gate": ATTN_GATE[name], "launches": launches,
+            "plan": {"splits": mla.decode_plan(B, H, max_len, num_splits)[0]},
+            "l2": (f"{rot} disjoint block ranges rotated" if rot > 1
+                   else "cache larger than L2"),
+            "algorithmic_bytes": byts}
+        del ws, out, lse, bts, q_lat, q_rope
+    return out_all
+
+
 def step_launches(step) -> int:
     """Kernels one DecodeStep launches: append 2, absorb_q 6, decode 1-3 (the library's
     own plan: + merge, + schedule), out 3."""
@@ -610,6 +737,8 @@ def main():
                          "attention alone on that attention workload")
     ap.add_argument("--cpu-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload attention timings in the step line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

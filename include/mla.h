@@ -111,7 +111,9 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  * seqlens[b] = 0 gives out = 0 and lse = -inf.
  *
  * q_lat [B][H][512] bf16, q_rope [B][H][64] bf16 (already rotated),
- * seqlens [B] int32 (0 <= seqlens[b] <= 64 * max_blocks; checked on the device),
+ * seqlens [B] int32 with 0 <= seqlens[b] <= max_seqlen (checked on the device: a length
+ * outside that range is recorded as MLA_ERR_OUT_OF_RANGE and clamped into it, by every
+ * work distribution alike),
  * out [B][H][512] bf16, lse [B][H] fp32.
  * scale must be finite and > 0 (1/sqrt(d_nope + d_rope) for DeepSeek-shaped heads).
  * H must be 16, 32, 64 or 128; 1 <= B <= 4096. num_splits: the number of equal token
@@ -139,7 +141,8 @@ mla_status_t mla_decode_plan(int B, int H, int max_seqlen, int num_splits, int *
 /*
  * The balanced schedule for these sequence lengths, computed on the host with the
  * arithmetic the device uses (no counterpart on the pages; no device memory is touched).
- * seqlens [B] host int32, clamped to [0, 64 * max_blocks] as on the device; clusters =
+ * seqlens [B] host int32, clamped to [0, 64 * max_blocks] (the device clamps to
+ * [0, max_seqlen] of its call, which is at most that, and records an error); clusters =
  * the number of work units (the device's resident count in mla_decode_attention; any
  * value >= 1 here). A sequence with v > 0 token blocks weighs v plus a fixed start-up
  * cost; work unit c takes the weight range [c*W/P, (c+1)*W/P) of the total W
@@ -233,24 +236,32 @@ mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int 
 /*
  * mla_decode_attention without a workspace: the same computation and outputs, for
  * callers that cannot obtain device memory for scratch -- code running while a
- * stream is captured into a CUDA graph, plugins whose host framework owns all device
- * allocations, serving loops that must not call cudaMalloc/cudaFree on their hot
- * path. (The pages describe no such entry point; it is a property of this library.)
+ * stream is captured into a CUDA graph (an allocation there is illegal or ends the
+ * capture), plugins whose host framework owns every device allocation and hands out
+ * only tensor pointers, serving loops that must not call cudaMalloc/cudaFree on their
+ * hot path because those calls can synchronise the device. (The pages describe no such
+ * entry point; it is a property of this library.)
  *
- * The split-KV scratch (partial outputs, their log-sum-exps, the error word) lives in
- * one array of MLA_NOALLOC_SCRATCH_BYTES that is part of the library image: every GPU
- * that loads the library holds it until the process exits. Requests whose scratch
- * (the figure mla_decode_workspace_size reports for the same B, H, max_seqlen and
- * num_splits) exceeds that size are rejected with MLA_ERR_WORKSPACE before anything
- * is launched; num_splits = 1 needs no partials and always fits.
+ * The split-KV scratch (partial outputs, their log-sum-exps, the schedule's offsets and
+ * the error word) lives in one array of MLA_NOALLOC_SCRATCH_BYTES (40 MiB) that is part
+ * of the library image: every GPU that loads the library holds it until the process
+ * exits. A request fits when the figure mla_decode_workspace_size reports for the same
+ * B, H, max_seqlen and num_splits is at most that size. With num_splits = 0 every plan
+ * of up to 128 query rows fits on a GPU with at most 76 resident work units (a GB300):
+ * the largest is the balanced schedule's 152 partial rows of 128 heads, 38.1 MiB (for
+ * instance B = 128 sequences of 8192 tokens). num_splits = 1 needs no partials and always
+ * fits; explicit splits fit while B * num_splits * H * 2 KiB stays below the limit.
+ * Larger requests, and every invalid argument, are rejected on the host before anything
+ * is queued (MLA_ERR_WORKSPACE, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED).
  * The first call on a device looks up the array's device address (no allocation) and
  * should happen before any stream capture. All calls share the array and it keeps the
- * last call's contents, so calls that overlap on the GPU (other streams, other host
- * threads) race and must be serialised by the caller. Device-detected range errors
- * skip the offending tokens as in mla_decode_attention but are not reported (there is
- * no workspace to read them from). Allocates nothing.
+ * last call's contents (each call clears the error word it needs), so calls that overlap
+ * on the GPU (other streams, other host threads) race and must be serialised by the
+ * caller. Device-detected range errors skip the offending tokens as in
+ * mla_decode_attention but are not reported (there is no workspace to read them from).
+ * Allocates nothing.
  */
-#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define MLA_NOALLOC_SCRATCH_BYTES (40u << 20)
 mla_status_t mla_decode_attention_noalloc(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                                           const mla_bf16_t *kv_cache, int num_blocks,
                                           const int32_t *block_table, int max_blocks,

@@ -259,25 +259,44 @@ mla_status_t mla_decode_schedule(const int32_t *seqlens, int B, int max_blocks, 
 
 }  // extern "C"
 
-namespace {
-// Decode over H = s_q x hq query rows per sequence (query token t, head h at row t*hq + h);
-// token t sees the rows j < seqlens[b] - (s_q - 1 - t). Plain decode: s_q = 1, hq = H.
-mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
-                        const mla_bf16_t *kv_cache, int num_blocks, const int32_t *block_table,
-                        int max_blocks, const int32_t *seqlens, int B, int s_q, int hq,
-                        int max_seqlen, float scale, int num_splits, void *workspace,
-                        size_t ws_bytes, mla_bf16_t *out, float *lse, mla_stream_t stream) {
-    const int H = s_q * hq;
-    if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !workspace || !out || !lse)
+namespace mla {
+// Host-side checks of a decode call's arguments (every one except the workspace), shared
+// by every decode entry point so that a rejected call touches nothing on the device.
+mla_status_t decode_validate(const void *q_lat, const void *q_rope, const void *kv_cache,
+                             int num_blocks, const int32_t *block_table, int max_blocks,
+                             const int32_t *seqlens, int B, int s_q, int hq, int max_seqlen,
+                             float scale, int num_splits, const void *out, const float *lse) {
+    if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !out || !lse)
         return MLA_ERR_INVALID_ARG;
     if (B < 1 || B > 4096 || num_blocks < 1 || max_blocks < 1 || max_seqlen < 0 ||
         max_seqlen > max_blocks * BLOCK || num_splits < 0 || num_splits > 256 ||
         !(scale > 0.f) || !isfinite(scale) || s_q < 1)
         return MLA_ERR_INVALID_ARG;
-    if (!heads_ok(hq) || H > 128) return MLA_ERR_UNSUPPORTED;
+    if (!heads_ok(hq) || s_q * hq > 128) return MLA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||
-        !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+        !aligned(out, 16) || !aligned(lse, 4))
         return MLA_ERR_INVALID_ARG;
+    return MLA_OK;
+}
+}  // namespace mla
+
+namespace {
+// Decode over H = s_q x hq query rows per sequence (query token t, head h at row t*hq + h);
+// token t sees the rows j < seqlens[b] - (s_q - 1 - t). Plain decode: s_q = 1, hq = H.
+// The output goes to `out` as bf16, or, when out_f32 is given, to out_f32 as fp32.
+mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                        const mla_bf16_t *kv_cache, int num_blocks, const int32_t *block_table,
+                        int max_blocks, const int32_t *seqlens, int B, int s_q, int hq,
+                        int max_seqlen, float scale, int num_splits, void *workspace,
+                        size_t ws_bytes, mla_bf16_t *out, float *out_f32, float *lse,
+                        mla_stream_t stream) {
+    const int H = s_q * hq;
+    const void *out_any = out_f32 ? static_cast<const void *>(out_f32) : out;
+    const mla_status_t v = decode_validate(q_lat, q_rope, kv_cache, num_blocks, block_table,
+                                           max_blocks, seqlens, B, s_q, hq, max_seqlen, scale,
+                                           num_splits, out_any, lse);
+    if (v != MLA_OK) return v;
+    if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
     const int splits = plan_decode_splits(B, H, max_seqlen, num_splits);
     const DecodeLayout lay = decode_layout(B, H, max_seqlen, splits);
     if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE;
@@ -288,9 +307,10 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     p.q_lat = q_lat; p.q_rope = q_rope; p.cache = kv_cache;
     p.block_table = block_table; p.seqlens = seqlens;
     p.num_blocks = num_blocks; p.max_blocks = max_blocks; p.B = B; p.H = H;
+    p.max_seqlen = max_seqlen;
     p.s_q = s_q; p.hq = hq;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.out = out; p.lse = lse;
+    p.out = out; p.out_f32 = out_f32; p.lse = lse;
     p.err = err_word(workspace);
     cudaStream_t st = S(stream);
     if (splits >= 1) {
@@ -302,7 +322,9 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
         }
         cudaError_t e = launch_decode_tc(p, B * splits, st);
         if (e != cudaSuccess) return MLA_ERR_CUDA;
-        if (splits > 1) e = launch_combine(p.o_part, p.lse_part, B, splits, H, out, lse, st);
+        if (splits > 1)
+            e = launch_combine(p.o_part, p.lse_part, B, splits, H, (long)splits * H * D_C,
+                               (long)H * D_C, (long)splits * H, H, out, out_f32, lse, st);
         return cuda_status(e);
     }
     // balanced schedule: tile offsets on the device, P persistent clusters, merge of cut sequences
@@ -319,12 +341,12 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     p.nparts = nparts;
     p.o_part = reinterpret_cast<float *>(w + lay.o_part);
     p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
-    if (launch_decode_schedule(seqlens, B, max_blocks, P, tile_start, wpos, part_begin, nparts,
+    if (launch_decode_schedule(seqlens, B, max_seqlen, P, tile_start, wpos, part_begin, nparts,
                                p.err, st) != cudaSuccess)
         return MLA_ERR_CUDA;
     if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_status(launch_combine_sched(p.o_part, p.lse_part, tile_start, part_begin, nparts,
-                                            B, H, out, lse, st));
+                                            B, H, out, out_f32, lse, st));
 }
 
 }  // namespace
@@ -339,7 +361,21 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
                                   size_t ws_bytes, mla_bf16_t *out, float *lse,
                                   mla_stream_t stream) {
     return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
-                      1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
+                      1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
+                      stream);
+}
+
+mla_status_t mla_decode_attention_partial(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                          const mla_bf16_t *kv_cache, int num_blocks,
+                                          const int32_t *block_table, int max_blocks,
+                                          const int32_t *seqlens, int B, int H, int max_seqlen,
+                                          float scale, int num_splits, void *workspace,
+                                          size_t ws_bytes, float *o_part, float *lse_part,
+                                          mla_stream_t stream) {
+    if (!o_part) return MLA_ERR_INVALID_ARG;
+    return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
+                      1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, nullptr, o_part,
+                      lse_part, stream);
 }
 
 mla_status_t mla_decode_mq_workspace_size(int B, int s_q, int H, int max_seqlen, int num_splits,
@@ -362,7 +398,8 @@ mla_status_t mla_decode_attention_mq(const mla_bf16_t *q_lat, const mla_bf16_t *
                                      size_t ws_bytes, mla_bf16_t *out, float *lse,
                                      mla_stream_t stream) {
     return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
-                      s_q, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, lse, stream);
+                      s_q, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
+                      stream);
 }
 
 // ------------------------------------------------------------- prefill
@@ -449,7 +486,20 @@ mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int 
     if (!o_part || !lse_part || !out || !lse || B < 1 || S_ < 1 || H < 1 || H > 65535)
         return MLA_ERR_INVALID_ARG;
     if (!aligned(o_part, 16) || !aligned(out, 8) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
-    return cuda_status(launch_combine(o_part, lse_part, B, S_, H, out, lse, S(stream)));
+    return cuda_status(launch_combine(o_part, lse_part, B, S_, H, (long)S_ * H * D_C,
+                                      (long)H * D_C, (long)S_ * H, H, out, nullptr, lse,
+                                      S(stream)));
+}
+
+mla_status_t mla_decode_combine_ranks(const float *o_parts, const float *lse_parts, int G, int B,
+                                      int H, mla_bf16_t *out, float *lse, mla_stream_t stream) {
+    if (!o_parts || !lse_parts || !out || !lse || G < 1 || G > 4096 || B < 1 || B > 4096 ||
+        H < 1 || H > 65535)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(o_parts, 16) || !aligned(out, 8) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(o_parts, lse_parts, B, G, H, (long)H * D_C,
+                                      (long)B * H * D_C, H, (long)B * H, out, nullptr, lse,
+                                      S(stream)));
 }
 
 // ------------------------------------------------------------ absorb_q

@@ -54,12 +54,16 @@ extern "C" mla_status_t mla_decode_attention_noalloc(
     int num_blocks, const int32_t *block_table, int max_blocks, const int32_t *seqlens, int B,
     int H, int max_seqlen, float scale, int num_splits, mla_bf16_t *out, float *lse,
     mla_stream_t stream) {
-    // Same validation as mla_decode_attention, then the scratch-size limit.
-    if (!q_lat || !q_rope || !kv_cache || !block_table || !seqlens || !out || !lse)
-        return MLA_ERR_INVALID_ARG;
-    size_t need = 0;
-    mla_status_t st = mla_decode_workspace_size(B, H, max_seqlen, num_splits, &need);
+    // The same argument checks as mla_decode_attention, then the scratch-size limit: a
+    // rejected call returns before anything is queued on the device (the shared array's
+    // header may belong to a call still running on another stream).
+    mla_status_t st = mla::decode_validate(q_lat, q_rope, kv_cache, num_blocks, block_table,
+                                           max_blocks, seqlens, B, 1, H, max_seqlen, scale,
+                                           num_splits, out, lse);
     if (st != MLA_OK) return st;
+    size_t need = 0;
+    if ((st = mla_decode_workspace_size(B, H, max_seqlen, num_splits, &need)) != MLA_OK)
+        return st;
     if (need > kScratchBytes) return MLA_ERR_WORKSPACE;
     void *scratch = nullptr;
     if ((st = scratch_on_current_device(&scratch)) != MLA_OK) return st;

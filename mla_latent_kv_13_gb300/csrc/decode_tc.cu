@@ -75,7 +75,12 @@ constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
 constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
 constexpr int NBAR = 40;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-constexpr int SMEM_USED = MISC_OFF + 64;
+// MISC: TMEM address, abort flags, and the counts of remote operations exchanged when a
+// pair stops early (byte offsets below)
+constexpr int MISC_BYTES = 128;
+constexpr int M_TMEM = 0, M_ABORT = 4, M_PEER_ABORT = 8, M_PEER_PV = 12, M_PEER_SENT = 16,
+              M_SENT = 32, M_RECV = 48, M_PV = 64;
+constexpr int SMEM_USED = MISC_OFF + MISC_BYTES;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 constexpr int NTHREADS = 224;                 // 7 warps
@@ -168,8 +173,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t qs_full = q_ready + 152;  // the next segment's Q rows staged
     // the peer's P half of the rows of warp quadrant q has landed in buffer x
     auto recv_full = [&](int q, int x) { return q_ready + 80 + 8u * (2 * q + x); };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF + M_TMEM);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + M_ABORT);
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + MISC_OFF);
+    const uint32_t misc_peer = mapa(sb + MISC_OFF, peer);  // the peer's MISC area
 
     auto init_barriers = [&]() {
         for (int s = 0; s < NKV; ++s) {
@@ -257,15 +264,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         part = sg.part;
     }
     int L = p.seqlens[b];
-    if (L < 0 || L > p.max_blocks * TOK) {
-        if (!sched && tid == 0 && rank == 0 && t_begin == 0)
-            flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
-        L = L < 0 ? 0 : p.max_blocks * TOK;
+    // a length outside [0, max_seqlen] is an error, recorded once per sequence (by the
+    // work item holding its first tile) and clamped exactly as the schedule clamps it, so
+    // both work distributions give the same result
+    if (L < 0 || L > p.max_seqlen) {
+        if (tid == 0 && rank == 0 && t_begin == 0) flag_error(p.err, MLA_ERR_OUT_OF_RANGE, b);
+        L = L < 0 ? 0 : p.max_seqlen;
     }
     const int ntiles = (L + TOK - 1) / TOK;
     t_end = min(ntiles, t_end);
     const int n = max(0, t_end - t_begin);
     const int32_t *btab = p.block_table + (size_t)b * p.max_blocks;
+    // remote operations of this segment, counted for an early stop of the pair:
+    // P halves sent to the peer (st.async; the receive barrier of each is armed right
+    // after), peer halves received, P.V commits multicast to the peer's rfree barriers
+    int n_sent = 0, n_recv = 0, n_pv = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -299,6 +312,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 }
             };
             const int next_at = sched ? max(0, n - (NKV + PF_DIST + 4)) : -1;
+            // L2 priorities: the own tokens' chunks in the peer's output columns are read
+            // again by the peer (its V ring) and keep the normal priority; every other
+            // chunk is read once and is marked to leave L2 first, so that the chunks still
+            // awaiting their second read are not the ones evicted
+            const uint64_t pol_once = l2_policy_evict_first();
+            const uint64_t pol_twice = l2_policy_evict_normal();
             int issued_kv = 0, issued_k = 0;
             for (int i = 0; i < n; ++i) {
                 const int skv = i % NKV, sk = i % NK;
@@ -312,7 +331,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t dst = sb + KV_OFF + skv * KV_SLOT;
                     mbar_arrive_expect_tx(kv_full(skv), KV_SLOT);
                     for (int k = 0; k < 4; ++k)
-                        tma_load_2d(dst + k * CH, &map_kv, kv_full(skv), 64 * (4 * rank + k), y_own);
+                        tma_load_2d_hint(dst + k * CH, &map_kv, kv_full(skv), 64 * (4 * rank + k),
+                                         y_own, pol_once);
                 } else {
                     mbar_arrive(kv_full(skv));  // no data: the consumers mask the tile
                 }
@@ -323,8 +343,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t dst = sb + K_OFF + sk * K_SLOT;
                     mbar_arrive_expect_tx(k_full(sk), K_SLOT);
                     for (int k = 0; k < 4; ++k)
-                        tma_load_2d(dst + k * CH, &map_kv, k_full(sk), 64 * (4 * peer + k), y_own);
-                    tma_load_2d(dst + 4 * CH, &map_kv, k_full(sk), D_C, y_own);
+                        tma_load_2d_hint(dst + k * CH, &map_kv, k_full(sk), 64 * (4 * peer + k),
+                                         y_own, pol_twice);
+                    tma_load_2d_hint(dst + 4 * CH, &map_kv, k_full(sk), D_C, y_own, pol_once);
                 } else {
                     mbar_arrive(k_full(sk));
                 }
@@ -352,6 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             auto wait_all = [&](uint32_t bar_, uint32_t par) {
                 return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
             };
+            const uint64_t pol_once = l2_policy_evict_first();  // the second and last read
             auto load_v = [&](int j) {
                 const int sv = j % NV;
                 const int blk = btab[t_begin + j];
@@ -359,8 +381,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const uint32_t dst = sb + V_OFF + sv * V_SLOT;
                     mbar_arrive_expect_tx(v_full(sv), V_SLOT);
                     for (int k = 0; k < 4; ++k)
-                        tma_load_2d(dst + k * CH, &map_kv, v_full(sv), 64 * (4 * rank + k),
-                                    blk * TOK + HALF * peer);
+                        tma_load_2d_hint(dst + k * CH, &map_kv, v_full(sv), 64 * (4 * rank + k),
+                                         blk * TOK + HALF * peer, pol_once);
                 } else {
                     mbar_arrive(v_full(sv));  // no data: the softmax zeroes the slot
                 }
@@ -403,6 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 if (!(ok = wait_all(v_full(i % NV), (i / NV) & 1))) break;
                 tc_fence_after();
                 issue_pv(i);
+                ++n_pv;
                 __syncwarp();
             }
             // every MMA this warp issued has finished, every copy it started has landed
@@ -634,8 +657,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                 __float_as_uint(e_own), rb);
                 }
                 if (lane == 0) mbar_arrive_expect_tx(recv_full(wq, x), XBYTES);
+                ++n_sent;
                 // ---- the peer's half of tile i
                 if (!(ok = wait_wc(recv_full(wq, x), (i >> 1) & 1))) break;
+                ++n_recv;
                 const float2 pm = ld_shared_v2f(recv + x * PBUF + mrow);
                 m_peer = pm.x;
                 e_peer = pm.y;
@@ -716,6 +741,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int nb = sched && ok && n > 0 ? sched_peek(p.tile_start, p.wpos, p.B, r1, seg_b)
                                             : -1;
         const int col0 = 256 * rank;
+        // fp32 rows: a part of a cut sequence, or the whole output when the caller asked
+        // for fp32 (partial attention over one rank's token range)
+        const bool out32 = !direct || p.out_f32 != nullptr;
+        float *const orow32 =
+            !out32 ? nullptr
+                   : (direct ? p.out_f32 + ((size_t)b * H + row) * D_C
+                             : p.o_part + ((size_t)part * H + row) * D_C) + col0;
         if (n > 0 && ok && wait_w(pv_done((n - 1) & 1), ((n - 1) >> 1) & 1)) {
             tc_fence_after();
             // Every product of this segment is done, so the rings are idle: the next
@@ -739,7 +771,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tl + TM_O + 32 * c, r);
                 tmem_ld_wait();
                 if (row < H) {
-                    if (direct) {
+                    if (!out32) {
                         uint4 *dst = reinterpret_cast<uint4 *>(
                             p.out + ((size_t)b * H + row) * D_C + col0 + 32 * c);
 #pragma unroll
@@ -754,8 +786,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                 pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv,
                                             __uint_as_float(r[8 * k + 7]) * inv));
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            p.o_part + ((size_t)part * H + row) * D_C + col0 + 32 * c);
+                        float4 *dst = reinterpret_cast<float4 *>(orow32 + 32 * c);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv,
@@ -800,12 +831,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
         } else if (row < H) {
             // empty range (or aborted): zero output, lse = -inf
-            if (direct) {
+            if (!out32) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)b * H + row) * D_C + col0);
                 for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
             } else {
-                float4 *dst = reinterpret_cast<float4 *>(
-                    p.o_part + ((size_t)part * H + row) * D_C + col0);
+                float4 *dst = reinterpret_cast<float4 *>(orow32);
                 for (int k = 0; k < 64; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             l = 0.f;
@@ -823,16 +853,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     // our own copies have read their rows, the peer's signals that its P.V has read our
     // halves have all arrived, every role is idle; then barriers restart
     if (warp >= 2 && lane == 0) bulk_wait_read_all();
-    if (tid == 64 && n > 0) {
+    if (tid == 64 && n > 0 && !*abort_flag) {
         for (int x = 0; x < 2; ++x) {
             const int cnt = (n + 1 - x) / 2;  // tiles of parity x
             if (cnt > 0) drain_wait(rfree(x), (cnt - 1) & 1);
         }
     }
+    if (warp >= 2 && warp < 6 && lane == 0) {
+        misc[(M_SENT >> 2) + (warp - 2)] = n_sent;  // = receive barriers armed
+        misc[(M_RECV >> 2) + (warp - 2)] = n_recv;
+    }
+    if (warp == 6 && lane == 0) misc[M_PV >> 2] = n_pv;
+    if (tid == 0) st_cluster_u32(misc_peer + M_PEER_ABORT, *abort_flag ? 1u : 0u);
     tc_fence_before();
     __syncthreads();
     cluster_sync();
-    if (!sched || *abort_flag) break;
+    // Both CTAs now see both abort flags and take the same branch.
+    if (*abort_flag || misc[M_PEER_ABORT >> 2]) {
+        // The pair stops early. Before either CTA may exit, every remote operation the
+        // peer issued into this CTA must have landed: its P halves (st.async, completing
+        // on recv_full) and its P.V commits (multicast arrivals on rfree). Each CTA tells
+        // the peer how many of each it issued, then waits (bounded) for the peer's.
+        // Neither CTA issues anything remote after the barrier above, and the peer can
+        // be at most two P halves ahead of what this CTA received (it sends tile t + 2
+        // only after this CTA's P.V of tile t released its buffer), so each barrier has
+        // at most one phase outstanding and the parity waits below are unambiguous.
+        if (tid == 0) {
+            st_cluster_u32(misc_peer + M_PEER_PV, static_cast<uint32_t>(misc[M_PV >> 2]));
+            for (int q = 0; q < 4; ++q)
+                st_cluster_u32(misc_peer + M_PEER_SENT + 4 * q,
+                               static_cast<uint32_t>(misc[(M_SENT >> 2) + q]));
+        }
+        __syncthreads();
+        cluster_sync();
+        if (warp >= 2 && warp < 6 && lane == 0) {
+            const int q = warp - 2;
+            const int sent = misc[(M_PEER_SENT >> 2) + q], armed = misc[(M_SENT >> 2) + q];
+            for (int t = misc[(M_RECV >> 2) + q]; t < sent; ++t) {
+                if (t >= armed) mbar_arrive_expect_tx(recv_full(q, t & 1), XBYTES);
+                drain_wait(recv_full(q, t & 1), (t >> 1) & 1);
+            }
+        }
+        if (tid == 64) {
+            const int pv = misc[M_PEER_PV >> 2];
+            for (int x = 0; x < 2; ++x) {
+                const int cnt = (pv + 1 - x) / 2;  // the peer's P.V commits of parity x
+                if (cnt > 0) drain_wait(rfree(x), (cnt - 1) & 1);
+            }
+        }
+        if (tid == 0) *abort_flag = 1;
+        break;  // the final cluster barrier follows
+    }
+    if (!sched) break;
     if (tid == 0) init_barriers();
     __syncthreads();
     cluster_sync();

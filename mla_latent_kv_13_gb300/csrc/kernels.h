@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mla.h"
+
 namespace mla {
 
 struct GemmParams {
@@ -42,10 +44,12 @@ struct DecodeParams {
     const int32_t *block_table;
     const int32_t *seqlens;
     int num_blocks, max_blocks, B, H;  // H = query rows per sequence (s_q x hq)
+    int max_seqlen;            // caller's bound on seqlens (<= 64 * max_blocks)
     int s_q, hq;  // query tokens per sequence (draft tokens, causal among them), heads each
     int num_splits, tiles_per_split;
     float scale_log2;          // scale * log2(e)
     uint16_t *out;             // [B][H][512]  (written when num_splits == 1)
+    float *out_f32;            // if non-null: the output as fp32 [B][H][512] instead of out
     float *lse;                // [B][H]       (written when num_splits == 1)
     float *o_part;             // [B][S][H][512] (num_splits > 1); [2P][H][512] if scheduled
     float *lse_part;           // [B][S][H]      (num_splits > 1); [2P][H]      if scheduled
@@ -127,21 +131,33 @@ __host__ __device__ inline int sched_peek(const int32_t *tile_start, const int32
     return b < B && wpos[b] < r1 ? b : -1;
 }
 
-cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
+// seqlens outside [0, max_len] are recorded as MLA_ERR_OUT_OF_RANGE and clamped to it
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P,
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
                                    int32_t *nparts, uint32_t *err, cudaStream_t stream);
+// out_f32 (if non-null) receives the merged rows as fp32 instead of bf16 out
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
                                  const int32_t *tile_start, const int32_t *part_begin,
-                                 const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
-                                 cudaStream_t stream);
+                                 const int32_t *nparts, int B, int H, uint16_t *out,
+                                 float *out_f32, float *lse, cudaStream_t stream);
 
 // grid = `clusters` two-CTA clusters (one per work item, or P with the schedule)
 cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream);
 int decode_tc_cluster_slots();
+// Merge S parts per (b, h) row: part s of row (b, h) at o_part + b*o_bstride + s*o_pstride
+// + h*512 (lse_part likewise with l_bstride, l_pstride, + h); out / out_f32 as above.
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
-                           uint16_t *out, float *lse, cudaStream_t stream);
+                           long o_bstride, long o_pstride, long l_bstride, long l_pstride,
+                           uint16_t *out, float *out_f32, float *lse, cudaStream_t stream);
 
 int device_sm_count();
+
+// Host-side argument checks of a decode call (all but the workspace): MLA_OK or the
+// status the entry point returns. Launches nothing.
+mla_status_t decode_validate(const void *q_lat, const void *q_rope, const void *kv_cache,
+                             int num_blocks, const int32_t *block_table, int max_blocks,
+                             const int32_t *seqlens, int B, int s_q, int hq, int max_seqlen,
+                             float scale, int num_splits, const void *out, const float *lse);
 
 // Chunked prefill: gather one sequence's first T cache rows contiguous (c_kv, k_rope), then
 // causal attention of the C chunk queries in the expanded form.

@@ -15,7 +15,7 @@ namespace {
 // accumulated in order. A part with lse = -inf (an empty range) contributes nothing.
 __device__ __forceinline__ void merge_row_warp(const float *o0, size_t ostride, const float *l0,
                                                size_t lstride, int np, uint16_t *orow,
-                                               float *lse_out, int lane) {
+                                               float *orow32, float *lse_out, int lane) {
     constexpr unsigned FULL = 0xffffffffu;
     float m = -INFINITY;
     for (int s = lane; s < np; s += 32) m = fmaxf(m, l0[s * lstride]);
@@ -53,28 +53,39 @@ __device__ __forceinline__ void merge_row_warp(const float *o0, size_t ostride, 
             }
         }
     }
+    if (orow32) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<uint2 *>(orow + lane * 4 + 128 * k) =
-            make_uint2(pack_bf16x2(acc[4 * k], acc[4 * k + 1]),
-                       pack_bf16x2(acc[4 * k + 2], acc[4 * k + 3]));
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4 *>(orow32 + lane * 4 + 128 * k) =
+                make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint2 *>(orow + lane * 4 + 128 * k) =
+                make_uint2(pack_bf16x2(acc[4 * k], acc[4 * k + 1]),
+                           pack_bf16x2(acc[4 * k + 2], acc[4 * k + 3]));
+    }
     if (lane == 0) *lse_out = tot;
 }
 
 constexpr int MERGE_ROWS = 8;  // head rows (one warp each) per CTA of the merge kernels
 
-// Fixed split: rows (b, h) of S token ranges each. Grid (ceil(H / 8), B), 256 threads.
-__global__ void __launch_bounds__(32 * MERGE_ROWS) combine_kernel(const float *o_part,
-                                                                 const float *lse_part, int S,
-                                                                 int H, uint16_t *out,
-                                                                 float *lse) {
+// Rows (b, h) of S parts each (token ranges of one sequence, or one range per rank), part s
+// of row (b, h) at o_part + b * o_bstride + s * o_pstride + h * 512 (lse likewise).
+// Grid (ceil(H / 8), B), 256 threads.
+__global__ void __launch_bounds__(32 * MERGE_ROWS)
+    combine_kernel(const float *o_part, const float *lse_part, int S, int H, long o_bstride,
+                   long o_pstride, long l_bstride, long l_pstride, uint16_t *out,
+                   float *out_f32, float *lse) {
     grid_launch_dependents();
     grid_dependency_wait();
     const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), b = blockIdx.y;
     if (h >= H) return;
-    merge_row_warp(o_part + ((size_t)b * S * H + h) * D_C, (size_t)H * D_C,
-                   lse_part + (size_t)b * S * H + h, H, S, out + ((size_t)b * H + h) * D_C,
-                   lse + (size_t)b * H + h, threadIdx.x & 31);
+    const size_t row = (size_t)b * H + h;
+    merge_row_warp(o_part + b * o_bstride + (size_t)h * D_C, o_pstride,
+                   lse_part + b * l_bstride + h, l_pstride, S,
+                   out_f32 ? nullptr : out + row * D_C, out_f32 ? out_f32 + row * D_C : nullptr,
+                   lse + row, threadIdx.x & 31);
 }
 
 // Sum k-split partials [S][batch][M][N] into bf16 C (batch stride c_bstride, row ldc).
@@ -146,7 +157,7 @@ __device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_to
 // positions (SEG_COST + tiles per sequence with tiles) -> wpos; parts of the sequences that
 // the equal split of the total weight cuts between clusters.
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seqlens, int B,
-                                                               int max_blocks, int P,
+                                                               int max_len, int P,
                                                                int32_t *tile_start,
                                                                int32_t *wpos,
                                                                int32_t *part_begin,
@@ -156,9 +167,9 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
     grid_dependency_wait();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seqlens[b];
-        if (L < 0 || L > max_blocks * BLOCK) {
+        if (L < 0 || L > max_len) {  // the attention kernel clamps the same way
             flag_error(err, MLA_ERR_OUT_OF_RANGE, b);
-            L = L < 0 ? 0 : max_blocks * BLOCK;
+            L = L < 0 ? 0 : max_len;
         }
         v[b] = (L + BLOCK - 1) / BLOCK;
     }
@@ -198,7 +209,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
 // written here; the decode kernel wrote the others. Grid (ceil(H / 8), B), 256 threads.
 __global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
     const float *o_part, const float *lse_part, const int32_t *tile_start,
-    const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *lse) {
+    const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *out_f32,
+    float *lse) {
     grid_launch_dependents();
     grid_dependency_wait();
     const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), b = blockIdx.y;
@@ -207,34 +219,37 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
     const bool empty = tile_start[b + 1] == tile_start[b];
     if (np == 0 && !empty) return;
     const int p0 = np > 0 ? part_begin[b] : 0;
+    const size_t row = (size_t)b * H + h;
     merge_row_warp(o_part + ((size_t)p0 * H + h) * D_C, (size_t)H * D_C,
-                   lse_part + (size_t)p0 * H + h, H, np, out + ((size_t)b * H + h) * D_C,
-                   lse + (size_t)b * H + h, threadIdx.x & 31);
+                   lse_part + (size_t)p0 * H + h, H, np,
+                   out_f32 ? nullptr : out + row * D_C, out_f32 ? out_f32 + row * D_C : nullptr,
+                   lse + row, threadIdx.x & 31);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_blocks, int P,
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P,
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
                                    int32_t *nparts, uint32_t *err, cudaStream_t stream) {
     return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
-                      max_blocks, P, tile_start, wpos, part_begin, nparts, err);
+                      max_len, P, tile_start, wpos, part_begin, nparts, err);
 }
 
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
                                  const int32_t *tile_start, const int32_t *part_begin,
-                                 const int32_t *nparts, int B, int H, uint16_t *out, float *lse,
-                                 cudaStream_t stream) {
+                                 const int32_t *nparts, int B, int H, uint16_t *out,
+                                 float *out_f32, float *lse, cudaStream_t stream) {
     dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, B);
     return launch_pdl(combine_sched_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part,
-                      lse_part, tile_start, part_begin, nparts, H, out, lse);
+                      lse_part, tile_start, part_begin, nparts, H, out, out_f32, lse);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,
-                           uint16_t *out, float *lse, cudaStream_t stream) {
+                           long o_bstride, long o_pstride, long l_bstride, long l_pstride,
+                           uint16_t *out, float *out_f32, float *lse, cudaStream_t stream) {
     dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, B);
     return launch_pdl(combine_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part, lse_part, S,
-                      H, out, lse);
+                      H, o_bstride, o_pstride, l_bstride, l_pstride, out, out_f32, lse);
 }
 
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,

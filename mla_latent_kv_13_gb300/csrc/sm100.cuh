@@ -169,6 +169,33 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// L2 eviction-priority policies for the cache-hinted copies below: lines read by a copy
+// with evict_first are the first candidates for eviction (data read once); evict_normal
+// keeps the default priority.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// tma_load_2d with an L2 cache policy for the lines it reads
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *map, uint32_t bar,
+                                                 int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+// Remote 32-bit store into a peer CTA's shared memory (address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t raddr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(raddr), "r"(v) : "memory");
+}
+
 // 3-D tiled load of the box at (x = innermost, y, z); completes its byte count on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint32_t bar, int x,
                                             int y, int z) {

@@ -158,6 +158,16 @@ def make_attention_inputs(w: Workload, seed: int = 0, sigma: float = 1.0,
                 seqlens=L, num_blocks=nblocks, B=B, H=H, scale=float(SCALE_192))
 
 
+def make_attention_queries(w: Workload, seed: int = 0, sigma: float = 1.0):
+    """q_lat and q_rope of one workload, the same values make_attention_inputs draws
+    (same streams), without drawing its cache."""
+    kids = np.random.SeedSequence(seed).spawn(8)
+    B, H = w.batch, w.heads
+    q_lat = _normal_bf16(kids[2], B * H * D_C, sigma).reshape(B, H, D_C)
+    q_rope = _normal_bf16(kids[3], B * H * D_ROPE, sigma).reshape(B, H, D_ROPE)
+    return q_lat, q_rope
+
+
 def make_step_inputs(w: Workload, seed: int = 0, prefilled: int | None = None):
     """Inputs of the full absorbed decode step: weights, hidden states, cache, tables.
 

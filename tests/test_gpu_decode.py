@@ -232,3 +232,26 @@ def test_reference_raised_by_one_half_mid_sequence(mla, splits):
     ref, lref = _oracle(d, cache=cache)
     assert_close_rows(out, ref)
     assert_lse(lse, lref)
+
+
+@pytest.mark.parametrize("splits", [1, 0])
+def test_seqlen_beyond_max_seqlen_is_reported_and_clamped(mla, splits):
+    """A length above the call's max_seqlen (still inside the block table) is recorded as
+    MLA_ERR_OUT_OF_RANGE and clamped to max_seqlen, on the fixed-split path and on the
+    balanced schedule alike (so neither silently truncates to its own token ranges)."""
+    B = 100 if splits == 0 else 3  # 100 sequences: more than one wave -> the schedule
+    rng = np.random.default_rng(11)
+    L = rng.integers(1, 300, size=B).astype(np.int32)
+    L[1] = 700  # within the table (built for 700) but above the max_seqlen passed below
+    d = _case(B, 64, tuple(int(x) for x in L), seed=12)
+    max_len = 500
+    if splits == 0:
+        assert mla.decode_plan(B, 64, max_len, 0)[0] == 0
+    t = _to_dev(d)
+    out, lse, ws = mla.decode_attention(t["q_lat"], t["q_rope"], t["cache"], t["bt"],
+                                        t["seqlens"], max_len, d["scale"], splits)
+    assert mla.check_device_status(ws) == 4  # MLA_ERR_OUT_OF_RANGE
+    clamped = dict(d, seqlens=np.minimum(d["seqlens"], max_len))
+    ref, lref = _oracle(clamped)
+    assert_close_rows(host_f64_from_bf16(out), ref)
+    assert_lse(lse.cpu().numpy(), lref)
