@@ -234,6 +234,42 @@ mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int 
                                 mla_bf16_t *out, float *lse, mla_stream_t stream);
 
 /*
+ * Context-parallel decode, one rank's share ("DeepSeek V3 MoE inference" §3: decode attention
+ * deployed as TP4 + SP4 + DP; "from the memory wall to the compute wall" §2.3: every head
+ * reads the same compressed cache, so splitting heads does not split the bytes, splitting
+ * tokens does). The cached tokens of each sequence are spread over G ranks by token range
+ * (each rank holds its range's rows in its own paged cache; k_rope is stored rotated at each
+ * row's absolute position, so scores do not depend on which rank holds a row). Each rank
+ * calls this with its own cache, block table and seqlens (the lengths of its ranges) and
+ * gets, per (b, h), the attention over its range alone, normalised, in fp32, with its
+ * log-sum-exp:
+ *   o_part[b][h] = sum_{j in range} softmax_range(s)_j c_kv_j,  lse_part[b][h] = ln sum exp(s_j)
+ * (an empty range gives o_part = 0, lse_part = -inf). The ranks then exchange
+ * (o_part, lse_part) -- an all-gather, outside this library -- and mla_decode_combine_ranks
+ * merges them exactly. Arguments, checks, workspace and plans as mla_decode_attention;
+ * o_part [B][H][512] fp32 (16-byte aligned), lse_part [B][H] fp32.
+ */
+mla_status_t mla_decode_attention_partial(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                          const mla_bf16_t *kv_cache, int num_blocks,
+                                          const int32_t *block_table, int max_blocks,
+                                          const int32_t *seqlens, int B, int H, int max_seqlen,
+                                          float scale, int num_splits, void *workspace,
+                                          size_t ws_bytes, float *o_part, float *lse_part,
+                                          mla_stream_t stream);
+
+/*
+ * The merge of G context-parallel ranks' partial results (the same exact log-sum-exp merge as
+ * mla_decode_combine, with the parts laid out by rank, as an all-gather leaves them):
+ *   lse[b][h] = ln sum_g exp(lse_parts[g][b][h]);
+ *   out[b][h] = sum_g exp(lse_parts[g][b][h] - lse[b][h]) * o_parts[g][b][h]
+ * o_parts [G][B][H][512] fp32, lse_parts [G][B][H] fp32 -> out [B][H][512] bf16,
+ * lse [B][H] fp32. Ranges with lse = -inf weigh zero; all-empty gives out = 0, lse = -inf.
+ * Needs no workspace. 1 <= G <= 4096, 1 <= B <= 4096.
+ */
+mla_status_t mla_decode_combine_ranks(const float *o_parts, const float *lse_parts, int G, int B,
+                                      int H, mla_bf16_t *out, float *lse, mla_stream_t stream);
+
+/*
  * mla_decode_attention without a workspace: the same computation and outputs, for
  * callers that cannot obtain device memory for scratch -- code running while a
  * stream is captured into a CUDA graph (an allocation there is illegal or ends the

@@ -53,6 +53,9 @@ _SIGS = {
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "mla_decode_attention_partial": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
+                                      _sz, _vp, _vp, _vp], _i),
+    "mla_decode_combine_ranks": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
     "mla_decode_mq_workspace_size": ([_i, _i, _i, _i, _i, _szp], _i),
     "mla_decode_attention_mq": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _f, _i, _vp,
                                  _sz, _vp, _vp, _vp], _i),
@@ -267,6 +270,45 @@ def decode_combine(o_part, lse_part, out=None, lse=None, stream=None):
     rc = _lib.mla_decode_combine(_ptr(o_part), _ptr(lse_part), B, S, H, _ptr(out), _ptr(lse),
                                  _stream(stream))
     _ok(rc, "mla_decode_combine")
+    return out, lse
+
+
+def decode_attention_partial(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, scale,
+                             num_splits=0, o_part=None, lse_part=None, workspace=None,
+                             stream=None):
+    """mla_decode_attention_partial: attention over this rank's token ranges only.
+    Returns (o_part [B,H,512] fp32, lse_part [B,H] fp32, workspace)."""
+    B, H, _ = q_lat.shape
+    dev = q_lat.device
+    if o_part is None:
+        o_part = torch.empty((B, H, D_C), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(decode_workspace_size(B, H, max_seqlen, num_splits),
+                                    stream=stream)
+    rc = _lib.mla_decode_attention_partial(_ptr(_bits(q_lat)), _ptr(_bits(q_rope)),
+                                           _ptr(_bits(kv_cache)), kv_cache.shape[0],
+                                           _ptr(block_table), block_table.shape[1],
+                                           _ptr(seqlens), B, H, int(max_seqlen), float(scale),
+                                           int(num_splits), _ptr(workspace), workspace.numel(),
+                                           _ptr(o_part), _ptr(lse_part), _stream(stream))
+    _ok(rc, "mla_decode_attention_partial")
+    return o_part, lse_part, workspace
+
+
+def decode_combine_ranks(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """mla_decode_combine_ranks: o_parts [G,B,H,512] fp32, lse_parts [G,B,H] fp32 ->
+    (out [B,H,512] bf16, lse [B,H] fp32)."""
+    G, B, H, _ = o_parts.shape
+    dev = o_parts.device
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    rc = _lib.mla_decode_combine_ranks(_ptr(o_parts), _ptr(lse_parts), G, B, H, _ptr(out),
+                                       _ptr(lse), _stream(stream))
+    _ok(rc, "mla_decode_combine_ranks")
     return out, lse
 
 
