@@ -22,11 +22,12 @@
 // reference is only raised when a score exceeds it by more than 2^8) and run P . V over
 // all 64 tokens for their own columns.
 //
-// Tensor memory (512 columns): O fp32 [0, 256), S fp32 [256, 288), Q bf16 pairs of
-// column chunks 0..6 [288, 512). Q chunks 7 (c_kv[448:512]) and 8 (k_rope) are read from
-// shared memory. The chunks of a tile sit in three rings sized by how long they are held:
-// the own tokens' own output columns (both products, 5 slots), the own tokens' other
-// columns and k_rope (scores only, 2 slots) and the peer tokens' own output columns
+// Tensor memory (512 columns): O fp32 [0, 256), S fp32 in two buffers [256, 320) (the
+// scores of the next tile are computed while the softmax still works on this one), Q bf16
+// pairs of column chunks 0..5 [320, 512). Q chunks 6, 7 (c_kv[384:512]) and 8 (k_rope) are
+// read from shared memory. The chunks of a tile sit in three rings sized by how long they
+// are held: the own tokens' own output columns (both products, 4 slots), the own tokens'
+// other columns and k_rope (scores only, 2 slots) and the peer tokens' own output columns
 // (P . V only, loaded late, 2 slots). P halves are double-buffered: the local half is the
 // A operand of P . V for the own tokens, the received half for the peer's.
 //
@@ -59,18 +60,19 @@ constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_r
 //   KV: own tokens x own output columns (4 chunks) -- both products, until P.V
 //   K : own tokens x the other 4 c_kv chunks and k_rope (5 chunks) -- scores only
 //   V : peer tokens x own output columns (4 chunks) -- P.V only, loaded later
-constexpr int NKV = 4, NK = 2, NV = 3;        // slots per ring
+constexpr int NKV = 4, NK = 2, NV = 2;        // slots per ring
 constexpr int KV_SLOT = 4 * CH, K_SLOT = 5 * CH, V_SLOT = 4 * CH;
-constexpr int NQT = 7;                        // Q chunks held in TMEM (the rest in smem)
+constexpr int NQT = 6;                        // Q chunks held in TMEM (the rest in smem)
+constexpr int NQS = NOWN - NQT;               // Q chunks in smem (c_kv[384:512), k_rope)
 constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
 constexpr int PGRP = 8 * 64 + 8 * 8;          // 8 rows: their 32 bf16 of P, then (reference, sum)
 constexpr int PBUF = 16 * PGRP;               // P half of 128 rows with its row data (9 KB)
 constexpr int PWARP = 4 * PGRP;               // the 32 rows of one warp (contiguous)
-constexpr int KV_OFF = 0;
+constexpr int QS_OFF = 0;
+constexpr int KV_OFF = QS_OFF + NQS * QCH;
 constexpr int K_OFF = KV_OFF + NKV * KV_SLOT;
 constexpr int V_OFF = K_OFF + NK * K_SLOT;
-constexpr int QS_OFF = V_OFF + NV * V_SLOT;
-constexpr int SEND_OFF = QS_OFF + 2 * QCH;    // local P half, x2
+constexpr int SEND_OFF = V_OFF + NV * V_SLOT;  // local P half, x2
 constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
 constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
 constexpr int NBAR = 40;
@@ -86,8 +88,8 @@ constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024
 constexpr int NTHREADS = 224;                 // 7 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
-constexpr uint32_t TM_S = 256;                // S: fp32 columns [256, 288)
-constexpr uint32_t TM_Q = 288;                // Q chunks 0..6: bf16 pairs, [288, 512)
+constexpr uint32_t TM_S = 256;                // S, two buffers: fp32 columns [256, 320)
+constexpr uint32_t TM_Q = 320;                // Q chunks 0..5: bf16 pairs, [320, 512)
 constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
@@ -98,15 +100,18 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(QS_OFF % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && CH % 1024 == 0,
+static_assert(QS_OFF % 1024 == 0 && KV_OFF % 1024 == 0 && K_OFF % 1024 == 0 &&
+                  V_OFF % 1024 == 0 && CH % 1024 == 0,
               "128-byte-swizzled operands need 1024-byte-aligned atoms");
 static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
 static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
-static_assert(2 * (NKV + NK + NV) + 20 <= NBAR, "mbarrier count");
-// Q rows staged in the idle rings between segments: one row (q_lat then q_rope) per
-// 1168 bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
+static_assert(2 * (NKV + NK + NV) + 23 <= NBAR, "mbarrier count");
+// Q rows staged between segments in the idle rings and local P buffers (from KV_OFF up to
+// the peer's P buffers, which stay untouched): one row (q_lat then q_rope) per 1168
+// bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
 constexpr int QSTG = 2 * (D_C + D_ROPE) + 16;
-static_assert(128 * QSTG <= QS_OFF - KV_OFF && QSTG % 16 == 0, "Q staging area");
+static_assert(KV_OFF + 128 * QSTG <= RECV_OFF && QSTG % 16 == 0, "Q staging area");
+static_assert(QS_OFF + NQS * QCH <= KV_OFF, "staged Q rows never overlap the Q chunks in smem");
 static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -161,18 +166,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     auto v_full = [&](int s) { return bar + 8u * (2 * NKV + 2 * NK + s); };
     auto v_empty = [&](int s) { return bar + 8u * (2 * NKV + 2 * NK + NV + s); };
     const uint32_t q_ready = bar + 8u * (2 * NKV + 2 * NK + 2 * NV);
-    const uint32_t s_full = q_ready + 8;
-    const uint32_t s_free = q_ready + 16;
-    auto p_ready = [&](int x) { return q_ready + 24 + 8u * x; };  // both P halves of tile parity x
-    auto pv_done = [&](int x) { return q_ready + 40 + 8u * x; };  // P.V of tile parity x finished
+    // scores of tile parity x in their TMEM buffer / read out by the softmax warps
+    auto s_full = [&](int x) { return q_ready + 8 + 8u * x; };
+    auto s_free = [&](int x) { return q_ready + 24 + 8u * x; };
+    auto p_ready = [&](int x) { return q_ready + 40 + 8u * x; };  // both P halves of tile parity x
+    auto pv_done = [&](int x) { return q_ready + 56 + 8u * x; };  // P.V of tile parity x finished
     // the peer's P.V of tile parity x finished (our P half in its buffer x may be
     // overwritten); arrived on by the peer's tcgen05.commit
-    auto rfree = [&](int x) { return q_ready + 56 + 8u * x; };
-    const uint32_t mma_drain = q_ready + 72;
-    const uint32_t pv_drain = q_ready + 144;
-    const uint32_t qs_full = q_ready + 152;  // the next segment's Q rows staged
+    auto rfree = [&](int x) { return q_ready + 72 + 8u * x; };
+    const uint32_t mma_drain = q_ready + 88;
+    const uint32_t pv_drain = q_ready + 96;
+    const uint32_t qs_full = q_ready + 104;  // the next segment's Q rows staged
     // the peer's P half of the rows of warp quadrant q has landed in buffer x
-    auto recv_full = [&](int q, int x) { return q_ready + 80 + 8u * (2 * q + x); };
+    auto recv_full = [&](int q, int x) { return q_ready + 112 + 8u * (2 * q + x); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF + M_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + M_ABORT);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + MISC_OFF);
@@ -192,9 +198,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             mbar_init(v_empty(s), 1);
         }
         mbar_init(q_ready, 4);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 4);
         for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_free(x), 4);
             mbar_init(p_ready(x), 4);
             mbar_init(pv_done(x), 1);
             mbar_init(rfree(x), 1);
@@ -450,10 +456,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
             };
             const uint32_t qs = sb + QS_OFF;
-            // scores of this CTA's 32 tokens of tile i over all 576 columns
+            // scores of this CTA's 32 tokens of tile i over all 576 columns, into the S
+            // buffer of the tile's parity
             auto issue_s = [&](int i) {
                 const uint32_t kv = sb + KV_OFF + (i % NKV) * KV_SLOT;
                 const uint32_t ko = sb + K_OFF + (i % NK) * K_SLOT;
+                const uint32_t sd = tmem + TM_S + 32u * (i & 1);
 #pragma unroll
                 for (int d = 0; d < NOWN; ++d)
 #pragma unroll
@@ -466,23 +474,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                                               : ko + (d < 8 ? d - 4 * static_cast<int>(peer) : 4) * CH;
                         const uint64_t bdesc = sdesc_sw128(src + kk * 32, 16, 1024);
                         if (d < NQT)
-                            tc_mma_ts_if(leader, tmem + TM_S, tmem + TM_Q + 32 * d + 8 * kk, bdesc,
-                                         IDESC_S, (d | kk) != 0);
+                            tc_mma_ts_if(leader, sd, tmem + TM_Q + 32 * d + 8 * kk, bdesc, IDESC_S,
+                                         (d | kk) != 0);
                         else
-                            tc_mma_if(leader, tmem + TM_S,
+                            tc_mma_if(leader, sd,
                                       sdesc_sw128(qs + (d - NQT) * QCH + kk * 32, 16, 1024), bdesc,
                                       IDESC_S, 1);
                     }
-                tc_commit_if(leader, s_full);
+                tc_commit_if(leader, s_full(i & 1));
                 tc_commit_if(leader, k_empty(i % NK));
             };
-            // scores of tile k need its cache chunks and the S columns back from the
-            // softmax (s_free of tile k-1)
+            // scores of tile k need its cache chunks and their S buffer back from the
+            // softmax (s_free of tile k-2): with two buffers the scores of the next tile
+            // are computed while the softmax still works on this one
             bool ok = wait_all(q_ready, 0);
             for (int k = 0; ok && k < n; ++k) {
                 if (!(ok = wait_all(kv_full(k % NKV), (k / NKV) & 1))) break;
                 if (!(ok = wait_all(k_full(k % NK), (k / NK) & 1))) break;
-                if (k > 0 && !(ok = wait_all(s_free, (k - 1) & 1))) break;
+                if (k > 1 && !(ok = wait_all(s_free(k & 1), ((k - 2) >> 1) & 1))) break;
                 tc_fence_after();
                 issue_s(k);
                 __syncwarp();
@@ -585,14 +594,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             const uint32_t vs = sb + V_OFF + (i % NV) * V_SLOT;
 
             // ---- scores of this CTA's 32 tokens, out of TMEM (releasing S)
-            if (!(ok = wait_w(s_full, i & 1))) break;
+            if (!(ok = wait_w(s_full(x), (i >> 1) & 1))) break;
             tc_fence_after();
             uint32_t sr[32];
-            tmem_ld32(tl + TM_S, sr);
+            tmem_ld32(tl + TM_S + 32u * x, sr);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(s_free(x));
 
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int tvalid = blk_ok ? min(TOK, L - tile * TOK) : 0;  // valid tokens of the tile
