@@ -52,6 +52,8 @@ def lib():
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_i8p = ctypes.POINTER(ctypes.c_int8)
 _i = ctypes.c_int
 _d = ctypes.c_double
 
@@ -82,6 +84,17 @@ def _declare(L):
     L.mla_oracle_absorb_q.restype = _i
     L.mla_oracle_out_absorb.argtypes = [_f64p, _i, _i, _i, _i, _u16p, _u16p, _i, _f64p]
     L.mla_oracle_out_absorb.restype = _i
+    L.mla_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    L.mla_oracle_e4m3_to_f64.restype = _d
+    L.mla_oracle_f64_to_e4m3.argtypes = [_d]
+    L.mla_oracle_f64_to_e4m3.restype = ctypes.c_uint8
+    L.mla_oracle_quantize_rows_fp8.argtypes = [_f64p, ctypes.c_long, _i, _u8p, _i8p]
+    L.mla_oracle_quantize_rows_fp8.restype = None
+    L.mla_oracle_dequantize_rows_fp8.argtypes = [_u8p, _i8p, ctypes.c_long, _i, _f64p]
+    L.mla_oracle_dequantize_rows_fp8.restype = None
+    L.mla_oracle_append_kv_fp8.argtypes = [_u16p, _i, _i, _u16p, _i, _i, _i32p, _i32p, _i, _u8p,
+                                           _i8p, _i, _i, _d]
+    L.mla_oracle_append_kv_fp8.restype = _i
 
 
 def _p(a, t):
@@ -252,6 +265,79 @@ def prefill_expanded(q_nope, q_rope, kv_cache, block_table_row, prefix, w_uk, w_
             out[i, h] = (e / den) @ v[h, :n]
             lse[i, h] = mx + np.log(den)
     return out, lse
+
+
+# ------------------------------------------------------------ fp8 cache
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of an e4m3 code (1-4-3, bias 7, no infinities, all-ones = NaN)."""
+    return float(lib().mla_oracle_e4m3_to_f64(int(code) & 0xFF))
+
+
+def f64_to_e4m3(x: float) -> int:
+    """Nearest e4m3 code, ties to the even mantissa, saturating at 448."""
+    return int(lib().mla_oracle_f64_to_e4m3(float(x)))
+
+
+def quantize_rows_fp8(x):
+    """Rows of values [..., D] (float64) -> (codes uint8 [..., D], exps int8 [...]): per row
+    the power-of-two scale 2^e with e the smallest integer such that max|x| 2^-e <= 448."""
+    x = _f64(x)
+    shp = x.shape
+    D = shp[-1]
+    rows = int(np.prod(shp[:-1])) if len(shp) > 1 else 1
+    codes = np.zeros(shp, dtype=np.uint8)
+    exps = np.zeros(shp[:-1], dtype=np.int8)
+    lib().mla_oracle_quantize_rows_fp8(_p(x, _f64p), rows, D, _p(codes, _u8p), _p(exps, _i8p))
+    return codes, exps
+
+
+def dequantize_fp8(codes, exps):
+    """codes [..., D] uint8, exps [...] int8 -> code * 2^e as float64."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    exps = np.ascontiguousarray(exps, dtype=np.int8)
+    D = codes.shape[-1]
+    rows = int(np.prod(codes.shape[:-1])) if codes.ndim > 1 else 1
+    out = np.zeros(codes.shape)
+    lib().mla_oracle_dequantize_rows_fp8(_p(codes, _u8p), _p(exps, _i8p), rows, D,
+                                         _p(out, _f64p))
+    return out
+
+
+def fp8_cache_as_bf16(codes, exps):
+    """The dequantised FP8 cache as bf16 bits. Every value code * 2^e has at most 4
+    significant bits, so it is exactly a bf16 value (checked)."""
+    v = dequantize_fp8(codes, exps).astype(np.float32)
+    bits = v.view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "dequantised value not exact in bf16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def append_kv_fp8(h, w_dkr, pos, block_table, kv_codes, kv_exps, d_c=512, rope_theta=10000.0,
+                  allow_range=False):
+    """append_kv into an FP8 cache: the fp64 row is quantised (per-row power-of-two scale)
+    and written into kv_codes [nb, bs, D] uint8 and kv_exps [nb, bs] int8 (in place)."""
+    h, w_dkr = _u16(h), _u16(w_dkr)
+    assert kv_codes.flags.c_contiguous and kv_codes.dtype == np.uint8
+    assert kv_exps.flags.c_contiguous and kv_exps.dtype == np.int8
+    B, dm = h.shape
+    D = w_dkr.shape[0]
+    nb, bs, D2 = kv_codes.shape
+    assert D2 == D and kv_exps.shape == (nb, bs)
+    bt, pos = _i32(block_table), _i32(pos)
+    rc = lib().mla_oracle_append_kv_fp8(_p(h, _u16p), B, dm, _p(w_dkr, _u16p), d_c, D - d_c,
+                                        _p(pos, _i32p), _p(bt, _i32p), bt.shape[1],
+                                        _p(kv_codes, _u8p), _p(kv_exps, _i8p), nb, bs,
+                                        float(rope_theta))
+    return _check(rc, allow_range)
+
+
+def decode_absorbed_fp8(q_lat, q_rope, kv_codes, kv_exps, block_table, seqlens, scale,
+                        allow_range=False):
+    """Absorbed decode attention over an FP8 cache: the attention of decode_absorbed over
+    the dequantised rows code * 2^e (exactly bf16 values, so the bf16 routine applies)."""
+    return decode_absorbed(q_lat, q_rope, fp8_cache_as_bf16(kv_codes, kv_exps), block_table,
+                           seqlens, scale, allow_range=allow_range)
 
 
 def combine(o_part, lse_part):

@@ -179,6 +179,143 @@ int mla_oracle_append_kv(const uint16_t *h, int B, int d_model, const uint16_t *
     return status;
 }
 
+/* ------------------------------------------------------------- fp8 cache */
+
+/*
+ * FP8 latent cache ("LLM inference: from the memory wall to the compute wall" §5 names a
+ * mixed-precision FP8/FP16 KV cache as the next step; "DeepSeek V3 MLA optimisation" turns
+ * on FP8 quantisation of the KV cache). The pages fix no format; the reading taken here:
+ *  - each value is stored as an e4m3 code: 1 sign bit, 4 exponent bits with bias 7, 3
+ *    mantissa bits; exponent field 0 holds the subnormals m/8 * 2^-6; there are no
+ *    infinities and the all-ones code of either sign is NaN, so the largest finite
+ *    magnitude is 1.75 * 2^8 = 448;
+ *  - rounding is to the nearest value, ties to the even mantissa, and magnitudes beyond
+ *    448 saturate to 448;
+ *  - every cached row (one token: [c_kv | k_rope]) carries one power-of-two scale 2^e,
+ *    e the smallest integer with max|x| * 2^-e <= 448 (e = 0 for an all-zero row), and the
+ *    codes hold x * 2^-e. The dequantised value is code * 2^e, exactly.
+ */
+
+/* Value of an e4m3 code, straight from the format definition (NaN codes give NaN). */
+double mla_oracle_e4m3_to_f64(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* The e4m3 code nearest to x (ties to the even mantissa; saturating at 448; the sign of
+ * x is kept, also for a result of zero). NaN gives the positive NaN code. */
+uint8_t mla_oracle_f64_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* spacing of the representable values around a: 2^-9 below 2^-6, else 2^(E-3) for
+     * a in [2^E, 2^(E+1)) */
+    double quantum;
+    if (a < ldexp(1.0, -6)) {
+        quantum = ldexp(1.0, -9);
+    } else {
+        int E;
+        frexp(a, &E); /* a = f * 2^E with f in [0.5, 1) */
+        quantum = ldexp(1.0, (E - 1) - 3);
+    }
+    double n = nearbyint(a / quantum); /* exact division; default mode: ties to even */
+    double v = n * quantum;            /* may step up to the next binade: still exact */
+    if (v > 448.0)
+        v = 448.0;
+    if (v < ldexp(1.0, -6))
+        return sign | (uint8_t)(v / ldexp(1.0, -9)); /* subnormal or zero: m = v / 2^-9 */
+    int E;
+    double f = frexp(v, &E); /* v = f * 2^E, f in [0.5, 1); as 1.mmm * 2^(E-1) */
+    int mant = (int)((2.0 * f - 1.0) * 8.0);
+    return sign | (uint8_t)(((E - 1 + 7) << 3) | mant);
+}
+
+/* One row of D values -> e4m3 codes and the exponent e of its power-of-two scale. */
+void mla_oracle_quantize_row_fp8(const double *x, int D, uint8_t *codes, int8_t *e_out)
+{
+    double mx = 0.0;
+    for (int n = 0; n < D; ++n)
+        if (fabs(x[n]) > mx)
+            mx = fabs(x[n]);
+    int e = 0;
+    if (mx > 0.0) {
+        e = (int)ceil(log2(mx / 448.0));
+        while (ldexp(mx, -e) > 448.0) /* make e the smallest with mx * 2^-e <= 448 */
+            ++e;
+        while (ldexp(mx, -(e - 1)) <= 448.0)
+            --e;
+    }
+    for (int n = 0; n < D; ++n)
+        codes[n] = mla_oracle_f64_to_e4m3(ldexp(x[n], -e));
+    *e_out = (int8_t)e;
+}
+
+/* rows x D values -> codes [rows][D] and exps [rows]. */
+void mla_oracle_quantize_rows_fp8(const double *x, long rows, int D, uint8_t *codes,
+                                  int8_t *exps)
+{
+    for (long r = 0; r < rows; ++r)
+        mla_oracle_quantize_row_fp8(x + r * D, D, codes + r * D, exps + r);
+}
+
+/* codes [rows][D], exps [rows] -> the dequantised values code * 2^e. */
+void mla_oracle_dequantize_rows_fp8(const uint8_t *codes, const int8_t *exps, long rows, int D,
+                                    double *out)
+{
+    for (long r = 0; r < rows; ++r)
+        for (int n = 0; n < D; ++n)
+            out[r * D + n] = ldexp(mla_oracle_e4m3_to_f64(codes[r * D + n]), exps[r]);
+}
+
+/* mla_oracle_append_kv into an FP8 cache: the projected, rotated row (fp64) is quantised
+ * as above and written as codes into kv_codes [num_blocks][block_size][D] and its exponent
+ * into kv_exps [num_blocks][block_size]. */
+int mla_oracle_append_kv_fp8(const uint16_t *h, int B, int d_model, const uint16_t *w_dkr,
+                             int d_c, int d_rope, const int32_t *pos, const int32_t *block_table,
+                             int max_blocks, uint8_t *kv_codes, int8_t *kv_exps, int num_blocks,
+                             int block_size, double rope_theta)
+{
+    int D = d_c + d_rope;
+    if (B < 0 || d_model <= 0 || d_c <= 0 || d_rope < 0 || (d_rope & 1) || block_size <= 0)
+        return ORC_ERR_ARG;
+    double *x = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!x)
+        return ORC_ERR_ARG;
+    int status = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        int p = pos[b];
+        if (p < 0 || p / block_size >= max_blocks) {
+            status = ORC_ERR_RANGE;
+            continue;
+        }
+        int blk = block_table[(size_t)b * max_blocks + p / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            status = ORC_ERR_RANGE;
+            continue;
+        }
+        for (int n = 0; n < D; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < d_model; ++k)
+                acc += bf16_to_f64(h[(size_t)b * d_model + k]) *
+                       bf16_to_f64(w_dkr[(size_t)n * d_model + k]);
+            x[n] = acc;
+        }
+        rope_rotate(x + d_c, d_rope, p, rope_theta);
+        size_t slot = (size_t)blk * block_size + (size_t)(p % block_size);
+        mla_oracle_quantize_row_fp8(x, D, kv_codes + slot * D, kv_exps + slot);
+    }
+    free(x);
+    return status;
+}
+
 /* ---------------------------------------------------- attention, absorbed */
 
 /*
