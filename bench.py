@@ -619,8 +619,8 @@ def run_gpu_prefill(args):
     print(json.dumps(line), flush=True)
 
 
-ATTN_CONFIGS = ("v3", "mixed", "long")
-ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70}
+ATTN_CONFIGS = ("v3", "mixed", "long", "long_fp8")
+ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70, "long_fp8": None}
 
 
 def time_attention_configs(pool, dev, launches: int, num_splits: int):
@@ -637,8 +637,12 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
     stream = torch.cuda.current_stream(dev)
     nb_pool = pool.shape[0]
     out_all = {}
+    fp8_pool = None
     for name in ATTN_CONFIGS:
-        w = synth.WORKLOADS[name]
+        fp8 = name.endswith("_fp8")
+        w = synth.WORKLOADS[name[:-4] if fp8 else name]
+        if fp8 and fp8_pool is None:  # the same pool as e4m3 codes with row exponents
+            fp8_pool = mla.quantize_kv_fp8(pool)
         L = synth.draw_seqlens(w, 0)
         bt, nblk = synth.make_block_table(L, w.shuffled, 0)
         if nblk > nb_pool:
@@ -667,8 +671,12 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
         lse = torch.empty((B, H), dtype=torch.float32, device=dev)
 
         def attend(i):
-            mla.decode_attention(q_lat, q_rope, pool, bts[i % rot], Ld, max_len,
-                                 synth.SCALE_192, num_splits, out, lse, ws)
+            if fp8:
+                mla.decode_attention_fp8(q_lat, q_rope, fp8_pool[0], fp8_pool[1], bts[i % rot], Ld,
+                                         max_len, synth.SCALE_192, num_splits, out, lse, ws)
+            else:
+                mla.decode_attention(q_lat, q_rope, pool, bts[i % rot], Ld, max_len,
+                                     synth.SCALE_192, num_splits, out, lse, ws)
 
         for i in range(3):
             attend(i)
@@ -682,7 +690,7 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
         if mla.check_device_status(ws) != 0:
             raise RuntimeError(f"device error in the {name} attention timing")
         ms = e0.elapsed_time(e1) / launches
-        byts = synth.algorithmic_attention_bytes(L, H)
+        byts = synth.algorithmic_attention_bytes(L, H, kv_bytes_per_value=1 if fp8 else 2)
         flops = synth.attention_flops(L, H)
         roof_s = max(byts / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
         out_all[name] = {
@@ -696,7 +704,8 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
             "plan": {"splits": mla.decode_plan(B, H, max_len, num_splits)[0]},
             "l2": (f"{rot} disjoint block ranges rotated" if rot > 1
                    else "cache larger than L2"),
-            "algorithmic_bytes": byts}
+            "algorithmic_bytes": byts,
+            "cache": "e4m3 codes + one power-of-two scale exponent per token" if fp8 else "bf16"}
         del ws, out, lse, bts, q_lat, q_rope
     return out_all
 

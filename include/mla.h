@@ -305,6 +305,46 @@ mla_status_t mla_decode_attention_noalloc(const mla_bf16_t *q_lat, const mla_bf1
                                           float scale, int num_splits, mla_bf16_t *out,
                                           float *lse, mla_stream_t stream);
 
+/* ------------------------------------------------------ FP8 latent cache */
+
+/*
+ * FP8 (e4m3) latent cache ("LLM inference: from the memory wall to the compute wall" §5:
+ * a mixed-precision FP8/FP16 KV cache; "DeepSeek V3 MLA optimisation" §3: FP8 quantisation
+ * of the KV cache). The pages fix no format; this library's format:
+ *   kv_codes [num_blocks][64][576] uint8: e4m3 codes (1 sign, 4 exponent bits with bias
+ *     7, 3 mantissa bits; largest finite 448; no infinities) of the row divided by its
+ *     scale, rounded to nearest with ties to even, saturating at 448;
+ *   kv_exps [num_blocks][64] int8: per cached row (one token) the exponent e of its scale
+ *     2^e, the smallest with max|x| * 2^-e <= 448 (0 for an all-zero row; at least -126).
+ * A row's dequantised values are code * 2^e, which are exactly bf16 values, so attention
+ * over an FP8 cache equals attention over that dequantised cache. Half the cache bytes
+ * of bf16 (plus one byte per token). Both arrays: device memory, 16-byte aligned.
+ */
+
+/* rows x 576 bf16 values -> codes [rows][576] and exps [rows]. Asynchronous. */
+mla_status_t mla_quantize_kv_fp8(const mla_bf16_t *rows_bf16, long rows, uint8_t *codes,
+                                 int8_t *exps, mla_stream_t stream);
+/* codes [rows][576] and exps [rows] -> the dequantised rows as bf16 (exact). */
+mla_status_t mla_dequantize_kv_fp8(const uint8_t *codes, const int8_t *exps, long rows,
+                                   mla_bf16_t *rows_bf16, mla_stream_t stream);
+/* mla_append_kv into an FP8 cache: the projected, rotated row is quantised (from fp32)
+ * into kv_codes / kv_exps at slot pos[b]. Same arguments and workspace as
+ * mla_append_kv otherwise. */
+mla_status_t mla_append_kv_fp8(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                               const int32_t *pos, const int32_t *block_table, int max_blocks,
+                               uint8_t *kv_codes, int8_t *kv_exps, int num_blocks,
+                               float rope_theta, void *workspace, size_t ws_bytes,
+                               mla_stream_t stream);
+/* mla_decode_attention over an FP8 cache (the same arguments, checks, workspace --
+ * mla_decode_workspace_size -- and plans; the cache tiles are widened to bf16 on chip). */
+mla_status_t mla_decode_attention_fp8(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                      const uint8_t *kv_codes, const int8_t *kv_exps,
+                                      int num_blocks, const int32_t *block_table, int max_blocks,
+                                      const int32_t *seqlens, int B, int H, int max_seqlen,
+                                      float scale, int num_splits, void *workspace,
+                                      size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                      mla_stream_t stream);
+
 /* ------------------------------------------------- absorbed projections */
 
 /*

@@ -183,6 +183,37 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
     return cuda_status(e);
 }
 
+mla_status_t mla_append_kv_fp8(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                               const int32_t *pos, const int32_t *block_table, int max_blocks,
+                               uint8_t *kv_codes, int8_t *kv_exps, int num_blocks,
+                               float rope_theta, void *workspace, size_t ws_bytes,
+                               mla_stream_t stream) {
+    if (!h || !w_dkr || !pos || !block_table || !kv_codes || !kv_exps || !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || max_blocks < 1 || num_blocks < 1 ||
+        !(rope_theta > 0.f) || !isfinite(rope_theta))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_dkr, 16) || !aligned(kv_codes, 16) ||
+        !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    size_t need;
+    mla_append_kv_workspace_size(B, d_model, &need);
+    if (ws_bytes < need) return MLA_ERR_WORKSPACE;
+    int splits, per;
+    plan_ksplit(B, D_QK, d_model, 1, splits, per);
+    float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + HDR);
+    GemmParams g{};
+    g.A = h; g.lda = d_model; g.a_bstride = 0;
+    g.B = w_dkr; g.ldb = d_model; g.b_bstride = 0;
+    g.M = B; g.N = D_QK; g.K = d_model; g.batch = 1;
+    g.k_splits = splits; g.k_per_split = per;
+    g.c_part = part;
+    if (launch_gemm_tc(g, false, S(stream), err_word(workspace)) != cudaSuccess) return MLA_ERR_CUDA;
+    return cuda_status(launch_append_finalize_fp8(part, splits, B, pos, block_table, max_blocks,
+                                                  kv_codes, kv_exps, num_blocks, rope_theta,
+                                                  err_word(workspace), S(stream)));
+}
+
 // ---------------------------------------------------------------- decode
 
 mla_status_t mla_decode_workspace_size(int B, int H, int max_seqlen, int num_splits,
@@ -284,18 +315,22 @@ namespace {
 // Decode over H = s_q x hq query rows per sequence (query token t, head h at row t*hq + h);
 // token t sees the rows j < seqlens[b] - (s_q - 1 - t). Plain decode: s_q = 1, hq = H.
 // The output goes to `out` as bf16, or, when out_f32 is given, to out_f32 as fp32.
+// The cache is bf16 rows (kv_cache), or e4m3 codes with row exponents (codes, exps).
 mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                         const mla_bf16_t *kv_cache, int num_blocks, const int32_t *block_table,
                         int max_blocks, const int32_t *seqlens, int B, int s_q, int hq,
                         int max_seqlen, float scale, int num_splits, void *workspace,
                         size_t ws_bytes, mla_bf16_t *out, float *out_f32, float *lse,
-                        mla_stream_t stream) {
+                        mla_stream_t stream, const uint8_t *codes = nullptr,
+                        const int8_t *exps = nullptr) {
     const int H = s_q * hq;
     const void *out_any = out_f32 ? static_cast<const void *>(out_f32) : out;
-    const mla_status_t v = decode_validate(q_lat, q_rope, kv_cache, num_blocks, block_table,
+    const void *cache_any = codes ? static_cast<const void *>(codes) : kv_cache;
+    const mla_status_t v = decode_validate(q_lat, q_rope, cache_any, num_blocks, block_table,
                                            max_blocks, seqlens, B, s_q, hq, max_seqlen, scale,
                                            num_splits, out_any, lse);
     if (v != MLA_OK) return v;
+    if (codes && (!exps || !aligned(exps, 16))) return MLA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
     const int splits = plan_decode_splits(B, H, max_seqlen, num_splits);
     const DecodeLayout lay = decode_layout(B, H, max_seqlen, splits);
@@ -305,6 +340,7 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     char *w = static_cast<char *>(workspace);
     DecodeParams p{};
     p.q_lat = q_lat; p.q_rope = q_rope; p.cache = kv_cache;
+    p.codes = codes; p.exps = exps;
     p.block_table = block_table; p.seqlens = seqlens;
     p.num_blocks = num_blocks; p.max_blocks = max_blocks; p.B = B; p.H = H;
     p.max_seqlen = max_seqlen;
@@ -363,6 +399,35 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
     return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
                       1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
                       stream);
+}
+
+mla_status_t mla_decode_attention_fp8(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                      const uint8_t *kv_codes, const int8_t *kv_exps,
+                                      int num_blocks, const int32_t *block_table, int max_blocks,
+                                      const int32_t *seqlens, int B, int H, int max_seqlen,
+                                      float scale, int num_splits, void *workspace,
+                                      size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                      mla_stream_t stream) {
+    if (!kv_codes) return MLA_ERR_INVALID_ARG;
+    return decode_run(q_lat, q_rope, nullptr, num_blocks, block_table, max_blocks, seqlens, B, 1,
+                      H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
+                      stream, kv_codes, kv_exps);
+}
+
+mla_status_t mla_quantize_kv_fp8(const mla_bf16_t *rows_bf16, long rows, uint8_t *codes,
+                                 int8_t *exps, mla_stream_t stream) {
+    if (!rows_bf16 || !codes || !exps || rows < 0 || rows > (1L << 40))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(rows_bf16, 16) || !aligned(codes, 16)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_rows(rows_bf16, rows, codes, exps, S(stream)));
+}
+
+mla_status_t mla_dequantize_kv_fp8(const uint8_t *codes, const int8_t *exps, long rows,
+                                   mla_bf16_t *rows_bf16, mla_stream_t stream) {
+    if (!rows_bf16 || !codes || !exps || rows < 0 || rows > (1L << 40))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned(rows_bf16, 16) || !aligned(codes, 16)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_dequantize_rows(codes, exps, rows, rows_bf16, S(stream)));
 }
 
 mla_status_t mla_decode_attention_partial(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,

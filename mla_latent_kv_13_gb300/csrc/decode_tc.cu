@@ -43,6 +43,7 @@
 // Every mbarrier wait is bounded (about one second); a wait that gives up records
 // MLA_ERR_TIMEOUT in the error word and the CTA drains and exits.
 #include "common.cuh"
+#include "fp8.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
 
@@ -75,17 +76,21 @@ constexpr int V_OFF = K_OFF + NK * K_SLOT;
 constexpr int SEND_OFF = V_OFF + NV * V_SLOT;  // local P half, x2
 constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
 constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
-constexpr int NBAR = 40;
+constexpr int NBAR = 48;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 // MISC: TMEM address, abort flags, and the counts of remote operations exchanged when a
 // pair stops early (byte offsets below)
 constexpr int MISC_BYTES = 128;
 constexpr int M_TMEM = 0, M_ABORT = 4, M_PEER_ABORT = 8, M_PEER_PV = 12, M_PEER_SENT = 16,
               M_SENT = 32, M_RECV = 48, M_PV = 64;
-constexpr int SMEM_USED = MISC_OFF + MISC_BYTES;
+// FP8 cache: each ring slot's 64 row exponents (the block's, one int8 per token)
+constexpr int EXP_OFF = MISC_OFF + MISC_BYTES;
+constexpr int EXP_SLOT = 64;
+constexpr int SMEM_USED = EXP_OFF + (NKV + NK + NV) * EXP_SLOT;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
 
 constexpr int NTHREADS = 224;                 // 7 warps
+constexpr int NTHREADS_FP8 = 320;             // + 3 warps widening the FP8 tiles
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
 constexpr uint32_t TM_S = 256;                // S, two buffers: fp32 columns [256, 320)
@@ -105,7 +110,8 @@ static_assert(QS_OFF % 1024 == 0 && KV_OFF % 1024 == 0 && K_OFF % 1024 == 0 &&
               "128-byte-swizzled operands need 1024-byte-aligned atoms");
 static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
 static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
-static_assert(2 * (NKV + NK + NV) + 23 <= NBAR, "mbarrier count");
+static_assert(3 * (NKV + NK + NV) + 23 <= NBAR, "mbarrier count");
+static_assert(EXP_OFF % 16 == 0, "bulk copies of the row exponents");
 // Q rows staged between segments in the idle rings and local P buffers (from KV_OFF up to
 // the peer's P buffers, which stay untouched): one row (q_lat then q_rope) per 1168
 // bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
@@ -146,7 +152,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > DRAIN_NS) return;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+// FP8 = true: the cache is e4m3 codes with one power-of-two scale per token (row
+// exponents in p.exps). TMA brings each 32-token x 64-column chunk of codes (2 KB) into
+// the upper half of its bf16 slot, with the block's 64 exponents beside the slot; three
+// more warps (one per ring) widen the chunks in place to bf16 code * 2^e -- exact, since
+// such a value has at most four significant bits -- and release the slot to the products
+// on a second barrier. Everything downstream is the bf16 path, unchanged.
+template <bool FP8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 : NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv, DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -179,6 +192,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t qs_full = q_ready + 104;  // the next segment's Q rows staged
     // the peer's P half of the rows of warp quadrant q has landed in buffer x
     auto recv_full = [&](int q, int x) { return q_ready + 112 + 8u * (2 * q + x); };
+    // FP8: the slot's codes have been widened to bf16 (the bf16 kernel uses the full
+    // barriers directly)
+    auto kv_ready = [&](int s) { return FP8 ? q_ready + 176 + 8u * s : kv_full(s); };
+    auto k_ready = [&](int s) { return FP8 ? q_ready + 176 + 8u * (NKV + s) : k_full(s); };
+    auto v_ready = [&](int s) { return FP8 ? q_ready + 176 + 8u * (NKV + NK + s) : v_full(s); };
+    auto exp_kv = [&](int s) { return sb + EXP_OFF + EXP_SLOT * s; };
+    auto exp_k = [&](int s) { return sb + EXP_OFF + EXP_SLOT * (NKV + s); };
+    auto exp_v = [&](int s) { return sb + EXP_OFF + EXP_SLOT * (NKV + NK + s); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF + M_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + M_ABORT);
     volatile int *misc = reinterpret_cast<volatile int *>(smem + MISC_OFF);
@@ -209,6 +230,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         mbar_init(pv_drain, 1);
         mbar_init(qs_full, 4);
         for (int k = 0; k < 8; ++k) mbar_init(recv_full(k >> 1, k & 1), 1);
+        if (FP8) {
+            for (int s = 0; s < NKV; ++s) mbar_init(kv_ready(s), 1);
+            for (int s = 0; s < NK; ++s) mbar_init(k_ready(s), 1);
+            for (int s = 0; s < NV; ++s) mbar_init(v_ready(s), 1);
+        }
         fence_mbar_init();
     };
     if (tid == 0) {
@@ -334,8 +360,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 // own tokens x own output columns
                 if (!mbar_wait(kv_empty(skv), ((i / NKV) & 1) ^ 1, abort_flag, WAIT_NS)) break;
                 if (blk_ok) {
-                    const uint32_t dst = sb + KV_OFF + skv * KV_SLOT;
-                    mbar_arrive_expect_tx(kv_full(skv), KV_SLOT);
+                    // FP8: codes into the upper half of each chunk, exponents beside the slot
+                    const uint32_t dst = sb + KV_OFF + skv * KV_SLOT + (FP8 ? CH / 2 : 0);
+                    mbar_arrive_expect_tx(kv_full(skv), FP8 ? KV_SLOT / 2 + EXP_SLOT : KV_SLOT);
+                    if (FP8) bulk_load(exp_kv(skv), p.exps + (size_t)blk * TOK, EXP_SLOT, kv_full(skv));
                     for (int k = 0; k < 4; ++k)
                         tma_load_2d_hint(dst + k * CH, &map_kv, kv_full(skv), 64 * (4 * rank + k),
                                          y_own, pol_once);
@@ -346,8 +374,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 // own tokens x the other c_kv columns and k_rope
                 if (!mbar_wait(k_empty(sk), ((i / NK) & 1) ^ 1, abort_flag, WAIT_NS)) break;
                 if (blk_ok) {
-                    const uint32_t dst = sb + K_OFF + sk * K_SLOT;
-                    mbar_arrive_expect_tx(k_full(sk), K_SLOT);
+                    const uint32_t dst = sb + K_OFF + sk * K_SLOT + (FP8 ? CH / 2 : 0);
+                    mbar_arrive_expect_tx(k_full(sk), FP8 ? K_SLOT / 2 + EXP_SLOT : K_SLOT);
+                    if (FP8) bulk_load(exp_k(sk), p.exps + (size_t)blk * TOK, EXP_SLOT, k_full(sk));
                     for (int k = 0; k < 4; ++k)
                         tma_load_2d_hint(dst + k * CH, &map_kv, k_full(sk), 64 * (4 * peer + k),
                                          y_own, pol_twice);
@@ -384,8 +413,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                 const int sv = j % NV;
                 const int blk = btab[t_begin + j];
                 if (blk >= 0 && blk < p.num_blocks) {
-                    const uint32_t dst = sb + V_OFF + sv * V_SLOT;
-                    mbar_arrive_expect_tx(v_full(sv), V_SLOT);
+                    const uint32_t dst = sb + V_OFF + sv * V_SLOT + (FP8 ? CH / 2 : 0);
+                    mbar_arrive_expect_tx(v_full(sv), FP8 ? V_SLOT / 2 + EXP_SLOT : V_SLOT);
+                    if (FP8) bulk_load(exp_v(sv), p.exps + (size_t)blk * TOK, EXP_SLOT, v_full(sv));
                     for (int k = 0; k < 4; ++k)
                         tma_load_2d_hint(dst + k * CH, &map_kv, v_full(sv), 64 * (4 * rank + k),
                                          blk * TOK + HALF * peer, pol_once);
@@ -428,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     ++loaded;
                 }
                 if (!(ok = wait_all(p_ready(i & 1), (i >> 1) & 1))) break;
-                if (!(ok = wait_all(v_full(i % NV), (i / NV) & 1))) break;
+                if (!(ok = wait_all(v_ready(i % NV), (i / NV) & 1))) break;
                 tc_fence_after();
                 issue_pv(i);
                 ++n_pv;
@@ -489,8 +519,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // are computed while the softmax still works on this one
             bool ok = wait_all(q_ready, 0);
             for (int k = 0; ok && k < n; ++k) {
-                if (!(ok = wait_all(kv_full(k % NKV), (k / NKV) & 1))) break;
-                if (!(ok = wait_all(k_full(k % NK), (k / NK) & 1))) break;
+                if (!(ok = wait_all(kv_ready(k % NKV), (k / NKV) & 1))) break;
+                if (!(ok = wait_all(k_ready(k % NK), (k / NK) & 1))) break;
                 if (k > 1 && !(ok = wait_all(s_free(k & 1), ((k - 2) >> 1) & 1))) break;
                 tc_fence_after();
                 issue_s(k);
@@ -500,6 +530,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (leader) {
                 tc_commit(mma_drain);
                 drain_wait(mma_drain, 0);
+            }
+        }
+        __syncwarp();
+    } else if (FP8 && warp >= 7) {
+        // --------------------------------------------- FP8: widen the tiles to bf16
+        // Warp 7 widens the K ring (the score products wait for it first), 8 the KV ring,
+        // 9 the V ring, tile by tile as the codes land, chunk by chunk: the warp reads all
+        // of a chunk's codes from its upper half into registers, syncs, then writes the
+        // 64 bf16 values of each row as one 128-byte-swizzled row over the whole chunk
+        // (the layout the bf16 TMA writes).
+        if (n > 0) {
+            const int ring = warp == 7 ? 1 : (warp == 8 ? 0 : 2);  // 0 KV, 1 K, 2 V
+            const int c0 = 0, cstep = 1;
+            const int nslot = ring == 0 ? NKV : (ring == 1 ? NK : NV);
+            const int nch = ring == 1 ? 5 : 4;
+            // the chunks' tokens: this CTA's own 32 for KV and K, the peer's for V
+            const int tok0 = HALF * static_cast<int>(ring == 2 ? peer : rank);
+            for (int i = 0; i < n; ++i) {
+                const int sl = i % nslot;
+                const uint32_t full = ring == 0 ? kv_full(sl) : (ring == 1 ? k_full(sl) : v_full(sl));
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(full, (i / nslot) & 1, abort_flag, WAIT_NS)))
+                    break;
+                const uint32_t base =
+                    sb + (ring == 0 ? KV_OFF + sl * KV_SLOT
+                                    : (ring == 1 ? K_OFF + sl * K_SLOT : V_OFF + sl * V_SLOT));
+                const uint32_t ex =
+                    ring == 0 ? exp_kv(sl) : (ring == 1 ? exp_k(sl) : exp_v(sl));
+                // Load k (of 4) reads 512 contiguous bytes of the staged codes -- rows
+                // 8k .. 8k+7, 64 bytes each -- so lane L holds row r_k = 8k + L/4, columns
+                // 16(L%4) .. 16(L%4)+15: free of bank conflicts. Each row's scale exponent
+                // is the same for every chunk of the tile.
+                uint32_t s2a[4], s2b[4];
+                bool two_steps = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 8 * k + (lane >> 2);
+                    const int e = static_cast<int8_t>(
+                        *reinterpret_cast<const volatile uint8_t *>(smem + (ex - sb) + tok0 + r));
+                    const int ee = e < -126 ? -126 : (e > 127 ? 127 : e);
+                    // code * 2^e = (the shifted f16 pattern, value * 2^-112) * 2^(112 + e), in
+                    // two exact steps when 112 + e > 127
+                    s2a[k] = bf16x2_pow2(112 + ee > 127 ? 127 : 112 + ee);
+                    s2b[k] = bf16x2_pow2(112 + ee > 127 ? 112 + ee - 127 : 0);
+                    two_steps |= 112 + ee > 127;
+                }
+                two_steps = __any_sync(0xffffffffu, two_steps);
+#pragma unroll 1
+                for (int c = c0; c < nch; c += cstep) {
+                    const uint32_t ch = base + c * CH;
+                    uint4 raw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) raw[k] = ld_shared_v4(ch + CH / 2 + k * 512 + lane * 16);
+                    __syncwarp();  // every code is in registers before the chunk is overwritten
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = 8 * k + (lane >> 2);
+                        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            o[2 * q] = e4m3x2_to_bf16x2_mul(static_cast<uint16_t>(w[q] & 0xFFFFu), s2a[k]);
+                            o[2 * q + 1] = e4m3x2_to_bf16x2_mul(static_cast<uint16_t>(w[q] >> 16), s2a[k]);
+                        }
+                        if (two_steps) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(o[q]) : "r"(s2b[k]));
+                        }
+                        // columns 16(L%4) .. +15 are the 16-byte pieces 2(L%4), 2(L%4)+1
+                        const int pc = 2 * (lane & 3);
+                        st_shared_v4(ch + r * 128 + ((pc ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        st_shared_v4(ch + r * 128 + (((pc + 1) ^ (r & 7)) << 4), o[4], o[5], o[6],
+                                     o[7]);
+                    }
+                    __syncwarp();
+                }
+                fence_proxy_async_smem();  // the tensor core reads what these stores wrote
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(ring == 0 ? kv_ready(sl) : (ring == 1 ? k_ready(sl) : v_ready(sl)));
             }
         }
         __syncwarp();
@@ -727,7 +838,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             // still poison the product
             if (tvalid < TOK) {
                 // the value chunks of the peer's tokens may still be in flight
-                if (!(ok = wait_w(v_full(i % NV), (i / NV) & 1))) break;
+                if (!(ok = wait_w(v_ready(i % NV), (i / NV) & 1))) break;
                 const int own_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(rank)));
                 const int peer_from = min(HALF, max(0, tvalid - HALF * static_cast<int>(peer)));
                 const int n_own = (HALF - own_from) * 32;  // 16-byte pieces: rows x 4 x 8
@@ -983,9 +1094,9 @@ int decode_tc_cluster_slots() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_TOTAL) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) == cudaSuccess && n > 0)
+        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) == cudaSuccess && n > 0)
         slots = n;
     else
         slots = device_sm_count() / 2;
@@ -994,13 +1105,31 @@ int decode_tc_cluster_slots() {
 
 cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream) {
     CUtensorMap mkv;
+    dim3 grid(2 * clusters);
+    if (p.codes) {
+        // e4m3 codes [num_blocks * 64 rows][576 bytes], 32-row x 64-byte boxes, no swizzle
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return cudaErrorInvalidValue;
+        cuuint64_t dims[2] = {D_QK, (cuuint64_t)p.num_blocks * TOK};
+        cuuint64_t strides[1] = {D_QK};
+        cuuint32_t box[2] = {64, HALF};
+        cuuint32_t estr[2] = {1, 1};
+        if (fn(&mkv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(p.codes), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        cudaError_t e = cudaFuncSetAttribute(
+            decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(decode_tc_kernel<true>, grid, dim3(NTHREADS_FP8), SMEM_TOTAL, stream,
+                          mkv, p);
+    }
     if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, HALF))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * clusters);
-    return launch_pdl(decode_tc_kernel, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mkv, p);
+    return launch_pdl(decode_tc_kernel<false>, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mkv, p);
 }
 
 }  // namespace mla

@@ -40,7 +40,9 @@ cudaError_t launch_qrope_finalize(const float *part, int S, int B, int H, const 
 struct DecodeParams {
     const uint16_t *q_lat;     // [B][H][512]
     const uint16_t *q_rope;    // [B][H][64]
-    const uint16_t *cache;     // [num_blocks][64][576]
+    const uint16_t *cache;     // [num_blocks][64][576] bf16 (when codes is null)
+    const uint8_t *codes;      // FP8 cache: e4m3 codes [num_blocks][64][576], or null
+    const int8_t *exps;        // FP8 cache: row exponents [num_blocks][64] (scale 2^e)
     const int32_t *block_table;
     const int32_t *seqlens;
     int num_blocks, max_blocks, B, H;  // H = query rows per sequence (s_q x hq)
@@ -151,6 +153,16 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, in
                            uint16_t *out, float *out_f32, float *lse, cudaStream_t stream);
 
 int device_sm_count();
+
+// FP8 (e4m3) cache rows of 576 values, one power-of-two scale per row.
+cudaError_t launch_quantize_rows(const uint16_t *src, long rows, uint8_t *codes, int8_t *exps,
+                                 cudaStream_t stream);
+cudaError_t launch_dequantize_rows(const uint8_t *codes, const int8_t *exps, long rows,
+                                   uint16_t *dst, cudaStream_t stream);
+cudaError_t launch_append_finalize_fp8(const float *part, int S, int B, const int32_t *pos,
+                                       const int32_t *block_table, int max_blocks,
+                                       uint8_t *codes, int8_t *exps, int num_blocks,
+                                       float theta, uint32_t *err, cudaStream_t stream);
 
 // Host-side argument checks of a decode call (all but the workspace): MLA_OK or the
 // status the entry point returns. Launches nothing.

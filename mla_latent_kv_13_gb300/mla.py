@@ -56,6 +56,11 @@ _SIGS = {
     "mla_decode_attention_partial": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
                                       _sz, _vp, _vp, _vp], _i),
     "mla_decode_combine_ranks": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
+    "mla_quantize_kv_fp8": ([_vp, ctypes.c_long, _vp, _vp, _vp], _i),
+    "mla_dequantize_kv_fp8": ([_vp, _vp, ctypes.c_long, _vp, _vp], _i),
+    "mla_append_kv_fp8": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _f, _vp, _sz, _vp], _i),
+    "mla_decode_attention_fp8": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
+                                  _sz, _vp, _vp, _vp], _i),
     "mla_decode_mq_workspace_size": ([_i, _i, _i, _i, _i, _szp], _i),
     "mla_decode_attention_mq": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _f, _i, _vp,
                                  _sz, _vp, _vp, _vp], _i),
@@ -310,6 +315,72 @@ def decode_combine_ranks(o_parts, lse_parts, out=None, lse=None, stream=None):
                                        _ptr(lse), _stream(stream))
     _ok(rc, "mla_decode_combine_ranks")
     return out, lse
+
+
+def _u8(t):
+    if t.dtype not in (torch.uint8, torch.int8):
+        raise TypeError(f"expected 8-bit storage, got {t.dtype}")
+    return t
+
+
+def quantize_kv_fp8(rows_bf16, codes=None, exps=None, stream=None):
+    """mla_quantize_kv_fp8: bf16 rows [..., 576] -> (codes uint8 [..., 576], exps int8 [...])."""
+    shp = rows_bf16.shape
+    rows = rows_bf16.numel() // D_QK
+    dev = rows_bf16.device
+    if codes is None:
+        codes = torch.empty(shp, dtype=torch.uint8, device=dev)
+    if exps is None:
+        exps = torch.empty(shp[:-1], dtype=torch.int8, device=dev)
+    _ok(_lib.mla_quantize_kv_fp8(_ptr(_bits(rows_bf16)), rows, _ptr(_u8(codes)), _ptr(_u8(exps)),
+                                 _stream(stream)), "mla_quantize_kv_fp8")
+    return codes, exps
+
+
+def dequantize_kv_fp8(codes, exps, out=None, stream=None):
+    """mla_dequantize_kv_fp8: (codes [..., 576], exps [...]) -> bf16 rows [..., 576]."""
+    rows = codes.numel() // D_QK
+    if out is None:
+        out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+    _ok(_lib.mla_dequantize_kv_fp8(_ptr(_u8(codes)), _ptr(_u8(exps)), rows, _ptr(_bits(out)),
+                                   _stream(stream)), "mla_dequantize_kv_fp8")
+    return out
+
+
+def append_kv_fp8(h, w_dkr, pos, block_table, kv_codes, kv_exps, rope_theta=10000.0,
+                  workspace=None, stream=None):
+    B, dm = h.shape
+    nb = kv_codes.shape[0]
+    if workspace is None:
+        workspace = alloc_workspace(append_kv_workspace_size(B, dm), stream=stream)
+    rc = _lib.mla_append_kv_fp8(_ptr(_bits(h)), B, dm, _ptr(_bits(w_dkr)), _ptr(pos),
+                                _ptr(block_table), block_table.shape[1], _ptr(_u8(kv_codes)),
+                                _ptr(_u8(kv_exps)), nb, float(rope_theta), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _ok(rc, "mla_append_kv_fp8")
+    return workspace
+
+
+def decode_attention_fp8(q_lat, q_rope, kv_codes, kv_exps, block_table, seqlens, max_seqlen,
+                         scale, num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """mla_decode_attention_fp8. Returns (out [B,H,512] bf16, lse [B,H] fp32, workspace)."""
+    B, H, _ = q_lat.shape
+    dev = q_lat.device
+    if out is None:
+        out = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(decode_workspace_size(B, H, max_seqlen, num_splits),
+                                    stream=stream)
+    rc = _lib.mla_decode_attention_fp8(_ptr(_bits(q_lat)), _ptr(_bits(q_rope)),
+                                       _ptr(_u8(kv_codes)), _ptr(_u8(kv_exps)), kv_codes.shape[0],
+                                       _ptr(block_table), block_table.shape[1], _ptr(seqlens), B,
+                                       H, int(max_seqlen), float(scale), int(num_splits),
+                                       _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                                       _stream(stream))
+    _ok(rc, "mla_decode_attention_fp8")
+    return out, lse, workspace
 
 
 def absorb_q(h, w_dq, w_uq, w_qr, w_uk, pos, rope_theta=10000.0, q_lat=None, q_rope=None,

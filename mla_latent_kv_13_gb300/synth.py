@@ -201,12 +201,14 @@ def make_step_inputs(w: Workload, seed: int = 0, prefilled: int | None = None):
     return d
 
 
-def algorithmic_attention_bytes(seqlens, H: int) -> int:
+def algorithmic_attention_bytes(seqlens, H: int, kv_bytes_per_value: int = 2) -> int:
     """Bytes a decode-attention pass must move at least once: the latent cache rows
-    of every valid token (576 bf16), q (576 bf16/head), out (512 bf16/head), lse (fp32/head)."""
+    of every valid token (576 values: bf16, or e4m3 codes plus one exponent byte),
+    q (576 bf16/head), out (512 bf16/head), lse (fp32/head)."""
     N = int(np.sum(seqlens))
     B = len(seqlens)
-    return N * D_QK * 2 + B * H * (D_QK * 2 + D_C * 2 + 4)
+    row = D_QK * 2 if kv_bytes_per_value == 2 else D_QK + 1
+    return N * row + B * H * (D_QK * 2 + D_C * 2 + 4)
 
 
 def attention_flops(seqlens, H: int) -> int:
