@@ -45,7 +45,7 @@ def test_append_exact_on_integer_inputs(mla):
 
 
 @pytest.mark.parametrize("B,dm", [(5, 256), (128, 7168)])
-def test_append_real_inputs_within_one_ulp(mla, B, dm):
+def test_append_real_inputs_within_fp32_summation_bound(mla, B, dm):
     rng = np.random.default_rng(1)
     h = bf16(rng.standard_normal((B, dm)))
     w = bf16(rng.standard_normal((576, dm)) * 0.02)
@@ -57,8 +57,26 @@ def test_append_real_inputs_within_one_ulp(mla, B, dm):
     assert st == 0
     diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
     # bf16 bit patterns of same-sign values differ by the number of ulps between them
-    assert diff.max() <= 1
     assert (diff > 0).mean() < 0.01
+    # The kernel sums the d_model products in fp32, in an order it does not fix; any order
+    # is within dm * 2^-24 * sum |h_k w_k| of the exact sum (the standard bound for
+    # recursive summation), and RoPE mixes each rotated pair with |cos|, |sin| <= 1. So the
+    # stored bf16 value and the oracle's rounding of the exact value differ by at most one
+    # bf16 ulp plus that bound.
+    hf, wf = synth.bf16_bits_to_f64(h), synth.bf16_bits_to_f64(w)
+    x = hf @ wf.T
+    gam = dm * 2.0 ** -24 * (np.abs(hf) @ np.abs(wf).T)
+    pair = gam[:, 512::2] + gam[:, 513::2] + 2.0 ** -21 * (np.abs(x[:, 512::2]) + np.abs(x[:, 513::2]))
+    gam[:, 512::2] = pair
+    gam[:, 513::2] = pair
+    blk, slot = bt[np.arange(B), pos // 64], pos % 64
+    g = synth.bf16_bits_to_f64(got[blk, slot])
+    r = synth.bf16_bits_to_f64(ref[blk, slot])
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.maximum(np.abs(g), np.abs(r)), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(g - r) <= ulp + gam)
+    mask = np.ones(got.shape[:2], dtype=bool)
+    mask[blk, slot] = False
+    assert np.array_equal(got[mask], ref[mask])  # nothing else written
 
 
 def test_append_out_of_range_is_flagged_and_dropped(mla):
