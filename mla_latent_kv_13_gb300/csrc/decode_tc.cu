@@ -22,14 +22,15 @@
 // reference is only raised when a score exceeds it by more than 2^8) and run P . V over
 // all 64 tokens for their own columns.
 //
-// Tensor memory (512 columns): O fp32 [0, 256), S fp32 in two buffers [256, 320) (the
-// scores of the next tile are computed while the softmax still works on this one), Q bf16
-// pairs of column chunks 0..5 [320, 512). Q chunks 6, 7 (c_kv[384:512]) and 8 (k_rope) are
-// read from shared memory. The chunks of a tile sit in three rings sized by how long they
-// are held: the own tokens' own output columns (both products, 4 slots), the own tokens'
-// other columns and k_rope (scores only, 2 slots) and the peer tokens' own output columns
-// (P . V only, loaded late, 2 slots). P halves are double-buffered: the local half is the
-// A operand of P . V for the own tokens, the received half for the peer's.
+// Tensor memory (512 columns): O fp32 [0, 256), then S fp32 (one 32-column buffer, or two
+// for at most 64 query rows, so that the scores of the next tile are computed while the
+// softmax still works on this one), then Q as bf16 pairs of as many column chunks as fit
+// (7 or 6); the remaining Q chunks (k_rope last) are read from shared memory. The chunks
+// of a tile sit in three rings sized by how long they are held: the own tokens' own
+// output columns (both products, 4 slots), the own tokens' other columns and k_rope
+// (scores only, 2 slots) and the peer tokens' own output columns (P . V only, loaded late,
+// 3 or 2 slots). P halves are double-buffered: the local half is the A operand of P . V
+// for the own tokens, the received half for the peer's.
 //
 // Roles per CTA (224 threads): warp 0 loads the own tokens' chunks (TMA, one lane);
 // warp 1 allocates TMEM and issues the score MMAs; warp 6 issues P . V and loads the
@@ -61,40 +62,73 @@ constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_r
 //   KV: own tokens x own output columns (4 chunks) -- both products, until P.V
 //   K : own tokens x the other 4 c_kv chunks and k_rope (5 chunks) -- scores only
 //   V : peer tokens x own output columns (4 chunks) -- P.V only, loaded later
-constexpr int NKV = 4, NK = 2, NV = 2;        // slots per ring
+constexpr int NKV = 4, NK = 2;                // slots of the KV and K rings
 constexpr int KV_SLOT = 4 * CH, K_SLOT = 5 * CH, V_SLOT = 4 * CH;
-constexpr int NQT = 6;                        // Q chunks held in TMEM (the rest in smem)
-constexpr int NQS = NOWN - NQT;               // Q chunks in smem (c_kv[384:512), k_rope)
 constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
 constexpr int PGRP = 8 * 64 + 8 * 8;          // 8 rows: their 32 bf16 of P, then (reference, sum)
 constexpr int PBUF = 16 * PGRP;               // P half of 128 rows with its row data (9 KB)
 constexpr int PWARP = 4 * PGRP;               // the 32 rows of one warp (contiguous)
-constexpr int QS_OFF = 0;
-constexpr int KV_OFF = QS_OFF + NQS * QCH;
-constexpr int K_OFF = KV_OFF + NKV * KV_SLOT;
-constexpr int V_OFF = K_OFF + NK * K_SLOT;
-constexpr int SEND_OFF = V_OFF + NV * V_SLOT;  // local P half, x2
-constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
-constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
-constexpr int NBAR = 48;
-constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+constexpr int NBAR = 56;
 // MISC: TMEM address, abort flags, and the counts of remote operations exchanged when a
 // pair stops early (byte offsets below)
 constexpr int MISC_BYTES = 128;
 constexpr int M_TMEM = 0, M_ABORT = 4, M_PEER_ABORT = 8, M_PEER_PV = 12, M_PEER_SENT = 16,
               M_SENT = 32, M_RECV = 48, M_PV = 64;
-// FP8 cache: each ring slot's 64 row exponents (the block's, one int8 per token)
-constexpr int EXP_OFF = MISC_OFF + MISC_BYTES;
-constexpr int EXP_SLOT = 64;
-constexpr int SMEM_USED = EXP_OFF + (NKV + NK + NV) * EXP_SLOT;
-constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
+constexpr int EXP_SLOT = 64;                  // FP8: one slot's 64 row exponents (int8 each)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
+// Q rows staged between segments in the idle rings and local P buffers (from KV_OFF up to
+// the peer's P buffers, which stay untouched): one row (q_lat then q_rope) per 1168
+// bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
+constexpr int QSTG = 2 * (D_C + D_ROPE) + 16;
+
+// Two layouts of shared and tensor memory. TMEM holds O (256 columns), the scores S (32
+// columns per buffer) and as many Q chunks as fit (32 columns each, bf16 pairs); the other
+// Q chunks are A operands in shared memory, which cost the tensor pipe more per score MMA.
+//   DS = true : two S buffers, so the next tile's scores are computed while the softmax
+//               still reads this one; Q chunks 0..5 in TMEM, 6..8 in smem; V ring 2 slots.
+//   DS = false: one S buffer; Q chunks 0..6 in TMEM, 7..8 in smem; V ring 3 slots.
+// Measured (B = 128 x 8192 tokens at 128 heads; 32 x 32768 at 64): the double buffer
+// takes the 64-row case from 271 to 257 us, but the 128-row case from 292 to 305 us, where
+// the tensor pipe's time per tile (the extra shared-memory operand) sets the period. The
+// host takes DS for at most 64 query rows.
+template <bool DS> struct Layout {
+    static constexpr int NSB = DS ? 2 : 1;    // S buffers
+    static constexpr int NV = DS ? 2 : 3;     // slots of the V ring
+    static constexpr int NQT = DS ? 6 : 7;    // Q chunks held in TMEM (the rest in smem)
+    static constexpr int NQS = NOWN - NQT;    // Q chunks in smem (the last ones, k_rope last)
+    static constexpr int QS_OFF = 0;
+    static constexpr int KV_OFF = QS_OFF + NQS * QCH;
+    static constexpr int K_OFF = KV_OFF + NKV * KV_SLOT;
+    static constexpr int V_OFF = K_OFF + NK * K_SLOT;
+    static constexpr int SEND_OFF = V_OFF + NV * V_SLOT;  // local P half, x2
+    static constexpr int RECV_OFF = SEND_OFF + 2 * PBUF;  // peer's P half, x2
+    static constexpr int BAR_OFF = RECV_OFF + 2 * PBUF;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr int EXP_OFF = MISC_OFF + MISC_BYTES;  // FP8: exponents of every slot
+    static constexpr int SMEM_USED = EXP_OFF + (NKV + NK + NV) * EXP_SLOT;
+    static constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack to align the base to 1024 B
+    static constexpr uint32_t TM_S = 256;                // S buffers: fp32 columns
+    static constexpr uint32_t TM_Q = TM_S + 32 * NSB;    // Q chunks 0..NQT-1: bf16 pairs
+
+    static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+    static_assert(QS_OFF % 1024 == 0 && KV_OFF % 1024 == 0 && K_OFF % 1024 == 0 &&
+                      V_OFF % 1024 == 0 && CH % 1024 == 0,
+                  "128-byte-swizzled operands need 1024-byte-aligned atoms");
+    static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
+    static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
+    static_assert(3 * (NKV + NK + NV) + 23 <= NBAR, "mbarrier count");
+    static_assert(EXP_OFF % 16 == 0, "bulk copies of the row exponents");
+    static_assert(KV_OFF + 128 * QSTG <= RECV_OFF && QSTG % 16 == 0, "Q staging area");
+    static_assert(QS_OFF + NQS * QCH <= KV_OFF, "staged Q rows never overlap the Q chunks in smem");
+    static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
+};
+constexpr int SMEM_TOTAL = Layout<false>::SMEM_TOTAL > Layout<true>::SMEM_TOTAL
+                               ? Layout<false>::SMEM_TOTAL
+                               : Layout<true>::SMEM_TOTAL;  // the larger, for occupancy
 
 constexpr int NTHREADS = 224;                 // 7 warps
 constexpr int NTHREADS_FP8 = 320;             // + 3 warps widening the FP8 tiles
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0;                  // O: fp32 columns [0, 256)
-constexpr uint32_t TM_S = 256;                // S, two buffers: fp32 columns [256, 320)
-constexpr uint32_t TM_Q = 320;                // Q chunks 0..5: bf16 pairs, [320, 512)
 constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
@@ -104,21 +138,6 @@ constexpr uint32_t XBYTES = PWARP;            // one warp's message: P rows + (r
 constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
-static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(QS_OFF % 1024 == 0 && KV_OFF % 1024 == 0 && K_OFF % 1024 == 0 &&
-                  V_OFF % 1024 == 0 && CH % 1024 == 0,
-              "128-byte-swizzled operands need 1024-byte-aligned atoms");
-static_assert(SEND_OFF % 16 == 0 && RECV_OFF % 16 == 0 && PGRP % 16 == 0, "16-byte stores");
-static_assert(BAR_OFF % 8 == 0, "mbarrier alignment");
-static_assert(3 * (NKV + NK + NV) + 23 <= NBAR, "mbarrier count");
-static_assert(EXP_OFF % 16 == 0, "bulk copies of the row exponents");
-// Q rows staged between segments in the idle rings and local P buffers (from KV_OFF up to
-// the peer's P buffers, which stay untouched): one row (q_lat then q_rope) per 1168
-// bytes, so that the 8 lanes of a 16-byte shared-memory access hit 8 bank groups
-constexpr int QSTG = 2 * (D_C + D_ROPE) + 16;
-static_assert(KV_OFF + 128 * QSTG <= RECV_OFF && QSTG % 16 == 0, "Q staging area");
-static_assert(QS_OFF + NQS * QCH <= KV_OFF, "staged Q rows never overlap the Q chunks in smem");
-static_assert(TM_Q + 32 * NQT == TMEM_COLS, "tensor-memory budget");
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -158,9 +177,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // more warps (one per ring) widen the chunks in place to bf16 code * 2^e -- exact, since
 // such a value has at most four significant bits -- and release the slot to the products
 // on a second barrier. Everything downstream is the bf16 path, unchanged.
-template <bool FP8>
+template <bool FP8, bool DS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 : NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv, DecodeParams p) {
+    using LY = Layout<DS>;
+    constexpr int NSB = LY::NSB, NV = LY::NV, NQT = LY::NQT;
+    constexpr int QS_OFF = LY::QS_OFF, KV_OFF = LY::KV_OFF, K_OFF = LY::K_OFF,
+                  V_OFF = LY::V_OFF, SEND_OFF = LY::SEND_OFF, RECV_OFF = LY::RECV_OFF,
+                  BAR_OFF = LY::BAR_OFF, MISC_OFF = LY::MISC_OFF, EXP_OFF = LY::EXP_OFF;
+    constexpr uint32_t TM_S = LY::TM_S, TM_Q = LY::TM_Q;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -491,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
             auto issue_s = [&](int i) {
                 const uint32_t kv = sb + KV_OFF + (i % NKV) * KV_SLOT;
                 const uint32_t ko = sb + K_OFF + (i % NK) * K_SLOT;
-                const uint32_t sd = tmem + TM_S + 32u * (i & 1);
+                const uint32_t sd = tmem + TM_S + 32u * (i % NSB);
 #pragma unroll
                 for (int d = 0; d < NOWN; ++d)
 #pragma unroll
@@ -511,17 +536,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
                                       sdesc_sw128(qs + (d - NQT) * QCH + kk * 32, 16, 1024), bdesc,
                                       IDESC_S, 1);
                     }
-                tc_commit_if(leader, s_full(i & 1));
+                tc_commit_if(leader, s_full(i % NSB));
                 tc_commit_if(leader, k_empty(i % NK));
             };
             // scores of tile k need its cache chunks and their S buffer back from the
-            // softmax (s_free of tile k-2): with two buffers the scores of the next tile
-            // are computed while the softmax still works on this one
+            // softmax (s_free of tile k - NSB): with two buffers the scores of the next
+            // tile are computed while the softmax still works on this one
             bool ok = wait_all(q_ready, 0);
             for (int k = 0; ok && k < n; ++k) {
                 if (!(ok = wait_all(kv_ready(k % NKV), (k / NKV) & 1))) break;
                 if (!(ok = wait_all(k_ready(k % NK), (k / NK) & 1))) break;
-                if (k > 1 && !(ok = wait_all(s_free(k & 1), ((k - 2) >> 1) & 1))) break;
+                if (k >= NSB && !(ok = wait_all(s_free(k % NSB), (k / NSB - 1) & 1))) break;
                 tc_fence_after();
                 issue_s(k);
                 __syncwarp();
@@ -705,14 +730,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
             const uint32_t vs = sb + V_OFF + (i % NV) * V_SLOT;
 
             // ---- scores of this CTA's 32 tokens, out of TMEM (releasing S)
-            if (!(ok = wait_w(s_full(x), (i >> 1) & 1))) break;
+            if (!(ok = wait_w(s_full(i % NSB), (i / NSB) & 1))) break;
             tc_fence_after();
             uint32_t sr[32];
-            tmem_ld32(tl + TM_S + 32u * x, sr);
+            tmem_ld32(tl + TM_S + 32u * (i % NSB), sr);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(x));
+            if (lane == 0) mbar_arrive(s_free(i % NSB));
 
             const bool blk_ok = blk >= 0 && blk < p.num_blocks;
             const int tvalid = blk_ok ? min(TOK, L - tile * TOK) : 0;  // valid tokens of the tile
@@ -1079,6 +1104,20 @@ bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t ro
 
 }  // namespace
 
+namespace {
+// Two S buffers for at most 64 query rows, one above (the layouts' comment gives why).
+template <bool FP8, bool DS>
+cudaError_t launch_variant(const CUtensorMap &mkv, const DecodeParams &p, dim3 grid,
+                           cudaStream_t stream) {
+    constexpr int smem = Layout<DS>::SMEM_TOTAL;
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<FP8, DS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_tc_kernel<FP8, DS>, grid, dim3(FP8 ? NTHREADS_FP8 : NTHREADS), smem,
+                      stream, mkv, p);
+}
+}  // namespace
+
 int decode_tc_cluster_slots() {
     static int slots = 0;
     if (slots > 0) return slots;
@@ -1094,9 +1133,10 @@ int decode_tc_cluster_slots() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaFuncSetAttribute(decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_TOTAL) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) == cudaSuccess && n > 0)
+    if (cudaFuncSetAttribute(decode_tc_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false, false>, &cfg) == cudaSuccess &&
+        n > 0)
         slots = n;
     else
         slots = device_sm_count() / 2;
@@ -1118,18 +1158,13 @@ cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t s
                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        cudaError_t e = cudaFuncSetAttribute(
-            decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(decode_tc_kernel<true>, grid, dim3(NTHREADS_FP8), SMEM_TOTAL, stream,
-                          mkv, p);
+        return p.H <= 64 ? launch_variant<true, true>(mkv, p, grid, stream)
+                         : launch_variant<true, false>(mkv, p, grid, stream);
     }
     if (!encode_bf16_2d(&mkv, p.cache, D_QK, (uint64_t)p.num_blocks * TOK, HALF))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(decode_tc_kernel<false>, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mkv, p);
+    return p.H <= 64 ? launch_variant<false, true>(mkv, p, grid, stream)
+                     : launch_variant<false, false>(mkv, p, grid, stream);
 }
 
 }  // namespace mla
