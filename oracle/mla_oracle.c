@@ -252,6 +252,8 @@ void mla_oracle_quantize_row_fp8(const double *x, int D, uint8_t *codes, int8_t 
             ++e;
         while (ldexp(mx, -(e - 1)) <= 448.0)
             --e;
+        if (e < -126) /* the stored scale 2^-e stays a normal float: rows below 2^-117 */
+            e = -126;
     }
     for (int n = 0; n < D; ++n)
         codes[n] = mla_oracle_f64_to_e4m3(ldexp(x[n], -e));

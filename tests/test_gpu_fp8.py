@@ -48,12 +48,15 @@ def test_quantise_bf16_rows_bit_exact(mla):
     x[4, :] = 0.0
     x[4, 100] = -448.0 * 2.0 ** 5   # max exactly at a power-of-two boundary
     x[5] = np.linspace(-500, 500, 576)  # ties and saturation-free spread
+    x[6] = 0.0
+    x[6, :3] = [2.0 ** -130, -(2.0 ** -131), 3 * 2.0 ** -133]  # subnormal row: e = -126
     bits = synth.f32_to_bf16_bits(x)
     codes, exps = mla.quantize_kv_fp8(dev_bf16(bits))
     torch.cuda.synchronize()
     want_c, want_e = oracle.quantize_rows_fp8(synth.bf16_bits_to_f64(bits))
     assert np.array_equal(exps.cpu().numpy(), want_e)
     assert np.array_equal(codes.cpu().numpy(), want_c)
+    assert want_e[6] == -126
 
 
 def test_append_kv_fp8_integer_inputs_bit_exact_and_real_inputs_close(mla):

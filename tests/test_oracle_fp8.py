@@ -102,6 +102,25 @@ def test_row_scale_is_the_smallest_power_of_two():
     assert exps[8] == -3
 
 
+def test_row_scale_exponent_floor_for_tiny_rows():
+    """The exponent is kept at or above -126 (its scale 2^-e a normal float), so a row whose
+    largest value is below 448 * 2^-126 is quantised with e = -126: its codes are those of
+    the values times 2^126, which e4m3 still represents or flushes by its own rounding."""
+    rows = np.zeros((3, 576))
+    rows[0, :4] = [2.0 ** -130, -2.0 ** -131, 3 * 2.0 ** -133, 2.0 ** -140]
+    rows[1, 0] = 448.0 * 2.0 ** -126   # exactly at the floor: e = -126 either way
+    rows[2, 0] = 448.0 * 2.0 ** -125
+    codes, exps = oracle.quantize_rows_fp8(rows)
+    assert list(exps) == [-126, -126, -125]
+    assert codes[0, 0] == oracle.f64_to_e4m3(2.0 ** -4)
+    assert codes[0, 1] == oracle.f64_to_e4m3(-(2.0 ** -5))
+    assert codes[0, 2] == oracle.f64_to_e4m3(3 * 2.0 ** -7)
+    assert codes[0, 3] == 0  # 2^-14 is below half the smallest subnormal (2^-9)
+    deq = oracle.dequantize_fp8(codes, exps)
+    assert deq[0, 0] == 2.0 ** -130 and deq[0, 2] == 3 * 2.0 ** -133
+    assert deq[1, 0] == rows[1, 0] and deq[2, 0] == rows[2, 0]
+
+
 def test_dequantised_rows_are_exact_bf16_values():
     rng = np.random.default_rng(2)
     x = rng.normal(0, 1, (64, 576))
