@@ -62,7 +62,6 @@ constexpr int NOWN = 9;                       // own tokens: 8 c_kv chunks + k_r
 //   KV: own tokens x own output columns (4 chunks) -- both products, until P.V
 //   K : own tokens x the other 4 c_kv chunks and k_rope (5 chunks) -- scores only
 //   V : peer tokens x own output columns (4 chunks) -- P.V only, loaded later
-constexpr int NKV = 4, NK = 2;                // slots of the KV and K rings
 constexpr int KV_SLOT = 4 * CH, K_SLOT = 5 * CH, V_SLOT = 4 * CH;
 constexpr int QCH = 128 * 128;                // one Q chunk in smem: 128 rows x 128 B
 constexpr int PGRP = 8 * 64 + 8 * 8;          // 8 rows: their 32 bf16 of P, then (reference, sum)
@@ -94,6 +93,7 @@ constexpr int QSTG = 2 * (D_C + D_ROPE) + 16;
 // host takes DS for at most 64 query rows.
 template <bool DS> struct Layout {
     static constexpr int NSB = DS ? 2 : 1;    // S buffers
+    static constexpr int NKV = 4, NK = 2;     // slots of the KV and K rings
     static constexpr int NV = DS ? 2 : 3;     // slots of the V ring
     static constexpr int NQT = DS ? 6 : 7;    // Q chunks held in TMEM (the rest in smem)
     static constexpr int NQS = NOWN - NQT;    // Q chunks in smem (the last ones, k_rope last)
@@ -181,7 +181,7 @@ template <bool FP8, bool DS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 : NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap map_kv, DecodeParams p) {
     using LY = Layout<DS>;
-    constexpr int NSB = LY::NSB, NV = LY::NV, NQT = LY::NQT;
+    constexpr int NSB = LY::NSB, NKV = LY::NKV, NK = LY::NK, NV = LY::NV, NQT = LY::NQT;
     constexpr int QS_OFF = LY::QS_OFF, KV_OFF = LY::KV_OFF, K_OFF = LY::K_OFF,
                   V_OFF = LY::V_OFF, SEND_OFF = LY::SEND_OFF, RECV_OFF = LY::RECV_OFF,
                   BAR_OFF = LY::BAR_OFF, MISC_OFF = LY::MISC_OFF, EXP_OFF = LY::EXP_OFF;
