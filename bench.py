@@ -412,10 +412,13 @@ def run_gpu(args, d, costs, metric, unit):
     h2d = h_host.numel() * 2 + pos_host.numel() * 4 + L_host.numel() * 4
     d2h = y_host.numel() * 2
 
-    # ---- decode attention alone on the other attention workloads (same process)
+    # ---- decode attention alone on the other attention workloads (same process), a
+    # fixed number of launches each: a few tens of milliseconds per workload, whatever the
+    # step count (after a long step run the part sits at its power cap, and thousands of
+    # further launches per workload would time that rather than the kernel)
     configs = None
     if rank == 0 and not args.no_configs:
-        configs = time_attention_configs(cache, dev, max(args.steps, 50), args.num_splits)
+        configs = time_attention_configs(cache, dev, CONFIG_LAUNCHES, args.num_splits)
 
     if rank != 0:
         return
@@ -621,6 +624,9 @@ def run_gpu_prefill(args):
 
 ATTN_CONFIGS = ("v3", "mixed", "long", "long_fp8")
 ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70, "long_fp8": None}
+
+
+CONFIG_LAUNCHES = 200  # timed launches per attention workload in the `configs` object
 
 
 def time_attention_configs(pool, dev, launches: int, num_splits: int):
