@@ -6,16 +6,21 @@
 // attention runs over the prefix and the chunk: for head h and query i of the chunk
 // (position prefix + i), keys j <= prefix + i,
 //   s_j = scale * (q_nope . k_nope_j + q_rope . k_rope_j),  o = sum_j softmax(s)_j v_j.
-// One CTA per (head, tile of 128 queries): Q [128 x 192] is staged once; K [128 keys x 192]
-// and V [128 keys x 128] tiles stream through two shared-memory stages:
-//   S  = Q . K^T   (M = 128 queries, N = 128 keys, K = 192; A and B from shared memory)
-//   O += P . V     (M = 128, N = 128, K = 128 keys; A = P from TMEM, B = V, MN-major)
-// with the online softmax (exp2 domain, lazy rescale as in decode) between them. S is
-// double-buffered in TMEM, so the scores of tile t+1 are computed while the softmax works
-// on tile t.
-// Roles (192 threads): warp 0 TMA, warp 1 TMEM + MMA issue (converged, one elected lane
-// issues through predicated instructions), warps 2-5 softmax/output (thread = query row =
-// TMEM lane). Every wait is bounded (one second).
+// One CTA per (head, 256 queries), as two tiles of 128 queries (A and B) that share the
+// key/value tiles: Q [2 x 128 x 192] is staged once; K [128 keys x 192] tiles stream through
+// two shared-memory stages and V [128 keys x 128] through one:
+//   S_g  = Q_g . K^T   (M = 128 queries, N = 128 keys, K = 192; A and B from shared memory)
+//   O_g += P_g . V     (M = 128, N = 128, K = 128 keys; A = P from TMEM, B = V, MN-major)
+// with the online softmax (exp2 domain, lazy rescale as in decode) between them. Each tile
+// has its own softmax warpgroup, O and S in TMEM, and P is written over the S columns it came
+// from. The two tiles' products and softmaxes interleave ("ping-pong"): while one group
+// turns its scores into P, the tensor pipe runs the other group's P.V and next scores, so
+// neither the softmax (128 exponentials per row and tile, one warp per SMSP and group) nor
+// the products wait for each other as a single tile does.
+// Roles (320 threads): warp 0 TMA, warp 1 TMEM + MMA issue (converged, one elected lane
+// issues through predicated instructions, whichever product is ready first), warps 2-5
+// softmax/output of tile A and warps 6-9 of tile B (thread = query row = TMEM lane). Every
+// wait is bounded (one second).
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -26,24 +31,25 @@ namespace {
 
 using namespace sm100;
 
-constexpr int QT = 128;                      // queries per CTA
+constexpr int QT = 128;                      // queries per tile; a CTA holds tiles A and B
 constexpr int KT = 128;                      // keys per tile
 constexpr int CH = 128 * 128;                // one 64-column chunk of 128 rows (16 KB)
-constexpr int Q_OFF = 0;                     // q_nope[0:64), q_nope[64:128), q_rope
-constexpr int NSTG = 2;
+constexpr int QCH = 3;                       // q_nope[0:64), q_nope[64:128), q_rope
 constexpr int K_CH = 3;                      // k_nope[0:64), k_nope[64:128), k_rope
 constexpr int V_CH = 2;                      // v[0:64), v[64:128)
-constexpr int STG = (K_CH + V_CH) * CH;      // 80 KB
-constexpr int STG_OFF = Q_OFF + 3 * CH;
-constexpr int BAR_OFF = STG_OFF + NSTG * STG;
+constexpr int NK = 2;                        // K stages (V has one)
+constexpr int Q_OFF = 0;                     // Q of tile A, then of tile B
+constexpr int K_OFF = Q_OFF + 2 * QCH * CH;
+constexpr int V_OFF = K_OFF + NK * K_CH * CH;
+constexpr int BAR_OFF = V_OFF + V_CH * CH;
 constexpr int NBAR = 16;
 constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
 constexpr int SMEM_TOTAL = MISC_OFF + 64 + 1024;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 0;                 // O: fp32 [0, 128)
-constexpr uint32_t TM_S = 128;               // S: fp32 [128, 256) and [256, 384)
-constexpr uint32_t TM_P = 384;               // P: bf16 pairs [384, 448)
+// O of tile g: fp32 [128 g, 128 g + 128); S of tile g: fp32 [256 + 128 g, +128), its P
+// (bf16 pairs) over the first 64 of those columns
+constexpr uint32_t TM_O = 0, TM_S = 256;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr float TAU = 8.0f;
 
@@ -51,12 +57,17 @@ constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
 
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
-static_assert(STG_OFF % 1024 == 0 && STG % 1024 == 0, "swizzle atoms");
+static_assert(K_OFF % 1024 == 0 && V_OFF % 1024 == 0 && CH % 1024 == 0, "swizzle atoms");
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     uint64_t t0 = globaltimer_ns();
     while (!mbar_test(bar, parity))
         if (globaltimer_ns() - t0 > 200000000ull) return;
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
 }
 
 struct PrefillArgs {
@@ -78,35 +89,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y;
-    const int i0 = blockIdx.x * QT;
-    // keys the tile's last query sees: [0, prefix + min(i0 + 127, C - 1)]
-    const int last_key = a.prefix + min(i0 + QT - 1, a.C - 1);
-    const int nkt = last_key / KT + 1;
+    const int i0 = blockIdx.x * (2 * QT);
+    // key tiles seen by query tile g: through the key of its last live query (none when
+    // the tile holds no live query)
+    auto tiles_of = [&](int g) {
+        const int first = i0 + g * QT;
+        return first >= a.C ? 0 : (a.prefix + min(first + QT - 1, a.C - 1)) / KT + 1;
+    };
+    const int ntile[2] = {tiles_of(0), tiles_of(1)};
+    const int nk = max(ntile[0], ntile[1]);
 
     const uint32_t bar = sb + BAR_OFF;
-    auto kv_full = [&](int s) { return bar + 8u * s; };
-    auto kv_empty = [&](int s) { return bar + 8u * (NSTG + s); };
-    const uint32_t q_full = bar + 8u * (2 * NSTG);
-    const uint32_t p_full = q_full + 8, pv_done = q_full + 16, mma_drain = q_full + 24;
-    // S buffer x (tiles t with t % 2 == x): computed / read out by the softmax
-    auto s_full = [&](int x) { return q_full + 32 + 8u * x; };
-    auto s_free = [&](int x) { return q_full + 48 + 8u * x; };
+    auto k_full = [&](int s) { return bar + 8u * s; };
+    auto k_empty = [&](int s) { return bar + 8u * (NK + s); };
+    const uint32_t v_full = bar + 8u * (2 * NK), v_empty = v_full + 8;
+    const uint32_t q_full = v_full + 16, mma_drain = v_full + 24;
+    auto s_full = [&](int g) { return v_full + 32 + 8u * g; };   // S_g(t) computed
+    auto p_full = [&](int g) { return v_full + 48 + 8u * g; };   // P_g(t) in TMEM (4 warps)
+    auto pv_done = [&](int g) { return v_full + 64 + 8u * g; };  // O_g += P_g(t) V(t) done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
 
     if (tid == 0) {
-        for (int s = 0; s < NSTG; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
         }
+        mbar_init(v_full, 1);
+        mbar_init(v_empty, 1);
         mbar_init(q_full, 1);
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full(x), 1);
-            mbar_init(s_free(x), 4);
-        }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
         mbar_init(mma_drain, 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full(g), 1);
+            mbar_init(p_full(g), 4);
+            mbar_init(pv_done(g), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -128,179 +145,219 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // K(0), K(1), V(0), then K(t + 1) before V(t): K(t + 1) frees with the scores of
+        // tile t - 1, V(t) only with the products P.V of tile t - 1, which come later
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, 3 * CH);
-            tma_load_3d(sb + Q_OFF, &m_qn, q_full, 0, h, i0);
-            tma_load_3d(sb + Q_OFF + CH, &m_qn, q_full, 64, h, i0);
-            tma_load_3d(sb + Q_OFF + 2 * CH, &m_qr, q_full, 0, h, i0);
-            int issued = 0;
-            for (int t = 0; t < nkt; ++t) {
-                const int s = t % NSTG;
-                if (!mbar_wait(kv_empty(s), ((t / NSTG) & 1) ^ 1, abort_flag, WAIT_NS)) break;
-                const uint32_t st = sb + STG_OFF + s * STG;
+            mbar_arrive_expect_tx(q_full, 2 * QCH * CH);
+            for (int g = 0; g < 2; ++g) {
+                const uint32_t q = sb + Q_OFF + g * QCH * CH;
+                tma_load_3d(q, &m_qn, q_full, 0, h, i0 + g * QT);
+                tma_load_3d(q + CH, &m_qn, q_full, 64, h, i0 + g * QT);
+                tma_load_3d(q + 2 * CH, &m_qr, q_full, 0, h, i0 + g * QT);
+            }
+            auto load_k = [&](int t) {
+                const int s = t % NK;
+                if (!mbar_wait(k_empty(s), ((t / NK) & 1) ^ 1, abort_flag, WAIT_NS)) return false;
+                const uint32_t st = sb + K_OFF + s * K_CH * CH;
                 const int j0 = t * KT;
-                mbar_arrive_expect_tx(kv_full(s), STG);
-                tma_load_3d(st, &m_kn, kv_full(s), 0, h, j0);
-                tma_load_3d(st + CH, &m_kn, kv_full(s), 64, h, j0);
-                tma_load_2d(st + 2 * CH, &m_kr, kv_full(s), 0, j0);
-                tma_load_3d(st + 3 * CH, &m_v, kv_full(s), 0, h, j0);
-                tma_load_3d(st + 4 * CH, &m_v, kv_full(s), 64, h, j0);
-                issued = t + 1;
+                mbar_arrive_expect_tx(k_full(s), K_CH * CH);
+                tma_load_3d(st, &m_kn, k_full(s), 0, h, j0);
+                tma_load_3d(st + CH, &m_kn, k_full(s), 64, h, j0);
+                tma_load_2d(st + 2 * CH, &m_kr, k_full(s), 0, j0);
+                return true;
+            };
+            auto load_v = [&](int t) {
+                if (!mbar_wait(v_empty, (t & 1) ^ 1, abort_flag, WAIT_NS)) return false;
+                const int j0 = t * KT;
+                mbar_arrive_expect_tx(v_full, V_CH * CH);
+                tma_load_3d(sb + V_OFF, &m_v, v_full, 0, h, j0);
+                tma_load_3d(sb + V_OFF + CH, &m_v, v_full, 64, h, j0);
+                return true;
+            };
+            int ik = 0, iv = 0;  // tiles whose K / V loads were issued
+            bool ok = true;
+            for (int t = 0; ok && t < min(nk, NK); ++t)
+                if ((ok = load_k(t))) ik = t + 1;
+            if (ok && nk > 0 && (ok = load_v(0))) iv = 1;
+            for (int t = 1; ok && t < nk; ++t) {
+                if (t + 1 < nk) {
+                    if (!(ok = load_k(t + 1))) break;
+                    ik = t + 2;
+                }
+                if ((ok = load_v(t))) iv = t + 1;
             }
             drain(q_full, 0);
-            for (int t = max(0, issued - NSTG); t < issued; ++t) drain(kv_full(t % NSTG), (t / NSTG) & 1);
+            for (int t = max(0, ik - NK); t < ik; ++t) drain(k_full(t % NK), (t / NK) & 1);
+            if (iv > 0) drain(v_full, (iv - 1) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA
-        // The whole warp runs the issue loop (decisions from lane 0's view of the barriers,
-        // non-suspending polls) and one elected lane issues through predicated
-        // instructions: a tcgen05.mma issued by a lone lane of a diverged warp costs that
-        // thread more than the tensor pipe's own time per instruction.
-        {
-            const bool leader = elect_one();
-            auto lane0 = [&](bool v) { return __shfl_sync(0xffffffffu, v, 0); };
-            bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, WAIT_NS));
-            if (ok) tc_fence_after();
-            int s_next = 0, pv_next = 0;
-            uint64_t t_idle = 0;  // start of the current idle stretch (0: progress since)
-            uint32_t spins = 0;
-            while (ok && pv_next < nkt) {
-                // S(t) into buffer t % 2 once the softmax has read tile t-2 out of it
-                if (lane0(s_next < nkt && mbar_poll(kv_full(s_next % NSTG), (s_next / NSTG) & 1) &&
-                          (s_next < 2 || mbar_poll(s_free(s_next & 1), ((s_next >> 1) - 1) & 1)))) {
+        // Per tile g, in order: S_g(0), P_g(0).V(0), S_g(1), ...; S_g(t + 1) overwrites the
+        // columns P_g(t) sits in, so it waits for P_g(t).V(t). The two tiles' streams are
+        // issued in whatever order their inputs become ready. A key or value tile is
+        // released by the commit after the last product that reads it (the second tile to
+        // use it, or the only one).
+        const bool leader = elect_one();
+        auto lane0 = [&](bool v) { return __shfl_sync(0xffffffffu, v, 0); };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, abort_flag, WAIT_NS));
+        if (ok) tc_fence_after();
+        int ns[2] = {0, 0}, np[2] = {0, 0};  // next S tile, next P.V tile, per query tile
+        uint64_t t_idle = 0;
+        uint32_t spins = 0;
+        while (ok && (np[0] < ntile[0] || np[1] < ntile[1])) {
+            bool progress = false;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int o = g ^ 1;
+                // P_g(t) . V(t)
+                const int tp = np[g];
+                if (tp < ns[g] &&
+                    lane0(mbar_poll(p_full(g), tp & 1) && mbar_poll(v_full, tp & 1))) {
                     tc_fence_after();
-                    const uint32_t st = sb + STG_OFF + (s_next % NSTG) * STG;
-                    const uint32_t ts = tmem + TM_S + 128 * (s_next & 1);
+#pragma unroll
+                    for (int kk = 0; kk < KT / 16; ++kk)
+                        tc_mma_ts_if(leader, tmem + TM_O + 128 * g, tmem + TM_S + 128 * g + 8 * kk,
+                                     sdesc_sw128(sb + V_OFF + kk * 2048, CH, 1024), IDESC_PV,
+                                     (tp > 0 || kk > 0));
+                    tc_commit_if(leader, pv_done(g));
+                    if (np[o] > tp || tp >= ntile[o]) tc_commit_if(leader, v_empty);
+                    __syncwarp();
+                    ++np[g];
+                    progress = true;
+                }
+                // S_g(t): its key tile loaded, its columns free (P_g(t - 1) . V(t - 1) done)
+                const int ts = ns[g];
+                if (ts < ntile[g] && ts == np[g] &&
+                    lane0(mbar_poll(k_full(ts % NK), (ts / NK) & 1) &&
+                          (ts == 0 || mbar_poll(pv_done(g), (ts - 1) & 1)))) {
+                    tc_fence_after();
+                    const uint32_t q = sb + Q_OFF + g * QCH * CH;
+                    const uint32_t st = sb + K_OFF + (ts % NK) * K_CH * CH;
 #pragma unroll
                     for (int c = 0; c < K_CH; ++c)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_if(leader, ts, sdesc_sw128(sb + Q_OFF + c * CH + kk * 32, 16, 1024),
+                            tc_mma_if(leader, tmem + TM_S + 128 * g,
+                                      sdesc_sw128(q + c * CH + kk * 32, 16, 1024),
                                       sdesc_sw128(st + c * CH + kk * 32, 16, 1024), IDESC_S,
                                       (c | kk) != 0);
-                    tc_commit_if(leader, s_full(s_next & 1));
+                    tc_commit_if(leader, s_full(g));
+                    if (ns[o] > ts || ts >= ntile[o]) tc_commit_if(leader, k_empty(ts % NK));
                     __syncwarp();
-                    ++s_next;
-                    t_idle = 0;
-                    continue;
-                }
-                if (lane0(pv_next < s_next && mbar_poll(p_full, pv_next & 1))) {
-                    tc_fence_after();
-                    const uint32_t vt = sb + STG_OFF + (pv_next % NSTG) * STG + 3 * CH;
-#pragma unroll
-                    for (int kk = 0; kk < KT / 16; ++kk)
-                        tc_mma_ts_if(leader, tmem + TM_O, tmem + TM_P + 8 * kk,
-                                     sdesc_sw128(vt + kk * 2048, CH, 1024), IDESC_PV,
-                                     (pv_next > 0 || kk > 0));
-                    tc_commit_if(leader, kv_empty(pv_next % NSTG));
-                    tc_commit_if(leader, pv_done);
-                    __syncwarp();
-                    ++pv_next;
-                    t_idle = 0;
-                    continue;
-                }
-                if ((++spins & 63) == 0) {
-                    const uint64_t now = globaltimer_ns();
-                    if (t_idle == 0) t_idle = now;
-                    bool stop = *abort_flag != 0;
-                    if (!stop && now - t_idle > WAIT_NS) {
-                        if (lane == 0) *abort_flag = 1;
-                        stop = true;
-                    }
-                    ok = !lane0(stop);
+                    ++ns[g];
+                    progress = true;
                 }
             }
-            if (leader) {
-                tc_commit(mma_drain);
-                drain(mma_drain, 0);
+            if (progress) {
+                t_idle = 0;
+                continue;
             }
+            if ((++spins & 63) == 0) {
+                const uint64_t now = globaltimer_ns();
+                if (t_idle == 0) t_idle = now;
+                bool stop = *abort_flag != 0;
+                if (!stop && now - t_idle > WAIT_NS) {
+                    if (lane == 0) *abort_flag = 1;
+                    stop = true;
+                }
+                ok = !lane0(stop);
+            }
+        }
+        if (leader) {
+            tc_commit(mma_drain);
+            drain(mma_drain, 0);
         }
         __syncwarp();
     } else {
         // ---------------------------------------------------- softmax / output
-        const int wq = warp & 3;
+        const int g = (warp - 2) >> 2;   // warps 2-5: tile A, 6-9: tile B
+        const int wq = warp & 3;         // TMEM lane quadrant of this warp
         const int row = wq * 32 + lane;  // query row == TMEM lane
-        const int i = i0 + row;          // query index in the chunk
+        const int i = i0 + g * QT + row;  // query index in the chunk
         const bool live = i < a.C;
         const int limit = live ? a.prefix + i : -1;  // last key this query sees
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t tO = tl + TM_O + 128 * g, tS = tl + TM_S + 128 * g;
+        const int nt = ntile[g];
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         auto wait_w = [&](uint32_t bar_, uint32_t par) {
             return __all_sync(0xffffffffu, mbar_wait(bar_, par, abort_flag, WAIT_NS));
         };
-        for (int t = 0; ok && t < nkt; ++t) {
-            if (!(ok = wait_w(s_full(t & 1), (t >> 1) & 1))) break;
+        for (int t = 0; ok && t < nt; ++t) {
+            if (!(ok = wait_w(s_full(g), t & 1))) break;
             tc_fence_after();
-            uint32_t raw_s[128];
-            const uint32_t ts = tl + TM_S + 128 * (t & 1);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld32(ts + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&raw_s[32 * c]));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(t & 1));
             const int vis = min(KT, max(0, limit - t * KT + 1));  // visible keys of the tile
+            // pass 1: the row maximum over the visible keys
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tS + 32 * c, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < KT; ++c)
-                if (c < vis) mx = fmaxf(mx, __uint_as_float(raw_s[c]));
+                for (int k = 0; k < 32; ++k)
+                    if (32 * c + k < vis) mx = fmaxf(mx, __uint_as_float(r[k]));
+            }
             mx *= a.scale_log2;
             const bool raise = mx > m + TAU;
             if (__any_sync(0xffffffffu, raise)) {
                 const float m_new = raise ? mx : m;
                 const float alpha = raise ? fast_exp2(m - m_new) : 1.f;
                 if (t > 0) {
-                    if (!(ok = wait_w(pv_done, (t - 1) & 1))) break;
+                    if (!(ok = wait_w(pv_done(g), (t - 1) & 1))) break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(tl + TM_O + 32 * c, r);
+                        tmem_ld32(tO + 32 * c, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
                             r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                        tmem_st32(tl + TM_O + 32 * c, r);
+                        tmem_st32(tO + 32 * c, r);
                     }
                     tmem_st_wait();
                 }
                 l *= alpha;
                 m = m_new;
             }
-            // P = exp2(scale * s - m) as bf16 pairs, 0 past the visible keys
+            // pass 2: P = exp2(scale * s - m) as bf16 pairs, 0 past the visible keys, over
+            // the S columns already read (keys 32c.. become columns 16c.., behind the reads)
             const float nm = m != -INFINITY ? -m : 0.f;
-            uint32_t pk[64];
             float es = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32], pk[16];
+                tmem_ld32(tS + 32 * c, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                const float p0 = 2 * k < vis
-                                     ? fast_exp2(fmaf(__uint_as_float(raw_s[2 * k]), a.scale_log2, nm))
-                                     : 0.f;
-                const float p1 = 2 * k + 1 < vis
-                                     ? fast_exp2(fmaf(__uint_as_float(raw_s[2 * k + 1]), a.scale_log2, nm))
-                                     : 0.f;
-                pk[k] = pack_bf16x2(p0, p1);
-                es += p0 + p1;
+                for (int k = 0; k < 16; ++k) {
+                    const int j = 32 * c + 2 * k;
+                    const float p0 =
+                        j < vis ? fast_exp2(fmaf(__uint_as_float(r[2 * k]), a.scale_log2, nm)) : 0.f;
+                    const float p1 = j + 1 < vis
+                                         ? fast_exp2(fmaf(__uint_as_float(r[2 * k + 1]), a.scale_log2, nm))
+                                         : 0.f;
+                    pk[k] = pack_bf16x2(p0, p1);
+                    es += p0 + p1;
+                }
+                tmem_st16(tS + 16 * c, pk);
             }
             l += es;
-            if (t > 0 && !(ok = wait_w(pv_done, (t - 1) & 1))) break;  // P columns free
-            tmem_st32(tl + TM_P, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(tl + TM_P + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(g));
         }
         // ------------------------------------------------------------- output
-        if (ok && wait_w(pv_done, (nkt - 1) & 1)) {
+        if (ok && nt > 0 && wait_w(pv_done(g), (nt - 1) & 1)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tl + TM_O + 32 * c, r);
+                tmem_ld32(tO + 32 * c, r);
                 tmem_ld_wait();
                 if (live) {
                     uint4 *dst = reinterpret_cast<uint4 *>(
@@ -422,7 +479,7 @@ cudaError_t launch_prefill_tc(const uint16_t *q_nope, const uint16_t *q_rope,
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    dim3 grid((C + QT - 1) / QT, H);
+    dim3 grid((C + 2 * QT - 1) / (2 * QT), H);
     return launch_pdl(prefill_tc_kernel, grid, dim3(NTHREADS), SMEM_TOTAL, stream, mqn, mqr, mkn, mkr,
                       mv, a);
 }
