@@ -288,16 +288,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = wait_w(s_full(g), t & 1))) break;
             tc_fence_after();
             const int vis = min(KT, max(0, limit - t * KT + 1));  // visible keys of the tile
-            // pass 1: the row maximum over the visible keys
+            // pass 1: the row maximum over the visible keys (all four loads in flight)
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS + 32 * c, r);
+            {
+                uint32_t r[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if (32 * c + k < vis) mx = fmaxf(mx, __uint_as_float(r[k]));
+                for (int k = 0; k < KT; ++k)
+                    if (k < vis) mx = fmaxf(mx, __uint_as_float(r[k]));
             }
             mx *= a.scale_log2;
             const bool raise = mx > m + TAU;
@@ -327,22 +328,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float nm = m != -INFINITY ? -m : 0.f;
             float es = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32], pk[16];
-                tmem_ld32(tS + 32 * c, r);
+            for (int c2 = 0; c2 < 2; ++c2) {  // 64 keys per load round
+                uint32_t r[64];
+                tmem_ld32(tS + 64 * c2, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(tS + 64 * c2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int j = 32 * c + 2 * k;
-                    const float p0 =
-                        j < vis ? fast_exp2(fmaf(__uint_as_float(r[2 * k]), a.scale_log2, nm)) : 0.f;
-                    const float p1 = j + 1 < vis
-                                         ? fast_exp2(fmaf(__uint_as_float(r[2 * k + 1]), a.scale_log2, nm))
-                                         : 0.f;
-                    pk[k] = pack_bf16x2(p0, p1);
-                    es += p0 + p1;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c = 2 * c2 + h2;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int j = 32 * c + 2 * k;
+                        const float p0 =
+                            j < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k]), a.scale_log2, nm))
+                                    : 0.f;
+                        const float p1 = j + 1 < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k + 1]),
+                                                                      a.scale_log2, nm))
+                                                     : 0.f;
+                        pk[k] = pack_bf16x2(p0, p1);
+                        es += p0 + p1;
+                    }
+                    tmem_st16(tS + 16 * c, pk);
                 }
-                tmem_st16(tS + 16 * c, pk);
             }
             l += es;
             tmem_st_wait();
