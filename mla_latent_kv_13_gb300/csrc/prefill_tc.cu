@@ -296,9 +296,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int c = 0; c < 4; ++c)
                     tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
                 tmem_ld_wait();
+                if (vis == KT) {  // every key visible (all but the diagonal tiles)
 #pragma unroll
-                for (int k = 0; k < KT; ++k)
-                    if (k < vis) mx = fmaxf(mx, __uint_as_float(r[k]));
+                    for (int k = 0; k < KT; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < KT; ++k)
+                        if (k < vis) mx = fmaxf(mx, __uint_as_float(r[k]));
+                }
             }
             mx *= a.scale_log2;
             const bool raise = mx > m + TAU;
@@ -333,21 +338,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tmem_ld32(tS + 64 * c2, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                 tmem_ld32(tS + 64 * c2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
+                const bool full = vis >= 64 * c2 + 64;  // every key of this round visible
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int c = 2 * c2 + h2;
                     uint32_t pk[16];
+                    if (full) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int j = 32 * c + 2 * k;
-                        const float p0 =
-                            j < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k]), a.scale_log2, nm))
-                                    : 0.f;
-                        const float p1 = j + 1 < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k + 1]),
+                        for (int k = 0; k < 16; ++k) {
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k]), a.scale_log2, nm));
+                            const float p1 =
+                                fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k + 1]), a.scale_log2, nm));
+                            pk[k] = pack_bf16x2(p0, p1);
+                            es += p0 + p1;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int j = 32 * c + 2 * k;
+                            const float p0 = j < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k]),
                                                                       a.scale_log2, nm))
                                                      : 0.f;
-                        pk[k] = pack_bf16x2(p0, p1);
-                        es += p0 + p1;
+                            const float p1 = j + 1 < vis ? fast_exp2(fmaf(__uint_as_float(r[32 * h2 + 2 * k + 1]),
+                                                                          a.scale_log2, nm))
+                                                         : 0.f;
+                            pk[k] = pack_bf16x2(p0, p1);
+                            es += p0 + p1;
+                        }
                     }
                     tmem_st16(tS + 16 * c, pk);
                 }
