@@ -173,3 +173,24 @@ def test_decode_fp8_long_sequences_sampled(mla):
                                            d["block_table"][rows], d["seqlens"][rows], d["scale"])
     assert_close_rows(out[rows], ref)
     assert_lse(lse[rows], lref)
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_decode_fp8_on_the_balanced_schedule(mla, H):
+    """More sequences than resident clusters, so the default plan is the balanced schedule:
+    clusters run several segments (the widening warps restart with every one) and
+    sequences cut between clusters are merged."""
+    rng = np.random.default_rng(9)
+    L = rng.integers(1, 900, 100)
+    L[:3] = (2000, 1, 64)
+    d, codes, exps = _fp8_case(100, H, tuple(int(x) for x in L), seed=9)
+    assert mla.decode_plan(100, H, int(L.max()), 0)[0] == 0
+    out, lse, st = _run_fp8(mla, d, codes, exps, 0)
+    assert st == 0
+    rows = [0, 1, 2, 17, 50, 99]
+    ref, lref = oracle.decode_absorbed_fp8(synth.bf16_bits_to_f64(d["q_lat"][rows]),
+                                           synth.bf16_bits_to_f64(d["q_rope"][rows]), codes, exps,
+                                           d["block_table"][rows], d["seqlens"][rows], d["scale"])
+    assert_close_rows(out[rows], ref)
+    assert_lse(lse[rows], lref)
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
