@@ -87,7 +87,7 @@ int sched_clusters(int B, int max_seqlen) {
 }
 
 struct DecodeLayout {
-    size_t tile_start, wpos, part_begin, nparts, o_part, lse_part, total;
+    size_t tile_start, wpos, part_begin, nparts, jobs, o_part, lse_part, total;
 };
 
 DecodeLayout decode_layout(int B, int H, int max_seqlen, int splits) {
@@ -108,7 +108,8 @@ DecodeLayout decode_layout(int B, int H, int max_seqlen, int splits) {
     L.wpos = L.tile_start + align256((size_t)(B + 1) * 4);
     L.part_begin = L.wpos + align256((size_t)(B + 1) * 4);
     L.nparts = L.part_begin + align256((size_t)B * 4);
-    L.o_part = L.nparts + align256((size_t)B * 4);
+    L.jobs = L.nparts + align256((size_t)B * 4);
+    L.o_part = L.jobs + align256((size_t)P * 16);
     L.lse_part = L.o_part + align256(parts * H * D_C * sizeof(float));
     L.total = L.lse_part + align256(parts * H * sizeof(float));
     return L;
@@ -377,12 +378,13 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     p.nparts = nparts;
     p.o_part = reinterpret_cast<float *>(w + lay.o_part);
     p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
-    if (launch_decode_schedule(seqlens, B, max_seqlen, P, tile_start, wpos, part_begin, nparts,
-                               p.err, st) != cudaSuccess)
+    int4 *jobs = reinterpret_cast<int4 *>(w + lay.jobs);
+    if (launch_decode_schedule(seqlens, B, max_seqlen, P, H, tile_start, wpos, part_begin,
+                               nparts, jobs, out, out_f32, lse, p.err, st) != cudaSuccess)
         return MLA_ERR_CUDA;
     if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
-    return cuda_status(launch_combine_sched(p.o_part, p.lse_part, tile_start, part_begin, nparts,
-                                            B, H, out, out_f32, lse, st));
+    return cuda_status(launch_combine_sched(p.o_part, p.lse_part, jobs, P, H, out, out_f32, lse,
+                                            st));
 }
 
 }  // namespace

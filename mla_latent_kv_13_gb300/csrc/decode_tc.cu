@@ -276,8 +276,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
     cluster_sync();  // the peer's barriers exist before any remote operation
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    grid_launch_dependents();
     grid_dependency_wait();  // q, the cache rows and the schedule come from predecessor kernels
+    // only now: the merge kernel that follows reads the schedule's job list before its own
+    // dependency wait
+    grid_launch_dependents();
 
     // ---- work: one (sequence, token range) per cluster, or, with the balanced
     // schedule, the segments of this cluster's equal share of the weighted tile list
@@ -931,13 +933,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
                                 pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv,
                                             __uint_as_float(r[8 * k + 7]) * inv));
                     } else {
-                        float4 *dst = reinterpret_cast<float4 *>(orow32 + 32 * c);
+                        // parts are kept in L2 (evict-last) until the merge that follows reads
+                        // them: the tail part of a cut sequence is written early in the launch
+                        const uint64_t pol = direct ? l2_policy_evict_normal() : l2_policy_evict_last();
+                        float *dst = orow32 + 32 * c;
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv,
-                                                 __uint_as_float(r[4 * k + 1]) * inv,
-                                                 __uint_as_float(r[4 * k + 2]) * inv,
-                                                 __uint_as_float(r[4 * k + 3]) * inv);
+                            st_global_v4_hint(dst + 4 * k, __uint_as_float(r[4 * k]) * inv,
+                                              __uint_as_float(r[4 * k + 1]) * inv,
+                                              __uint_as_float(r[4 * k + 2]) * inv,
+                                              __uint_as_float(r[4 * k + 3]) * inv, pol);
                     }
                 }
             }

@@ -10,47 +10,60 @@ namespace {
 
 // Merge np partial rows (fp32 [512], each with its log-sum-exp) into one bf16 row and its
 // log-sum-exp, with one warp: lane l holds columns 4l + 128k (k < 4), so every part row is
-// read as four coalesced 512-byte segments; the parts' log-sum-exps are read in parallel
-// across lanes (part s on lane s % 32) and their weights shared by shuffles. Parts are
+// read as four coalesced 512-byte segments. Every lane reads every part's log-sum-exp (one
+// broadcast load each). The rows of the first two parts are loaded together with the
+// log-sum-exps, before the weights are known, so that merging two parts (a sequence cut
+// once) takes one memory round trip; further parts follow two at a time. Parts are
 // accumulated in order. A part with lse = -inf (an empty range) contributes nothing.
 __device__ __forceinline__ void merge_row_warp(const float *o0, size_t ostride, const float *l0,
                                                size_t lstride, int np, uint16_t *orow,
                                                float *orow32, float *lse_out, int lane) {
-    constexpr unsigned FULL = 0xffffffffu;
-    float m = -INFINITY;
-    for (int s = lane; s < np; s += 32) m = fmaxf(m, l0[s * lstride]);
+    auto load_row = [&](int s, float4 (&v)[4]) {
+        const float *row = o0 + (size_t)s * ostride + lane * 4;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        for (int k = 0; k < 4; ++k) v[k] = __ldcs(reinterpret_cast<const float4 *>(row + 128 * k));
+    };
+    float4 va[4], vb[4];
+    const float la = np > 0 ? l0[0] : -INFINITY;
+    const float lb = np > 1 ? l0[lstride] : -INFINITY;
+    if (np > 0) load_row(0, va);
+    if (np > 1) load_row(1, vb);
+    float m = fmaxf(la, lb);
+    for (int s = 2; s < np; ++s) m = fmaxf(m, l0[s * lstride]);
     float tot = -INFINITY;
     if (m != -INFINITY) {
         float den = 0.f;
-        for (int s = lane; s < np; s += 32) {
+        if (la != -INFINITY) den += __expf(la - m);
+        if (lb != -INFINITY) den += __expf(lb - m);
+        for (int s = 2; s < np; ++s) {
             const float l = l0[s * lstride];
             if (l != -INFINITY) den += __expf(l - m);
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(FULL, den, o);
         tot = m + __logf(den);
-        for (int s0 = 0; s0 < np; s0 += 32) {
-            const float lmine = s0 + lane < np ? l0[(s0 + lane) * lstride] : -INFINITY;
-            const float wmine = lmine != -INFINITY ? __expf(lmine - tot) : 0.f;
-            const int cnt = min(32, np - s0);
-            for (int j = 0; j < cnt; ++j) {
-                if (__shfl_sync(FULL, lmine, j) == -INFINITY) continue;
-                const float w = __shfl_sync(FULL, wmine, j);
-                const float *row = o0 + (size_t)(s0 + j) * ostride + lane * 4;
+    }
+    float acc[16];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 v = *reinterpret_cast<const float4 *>(row + 128 * k);
-                    acc[4 * k] += w * v.x;
-                    acc[4 * k + 1] += w * v.y;
-                    acc[4 * k + 2] += w * v.z;
-                    acc[4 * k + 3] += w * v.w;
-                }
-            }
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    auto add_row = [&](float l, const float4 (&v)[4]) {
+        const float w = l != -INFINITY ? __expf(l - tot) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[4 * k] += w * v[k].x;
+            acc[4 * k + 1] += w * v[k].y;
+            acc[4 * k + 2] += w * v[k].z;
+            acc[4 * k + 3] += w * v[k].w;
+        }
+    };
+    if (tot != -INFINITY) {
+        if (np > 0) add_row(la, va);
+        if (np > 1) add_row(lb, vb);
+        for (int s = 2; s < np; s += 2) {
+            const float l2 = l0[s * lstride];
+            const float l3 = s + 1 < np ? l0[(s + 1) * lstride] : -INFINITY;
+            load_row(s, va);
+            if (s + 1 < np) load_row(s + 1, vb);
+            add_row(l2, va);
+            if (s + 1 < np) add_row(l3, vb);
         }
     }
     if (orow32) {
@@ -153,18 +166,41 @@ __device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_to
     return total;
 }
 
-// One CTA of 1024 threads (B <= 4096): tiles per sequence -> tile_start; weighted
-// positions (SEG_COST + tiles per sequence with tiles) -> wpos; parts of the sequences that
-// the equal split of the total weight cuts between clusters.
-__global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seqlens, int B,
-                                                               int max_len, int P,
-                                                               int32_t *tile_start,
-                                                               int32_t *wpos,
-                                                               int32_t *part_begin,
-                                                               int32_t *nparts, uint32_t *err) {
+constexpr int EMPTY_CTAS = 32;  // CTAs of the schedule kernel writing empty sequences
+
+// CTA 0 of 1024 threads (B <= 4096): tiles per sequence -> tile_start; weighted positions
+// (SEG_COST + tiles per sequence with tiles) -> wpos; parts of the sequences that the equal
+// split of the total weight cuts between clusters -> nparts, part_begin; and the merge jobs:
+// the sequence cut at the end of cluster c's range (its first tile in that range) is job c,
+// jobs[c] = (b, first part, parts), else (-1, 0, 0). CTAs 1..EMPTY_CTAS write the output of
+// the sequences without tiles, which no cluster's range holds: out = 0 (or out_f32 = 0),
+// lse = -inf; CTA j takes b = j - 1 (mod EMPTY_CTAS), 16 rows of H at a time.
+__global__ void __launch_bounds__(1024) decode_schedule_kernel(
+    const int32_t *seqlens, int B, int max_len, int P, int H, int32_t *tile_start,
+    int32_t *wpos, int32_t *part_begin, int32_t *nparts, int4 *jobs, uint16_t *out,
+    float *out_f32, float *lse, uint32_t *err) {
     __shared__ int v[4096], ex[4096], warp_tot[33];
     grid_launch_dependents();
     grid_dependency_wait();
+    if (blockIdx.x > 0) {
+        for (int b = blockIdx.x - 1; b < B; b += EMPTY_CTAS) {
+            const int L = seqlens[b];  // clamped to [0, max_len] as below: empty iff 0
+            if (L > 0 && max_len > 0) continue;
+            const int t = threadIdx.x & 63;
+            for (int h = threadIdx.x >> 6; h < H; h += 16) {
+                const size_t row = ((size_t)b * H + h) * D_C;
+                if (out_f32) {
+                    float4 *d = reinterpret_cast<float4 *>(out_f32 + row);
+                    d[t] = d[t + 64] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    reinterpret_cast<uint4 *>(out + row)[t] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            for (int h = threadIdx.x; h < H; h += blockDim.x) lse[(size_t)b * H + h] = -INFINITY;
+        }
+        return;
+    }
+    for (int c = threadIdx.x; c < P; c += blockDim.x) jobs[c] = make_int4(-1, 0, 0, 0);
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seqlens[b];
         if (L < 0 || L > max_len) {  // the attention kernel clamps the same way
@@ -200,48 +236,49 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
     for (int b = threadIdx.x; b < B; b += blockDim.x) v[b] = nparts[b];
     __syncthreads();
     block_exclusive_scan4(v, B, ex, warp_tot);
-    for (int b = threadIdx.x; b < B; b += blockDim.x) part_begin[b] = ex[b];
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        part_begin[b] = ex[b];
+        if (v[b] > 0)  // after the initialisation above (block_exclusive_scan4 synchronises)
+            jobs[cluster_of_tile(wpos[b], W, Pe)] = make_int4(b, ex[b], v[b], 0);
+    }
 }
 
-// Merge of the parts of each cut sequence; empty sequences get out = 0, lse = -inf;
-// sequences finished inside one cluster were written by the attention kernel itself.
-// Balanced schedule: only sequences cut between clusters (nparts > 0) and empty ones are
-// written here; the decode kernel wrote the others. Grid (ceil(H / 8), B), 256 threads.
+// Merge of the parts of each sequence cut between clusters. Grid (ceil(H / 8), P): CTA
+// (x, c) merges rows 8x .. 8x+7 of job c, one warp per row. The job list comes from the
+// schedule kernel, which had finished before the attention kernel let this grid start, so
+// it is read before the dependency wait.
 __global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
-    const float *o_part, const float *lse_part, const int32_t *tile_start,
-    const int32_t *part_begin, const int32_t *nparts, int H, uint16_t *out, float *out_f32,
-    float *lse) {
+    const float *o_part, const float *lse_part, const int4 *jobs, int H, uint16_t *out,
+    float *out_f32, float *lse) {
+    const int4 job = __ldcg(jobs + blockIdx.y);
+    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5);
     grid_launch_dependents();
+    if (job.x < 0 || h >= H) return;
     grid_dependency_wait();
-    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), b = blockIdx.y;
-    if (h >= H) return;
-    const int np = nparts[b];
-    const bool empty = tile_start[b + 1] == tile_start[b];
-    if (np == 0 && !empty) return;
-    const int p0 = np > 0 ? part_begin[b] : 0;
-    const size_t row = (size_t)b * H + h;
-    merge_row_warp(o_part + ((size_t)p0 * H + h) * D_C, (size_t)H * D_C,
-                   lse_part + (size_t)p0 * H + h, H, np,
+    const size_t row = (size_t)job.x * H + h;
+    merge_row_warp(o_part + ((size_t)job.y * H + h) * D_C, (size_t)H * D_C,
+                   lse_part + (size_t)job.y * H + h, H, job.z,
                    out_f32 ? nullptr : out + row * D_C, out_f32 ? out_f32 + row * D_C : nullptr,
                    lse + row, threadIdx.x & 31);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P,
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P, int H,
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
-                                   int32_t *nparts, uint32_t *err, cudaStream_t stream) {
-    return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
-                      max_len, P, tile_start, wpos, part_begin, nparts, err);
+                                   int32_t *nparts, int4 *jobs, uint16_t *out, float *out_f32,
+                                   float *lse, uint32_t *err, cudaStream_t stream) {
+    return launch_pdl(decode_schedule_kernel, dim3(1 + EMPTY_CTAS), dim3(1024), 0, stream,
+                      seqlens, B, max_len, P, H, tile_start, wpos, part_begin, nparts, jobs, out,
+                      out_f32, lse, err);
 }
 
-cudaError_t launch_combine_sched(const float *o_part, const float *lse_part,
-                                 const int32_t *tile_start, const int32_t *part_begin,
-                                 const int32_t *nparts, int B, int H, uint16_t *out,
-                                 float *out_f32, float *lse, cudaStream_t stream) {
-    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, B);
+cudaError_t launch_combine_sched(const float *o_part, const float *lse_part, const int4 *jobs,
+                                 int P, int H, uint16_t *out, float *out_f32, float *lse,
+                                 cudaStream_t stream) {
+    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, P);
     return launch_pdl(combine_sched_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part,
-                      lse_part, tile_start, part_begin, nparts, H, out, out_f32, lse);
+                      lse_part, jobs, H, out, out_f32, lse);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,

@@ -182,6 +182,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 16-byte global store with an L2 cache policy for the line it writes
+__device__ __forceinline__ void st_global_v4_hint(void *ptr, float a, float b, float c, float d,
+                                                  uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol)
+                 : "memory");
+}
 // tma_load_2d with an L2 cache policy for the lines it reads
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *map, uint32_t bar,
                                                  int x, int y, uint64_t policy) {
