@@ -152,6 +152,10 @@ def _check_schedule(seqlens, max_blocks, clusters, seg_cost=12):
         cls = [c for c, _ in ps]
         assert cls == list(range(cls[0], cls[0] + len(ps)))
         assert [p for _, p in ps] == list(range(ps[0][1], ps[0][1] + len(ps)))
+    # the merge kernel takes one job per cluster, the sequence whose first part that cluster
+    # holds: no two cut sequences start in the same cluster
+    firsts = [ps[0][0] for ps in parts_of.values()]
+    assert len(firsts) == len(set(firsts))
     # balance: no cluster costs more than its share of the weight plus one start-up
     share = -(-W // P) if P else 0
     for ss in by_cluster.values():
