@@ -132,7 +132,6 @@ constexpr int NTHREADS_FP8 = 320;             // + 3 warps widening the FP8 tile
 constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded waits: 1 s
 constexpr uint64_t DRAIN_NS = 200000000ull;
 constexpr float TAU = 8.0f;                   // lazy-rescale threshold (log2 units)
-constexpr int PF_DIST = 4;                    // tiles prefetched into L2 beyond the rings
 constexpr uint32_t XBYTES = PWARP;            // one warp's message: P rows + (reference, sum)
 
 constexpr uint32_t IDESC_S = idesc_bf16(128, HALF, false, false);
@@ -342,35 +341,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
-            // Tiles beyond the shared-memory rings are prefetched into L2 (each CTA its own
-            // 32 tokens, all columns: the peer's value chunks of them included), so that a
-            // load issued when a slot frees up is served from L2 rather than from HBM.
-            auto prefetch = [&](int t) {
-                if (t >= n) return;
-                const int blk = btab[t_begin + t];
-                if (blk < 0 || blk >= p.num_blocks) return;
-                for (int d = 0; d < NOWN; ++d)
-                    tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
-            };
-            // Near the end of a scheduled segment, warm L2 with the next segment's Q rows
-            // and first tiles, so that its start does not wait on HBM round trips.
+            // The rings are the only lookahead for the cache tiles: prefetching tiles beyond
+            // them into L2 (2, 4 or 6 tiles ahead, or the next segment's first tiles) made
+            // every workload slower, and the longer distances raised the DRAM reads (the
+            // prefetched lines left L2 before their loads came). Near the end of a scheduled
+            // segment only the next segment's Q rows are sent to L2.
             auto prefetch_next = [&]() {
                 const int nb = sched_peek(p.tile_start, p.wpos, p.B, r1, seg_b);
                 if (nb < 0) return;  // no further sequence in this cluster's share
                 bulk_prefetch_l2(p.q_lat + (size_t)nb * H * D_C, static_cast<uint32_t>(H * D_C * 2));
                 bulk_prefetch_l2(p.q_rope + (size_t)nb * H * D_ROPE,
                                  static_cast<uint32_t>(H * D_ROPE * 2));
-                const long ws = p.wpos[nb], we = ws + (p.tile_start[nb + 1] - p.tile_start[nb]);
-                const long nt = min(static_cast<long>(NKV + PF_DIST), min(r1, we) - ws);
-                const int32_t *bt = p.block_table + (size_t)nb * p.max_blocks;
-                for (int t = 0; t < nt; ++t) {
-                    const int blk = bt[t];
-                    if (blk < 0 || blk >= p.num_blocks) continue;
-                    for (int d = 0; d < NOWN; ++d)
-                        tma_prefetch_l2_2d(&map_kv, 64 * d, blk * TOK + HALF * rank);
-                }
             };
-            const int next_at = sched ? max(0, n - (NKV + PF_DIST + 4)) : -1;
+            const int next_at = sched ? max(0, n - (NKV + 8)) : -1;
             // L2 priorities: the own tokens' chunks in the peer's output columns are read
             // again by the peer (its V ring) and keep the normal priority; every other
             // chunk is read once and is marked to leave L2 first, so that the chunks still
@@ -412,9 +395,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
                     mbar_arrive(k_full(sk));
                 }
                 issued_k = i + 1;
-                if (i == 0)  // after the first tile's loads are on their way
-                    for (int t = NKV; t < NKV + PF_DIST; ++t) prefetch(t);
-                if (i >= NKV) prefetch(i + PF_DIST);
                 if (i == next_at) prefetch_next();
             }
             // copies still in flight must land before this CTA may exit
