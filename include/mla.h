@@ -162,6 +162,34 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
                                   float scale, int num_splits, void *workspace,
                                   size_t ws_bytes, mla_bf16_t *out, float *lse,
                                   mla_stream_t stream);
+/*
+ * The balanced schedule of mla_decode_attention computed ahead of the call (no counterpart
+ * on the pages: it depends only on the sequence lengths, so a decode step computes it once
+ * for every layer, and may compute it on another stream, next to the query projections).
+ * Writes the schedule into the workspace: the same workspace layout, the same arguments
+ * (B, H, max_seqlen, num_splits) as the attention calls that use it; does nothing when the
+ * plan for them is a fixed split. seqlens [B] device int32 as in mla_decode_attention
+ * (lengths outside [0, max_seqlen] are recorded and clamped here). The workspace's first
+ * 256 bytes (the error word) must be zero as for mla_decode_attention.
+ * MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED / MLA_ERR_WORKSPACE as mla_decode_attention.
+ */
+mla_status_t mla_decode_prepare(const int32_t *seqlens, int B, int H, int max_seqlen,
+                                int num_splits, void *workspace, size_t ws_bytes,
+                                mla_stream_t stream);
+/*
+ * mla_decode_attention over a workspace that mla_decode_prepare filled for the same seqlens
+ * (unchanged since), B, H, max_seqlen and num_splits: the same outputs, bit for bit, without
+ * the schedule launch. The prepare call's kernel must be complete before this call's kernels
+ * start (the same stream, or an event the caller waits for). A workspace not prepared for
+ * these arguments gives undefined results.
+ */
+mla_status_t mla_decode_attention_prepared(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                           const mla_bf16_t *kv_cache, int num_blocks,
+                                           const int32_t *block_table, int max_blocks,
+                                           const int32_t *seqlens, int B, int H, int max_seqlen,
+                                           float scale, int num_splits, void *workspace,
+                                           size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                           mla_stream_t stream);
 
 /*
  * Decode attention for s_q query tokens per sequence: the draft tokens a main model

@@ -323,7 +323,7 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                         int max_seqlen, float scale, int num_splits, void *workspace,
                         size_t ws_bytes, mla_bf16_t *out, float *out_f32, float *lse,
                         mla_stream_t stream, const uint8_t *codes = nullptr,
-                        const int8_t *exps = nullptr) {
+                        const int8_t *exps = nullptr, bool prepared = false) {
     const int H = s_q * hq;
     const void *out_any = out_f32 ? static_cast<const void *>(out_f32) : out;
     const void *cache_any = codes ? static_cast<const void *>(codes) : kv_cache;
@@ -379,12 +379,12 @@ mla_status_t decode_run(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
     p.o_part = reinterpret_cast<float *>(w + lay.o_part);
     p.lse_part = reinterpret_cast<float *>(w + lay.lse_part);
     int4 *jobs = reinterpret_cast<int4 *>(w + lay.jobs);
-    if (launch_decode_schedule(seqlens, B, max_seqlen, P, H, tile_start, wpos, part_begin,
-                               nparts, jobs, out, out_f32, lse, p.err, st) != cudaSuccess)
+    if (!prepared && launch_decode_schedule(seqlens, B, max_seqlen, P, tile_start, wpos,
+                                            part_begin, nparts, jobs, p.err, st) != cudaSuccess)
         return MLA_ERR_CUDA;
     if (launch_decode_tc(p, P, st) != cudaSuccess) return MLA_ERR_CUDA;
-    return cuda_status(launch_combine_sched(p.o_part, p.lse_part, jobs, P, H, out, out_f32, lse,
-                                            st));
+    return cuda_status(launch_combine_sched(p.o_part, p.lse_part, jobs, tile_start, B, P, H, out,
+                                            out_f32, lse, st));
 }
 
 }  // namespace
@@ -401,6 +401,38 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
     return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
                       1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
                       stream);
+}
+
+mla_status_t mla_decode_prepare(const int32_t *seqlens, int B, int H, int max_seqlen,
+                                int num_splits, void *workspace, size_t ws_bytes,
+                                mla_stream_t stream) {
+    if (!seqlens || !workspace || B < 1 || B > 4096 || max_seqlen < 0 || num_splits < 0 ||
+        num_splits > 256)
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+    const int splits = plan_decode_splits(B, H, max_seqlen, num_splits);
+    const DecodeLayout lay = decode_layout(B, H, max_seqlen, splits);
+    if (ws_bytes < lay.total) return MLA_ERR_WORKSPACE;
+    if (splits != 0) return MLA_OK;  // a fixed split needs no schedule
+    char *w = static_cast<char *>(workspace);
+    return cuda_status(launch_decode_schedule(
+        seqlens, B, max_seqlen, sched_clusters(B, max_seqlen),
+        reinterpret_cast<int32_t *>(w + lay.tile_start), reinterpret_cast<int32_t *>(w + lay.wpos),
+        reinterpret_cast<int32_t *>(w + lay.part_begin), reinterpret_cast<int32_t *>(w + lay.nparts),
+        reinterpret_cast<int4 *>(w + lay.jobs), err_word(workspace), S(stream)));
+}
+
+mla_status_t mla_decode_attention_prepared(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
+                                           const mla_bf16_t *kv_cache, int num_blocks,
+                                           const int32_t *block_table, int max_blocks,
+                                           const int32_t *seqlens, int B, int H, int max_seqlen,
+                                           float scale, int num_splits, void *workspace,
+                                           size_t ws_bytes, mla_bf16_t *out, float *lse,
+                                           mla_stream_t stream) {
+    return decode_run(q_lat, q_rope, kv_cache, num_blocks, block_table, max_blocks, seqlens, B,
+                      1, H, max_seqlen, scale, num_splits, workspace, ws_bytes, out, nullptr, lse,
+                      stream, nullptr, nullptr, true);
 }
 
 mla_status_t mla_decode_attention_fp8(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,

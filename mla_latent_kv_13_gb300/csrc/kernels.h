@@ -135,16 +135,16 @@ __host__ __device__ inline int sched_peek(const int32_t *tile_start, const int32
 
 // seqlens outside [0, max_len] are recorded as MLA_ERR_OUT_OF_RANGE and clamped to it.
 // Also lists the merge jobs (jobs [P]: (sequence, first part, parts) of the sequence cut at
-// the end of cluster c's range, or (-1, 0, 0)) and writes the output of the sequences
-// without tiles (out = 0, or out_f32 = 0 when given; lse = -inf).
-cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P, int H,
+// the end of cluster c's range, or (-1, 0, 0)).
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P,
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
-                                   int32_t *nparts, int4 *jobs, uint16_t *out, float *out_f32,
-                                   float *lse, uint32_t *err, cudaStream_t stream);
-// Merges the jobs' parts; out_f32 (if non-null) receives the rows as fp32 instead of out
+                                   int32_t *nparts, int4 *jobs, uint32_t *err,
+                                   cudaStream_t stream);
+// Merges the jobs' parts and writes the sequences without tiles (out = 0, lse = -inf);
+// out_f32 (if non-null) receives the rows as fp32 instead of out
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part, const int4 *jobs,
-                                 int P, int H, uint16_t *out, float *out_f32, float *lse,
-                                 cudaStream_t stream);
+                                 const int32_t *tile_start, int B, int P, int H, uint16_t *out,
+                                 float *out_f32, float *lse, cudaStream_t stream);
 
 // grid = `clusters` two-CTA clusters (one per work item, or P with the schedule)
 cudaError_t launch_decode_tc(const DecodeParams &p, int clusters, cudaStream_t stream);

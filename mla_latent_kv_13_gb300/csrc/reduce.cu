@@ -166,40 +166,18 @@ __device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_to
     return total;
 }
 
-constexpr int EMPTY_CTAS = 32;  // CTAs of the schedule kernel writing empty sequences
-
-// CTA 0 of 1024 threads (B <= 4096): tiles per sequence -> tile_start; weighted positions
+// One CTA of 1024 threads (B <= 4096): tiles per sequence -> tile_start; weighted positions
 // (SEG_COST + tiles per sequence with tiles) -> wpos; parts of the sequences that the equal
 // split of the total weight cuts between clusters -> nparts, part_begin; and the merge jobs:
 // the sequence cut at the end of cluster c's range (its first tile in that range) is job c,
-// jobs[c] = (b, first part, parts), else (-1, 0, 0). CTAs 1..EMPTY_CTAS write the output of
-// the sequences without tiles, which no cluster's range holds: out = 0 (or out_f32 = 0),
-// lse = -inf; CTA j takes b = j - 1 (mod EMPTY_CTAS), 16 rows of H at a time.
+// jobs[c] = (b, first part, parts), else (-1, 0, 0). Reads only seqlens, so it may run once
+// for several attention calls over the same lengths.
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(
-    const int32_t *seqlens, int B, int max_len, int P, int H, int32_t *tile_start,
-    int32_t *wpos, int32_t *part_begin, int32_t *nparts, int4 *jobs, uint16_t *out,
-    float *out_f32, float *lse, uint32_t *err) {
+    const int32_t *seqlens, int B, int max_len, int P, int32_t *tile_start, int32_t *wpos,
+    int32_t *part_begin, int32_t *nparts, int4 *jobs, uint32_t *err) {
     __shared__ int v[4096], ex[4096], warp_tot[33];
     grid_launch_dependents();
     grid_dependency_wait();
-    if (blockIdx.x > 0) {
-        for (int b = blockIdx.x - 1; b < B; b += EMPTY_CTAS) {
-            const int L = seqlens[b];  // clamped to [0, max_len] as below: empty iff 0
-            if (L > 0 && max_len > 0) continue;
-            const int t = threadIdx.x & 63;
-            for (int h = threadIdx.x >> 6; h < H; h += 16) {
-                const size_t row = ((size_t)b * H + h) * D_C;
-                if (out_f32) {
-                    float4 *d = reinterpret_cast<float4 *>(out_f32 + row);
-                    d[t] = d[t + 64] = make_float4(0.f, 0.f, 0.f, 0.f);
-                } else {
-                    reinterpret_cast<uint4 *>(out + row)[t] = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            for (int h = threadIdx.x; h < H; h += blockDim.x) lse[(size_t)b * H + h] = -INFINITY;
-        }
-        return;
-    }
     for (int c = threadIdx.x; c < P; c += blockDim.x) jobs[c] = make_int4(-1, 0, 0, 0);
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seqlens[b];
@@ -243,42 +221,70 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(
     }
 }
 
-// Merge of the parts of each sequence cut between clusters. Grid (ceil(H / 8), P): CTA
-// (x, c) merges rows 8x .. 8x+7 of job c, one warp per row. The job list comes from the
-// schedule kernel, which had finished before the attention kernel let this grid start, so
-// it is read before the dependency wait.
+constexpr int EMPTY_CTAS = 32;  // rows of CTAs of the merge kernel writing empty sequences
+
+// Balanced schedule, after the attention kernel. Grid (ceil(H / 8), P + EMPTY_CTAS), one warp
+// per head row. CTA (x, c < P) merges rows 8x .. 8x+7 of job c, the sequence cut at the end
+// of cluster c's range. CTA (x, P + j) writes rows 8x .. 8x+7 of the sequences without tiles
+// among b = j (mod EMPTY_CTAS), which no cluster's range holds: out = 0 (or out_f32 = 0),
+// lse = -inf. The job list comes from the schedule kernel, which had finished before the
+// attention kernel let this grid start, so it is read before the dependency wait. CTA (0, 0)
+// waits even without a job: a grid that completes counts as done for its successors only
+// once one of its CTAs has waited for the attention kernel.
 __global__ void __launch_bounds__(32 * MERGE_ROWS) combine_sched_kernel(
-    const float *o_part, const float *lse_part, const int4 *jobs, int H, uint16_t *out,
-    float *out_f32, float *lse) {
-    const int4 job = __ldcg(jobs + blockIdx.y);
-    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5);
+    const float *o_part, const float *lse_part, const int4 *jobs, const int32_t *tile_start,
+    int B, int P, int H, uint16_t *out, float *out_f32, float *lse) {
+    const int h = blockIdx.x * MERGE_ROWS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     grid_launch_dependents();
-    if (job.x < 0 || h >= H) return;
+    if (blockIdx.y >= P) {  // empty sequences
+        grid_dependency_wait();
+        if (h >= H) return;
+        const int j = blockIdx.y - P;
+        for (int base = j; base < B; base += 32 * EMPTY_CTAS) {
+            const int bq = base + EMPTY_CTAS * lane;
+            const bool e = bq < B && tile_start[bq + 1] == tile_start[bq];
+            for (unsigned m = __ballot_sync(0xffffffffu, e); m; m &= m - 1) {
+                const size_t row = (size_t)(base + EMPTY_CTAS * (__ffs(m) - 1)) * H + h;
+                if (out_f32) {
+                    float4 *d = reinterpret_cast<float4 *>(out_f32 + row * D_C);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) d[lane + 32 * k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    uint4 *d = reinterpret_cast<uint4 *>(out + row * D_C);
+                    d[lane] = d[lane + 32] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (lane == 0) lse[row] = -INFINITY;
+            }
+        }
+        return;
+    }
+    const int4 job = __ldcg(jobs + blockIdx.y);
+    if ((job.x < 0 || h >= H) && (blockIdx.x | blockIdx.y) != 0) return;
     grid_dependency_wait();
+    if (job.x < 0 || h >= H) return;
     const size_t row = (size_t)job.x * H + h;
     merge_row_warp(o_part + ((size_t)job.y * H + h) * D_C, (size_t)H * D_C,
                    lse_part + (size_t)job.y * H + h, H, job.z,
                    out_f32 ? nullptr : out + row * D_C, out_f32 ? out_f32 + row * D_C : nullptr,
-                   lse + row, threadIdx.x & 31);
+                   lse + row, lane);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P, int H,
+cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, int P,
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
-                                   int32_t *nparts, int4 *jobs, uint16_t *out, float *out_f32,
-                                   float *lse, uint32_t *err, cudaStream_t stream) {
-    return launch_pdl(decode_schedule_kernel, dim3(1 + EMPTY_CTAS), dim3(1024), 0, stream,
-                      seqlens, B, max_len, P, H, tile_start, wpos, part_begin, nparts, jobs, out,
-                      out_f32, lse, err);
+                                   int32_t *nparts, int4 *jobs, uint32_t *err,
+                                   cudaStream_t stream) {
+    return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
+                      max_len, P, tile_start, wpos, part_begin, nparts, jobs, err);
 }
 
 cudaError_t launch_combine_sched(const float *o_part, const float *lse_part, const int4 *jobs,
-                                 int P, int H, uint16_t *out, float *out_f32, float *lse,
-                                 cudaStream_t stream) {
-    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, P);
+                                 const int32_t *tile_start, int B, int P, int H, uint16_t *out,
+                                 float *out_f32, float *lse, cudaStream_t stream) {
+    dim3 grid((H + MERGE_ROWS - 1) / MERGE_ROWS, P + EMPTY_CTAS);
     return launch_pdl(combine_sched_kernel, grid, dim3(32 * MERGE_ROWS), 0, stream, o_part,
-                      lse_part, jobs, H, out, out_f32, lse);
+                      lse_part, jobs, tile_start, B, P, H, out, out_f32, lse);
 }
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int B, int S, int H,

@@ -52,6 +52,9 @@ _SIGS = {
                             _i),
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
                               _vp, _vp, _vp], _i),
+    "mla_decode_prepare": ([_vp, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "mla_decode_attention_prepared": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
+                                       _sz, _vp, _vp, _vp], _i),
     "mla_decode_combine": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
     "mla_decode_attention_partial": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp,
                                       _sz, _vp, _vp, _vp], _i),
@@ -215,6 +218,30 @@ def decode_attention(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, 
                                    float(scale), int(num_splits), _ptr(workspace),
                                    workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
     _ok(rc, "mla_decode_attention")
+    return out, lse, workspace
+
+
+def decode_prepare(seqlens, B, H, max_seqlen, num_splits, workspace, stream=None):
+    """mla_decode_prepare: the balanced schedule for these lengths into the workspace (nothing
+    when the plan is a fixed split), for decode_attention_prepared calls over the same
+    lengths and arguments."""
+    rc = _lib.mla_decode_prepare(_ptr(seqlens), int(B), int(H), int(max_seqlen), int(num_splits),
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _ok(rc, "mla_decode_prepare")
+    return workspace
+
+
+def decode_attention_prepared(q_lat, q_rope, kv_cache, block_table, seqlens, max_seqlen, scale,
+                              num_splits, out, lse, workspace, stream=None):
+    """mla_decode_attention_prepared: decode_attention over a workspace that decode_prepare
+    filled for the same lengths and arguments. Returns (out, lse, workspace)."""
+    B, H, _ = q_lat.shape
+    rc = _lib.mla_decode_attention_prepared(
+        _ptr(_bits(q_lat)), _ptr(_bits(q_rope)), _ptr(_bits(kv_cache)), kv_cache.shape[0],
+        _ptr(block_table), block_table.shape[1], _ptr(seqlens), B, H, int(max_seqlen),
+        float(scale), int(num_splits), _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+        _stream(stream))
+    _ok(rc, "mla_decode_attention_prepared")
     return out, lse, workspace
 
 
@@ -487,8 +514,9 @@ class DecodeStep:
         self.o_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.y = torch.empty((B, self.dm), dtype=torch.bfloat16, device=dev)
-        # append_kv and absorb_q read only h and pos: the append runs on a side stream,
-        # forked from and joined back into the caller's stream by events
+        # append_kv and absorb_q read only h and pos, the attention schedule only the
+        # lengths: the append and the schedule run on a side stream, forked from and joined
+        # back into the caller's stream by events
         self.side = torch.cuda.Stream(device=dev)
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()
@@ -501,15 +529,17 @@ class DecodeStep:
         main = torch.cuda.current_stream() if stream is None else stream
         self.ev_fork.record(main)
         self.side.wait_event(self.ev_fork)
+        decode_prepare(seqlens_after, self.B, self.H, self.max_seqlen, self.num_splits,
+                       self.ws_att, self.side)
         append_kv(h, w["w_dkr"], pos, block_table, kv_cache, self.theta, self.ws_append,
                   self.side)
         self.ev_join.record(self.side)
         absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, self.theta, self.q_lat,
                  self.q_rope, self.ws_q, main)
         main.wait_event(self.ev_join)  # attention reads the row the append wrote
-        decode_attention(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
-                         self.max_seqlen, self.scale, self.num_splits, self.o_lat, self.lse,
-                         self.ws_att, main)
+        decode_attention_prepared(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
+                                  self.max_seqlen, self.scale, self.num_splits, self.o_lat,
+                                  self.lse, self.ws_att, main)
         out_absorb(self.o_lat, w["w_uv"], w["w_o"], y, self.ws_out, main)
         return y
 

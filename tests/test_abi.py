@@ -83,6 +83,28 @@ def test_decode_plan_reports_splits_and_launches(lib):
     assert lib.mla_decode_plan(4, 48, 64, 0, None, None) == 2
 
 
+def test_prepare_validation_before_launch(lib):
+    """mla_decode_prepare checks its arguments and the workspace size on the host; a fixed
+    split needs no schedule, so the call returns at once. (Every call below returns before
+    anything is launched: the pointers are never dereferenced.)"""
+    from mla_latent_kv_13_gb300 import mla
+    f = lib.mla_decode_prepare
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    ws, sl, big = 256, 512, 1 << 40
+    assert f(None, 4, 128, 64, 0, ws, big, None) == 1
+    assert f(sl, 0, 128, 64, 0, ws, big, None) == 1
+    assert f(sl, 4, 48, 64, 0, ws, big, None) == 2
+    assert f(sl, 4, 128, 64, 300, ws, big, None) == 1
+    assert f(sl, 4, 128, 64, 0, 255, big, None) == 1
+    need = mla.decode_workspace_size(4096, 128, 32768, 0)
+    assert f(sl, 4096, 128, 32768, 0, ws, need - 1, None) == 3
+    # a fixed split: nothing to prepare, nothing launched
+    assert mla.decode_plan(4, 128, 64, 1)[0] == 1
+    assert f(sl, 4, 128, 64, 1, ws, 256, None) == 0
+
+
 def test_multi_query_validation_before_launch(lib):
     from mla_latent_kv_13_gb300 import mla
     # s_q * H rows must fit the 128 TMEM lanes; H itself a supported head count

@@ -255,3 +255,39 @@ def test_seqlen_beyond_max_seqlen_is_reported_and_clamped(mla, splits):
     ref, lref = _oracle(clamped)
     assert_close_rows(host_f64_from_bf16(out), ref)
     assert_lse(lse.cpu().numpy(), lref)
+
+
+@pytest.mark.parametrize("B", [100, 3])
+def test_prepared_schedule_gives_the_same_bits(mla, B):
+    """mla_decode_prepare once, then two mla_decode_attention_prepared calls (two layers
+    over the same lengths), the first with the schedule prepared on another stream: the
+    outputs equal mla_decode_attention's bit for bit, empty sequences included; B = 100
+    runs the balanced schedule, B = 3 a fixed split (the prepare call does nothing)."""
+    rng = np.random.default_rng(21 + B)
+    L = rng.integers(1, 600, size=B).astype(np.int32)
+    L[0] = 0
+    if B > 3:
+        L[57] = 0
+    d = _case(B, 128, tuple(int(x) for x in L), seed=22)
+    max_len = int(L.max())
+    assert (mla.decode_plan(B, 128, max_len, 0)[0] == 0) == (B == 100)
+    t = _to_dev(d)
+    ref_out, ref_lse, _ = mla.decode_attention(t["q_lat"], t["q_rope"], t["cache"], t["bt"],
+                                               t["seqlens"], max_len, d["scale"], 0)
+    ws = mla.alloc_workspace(mla.decode_workspace_size(B, 128, max_len, 0))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    mla.decode_prepare(t["seqlens"], B, 128, max_len, 0, ws, side)
+    done = torch.cuda.Event()
+    done.record(side)
+    torch.cuda.current_stream().wait_event(done)
+    for _ in range(2):
+        out = torch.full_like(ref_out, 7.0)
+        lse = torch.full_like(ref_lse, 7.0)
+        mla.decode_attention_prepared(t["q_lat"], t["q_rope"], t["cache"], t["bt"], t["seqlens"],
+                                      max_len, d["scale"], 0, out, lse, ws)
+        assert mla.check_device_status(ws) == 0
+        assert np.array_equal(host_bits(out), host_bits(ref_out))
+        assert np.array_equal(lse.cpu().numpy(), ref_lse.cpu().numpy())
+    o = host_f64_from_bf16(out)
+    assert np.all(o[L == 0] == 0) and np.all(np.isneginf(lse.cpu().numpy()[L == 0]))
