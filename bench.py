@@ -632,16 +632,18 @@ def run_gpu_prefill(args):
     print(json.dumps(line), flush=True)
 
 
-ATTN_CONFIGS = ("v3", "mixed", "long", "long_fp8")
-ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70, "long_fp8": None}
+ATTN_CONFIGS = ("v3", "mixed", "long", "long_fp8", "step_prepared")
+ATTN_GATE = {"v3": None, "mixed": 0.70, "long": 0.70, "long_fp8": None, "step_prepared": None}
 
 
 CONFIG_LAUNCHES = 200  # timed launches per attention workload in the `configs` object
 
 
 def time_attention_configs(pool, dev, launches: int, num_splits: int):
-    """mla_decode_attention alone on the v3-shaped, mixed-length and long-context workloads,
-    in this process after the step: their seqlens, block tables and queries follow the
+    """mla_decode_attention alone on the v3-shaped, mixed-length and long-context workloads
+    (the long one also over the FP8 cache), and mla_decode_attention_prepared on the
+    full-step shape with its schedule prepared once, in this process after the step: their
+    seqlens, block tables and queries follow the
     seeded recipe of each workload; their cache rows are the step's resident pool (the same
     N(0, 1) bf16 values; every block table indexes into it). Launches back to back on one
     stream between CUDA events; a workload whose cache is under twice the L2 size reads a
@@ -656,7 +658,10 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
     fp8_pool = None
     for name in ATTN_CONFIGS:
         fp8 = name.endswith("_fp8")
-        w = synth.WORKLOADS[name[:-4] if fp8 else name]
+        # step_prepared: the full-step shape as the layers of one decode step see it, the
+        # schedule prepared once (mla_decode_prepare) and every call skipping it
+        prepared = name.endswith("_prepared")
+        w = synth.WORKLOADS[name[:-4] if fp8 else (name[:-9] if prepared else name)]
         if fp8 and fp8_pool is None:  # the same pool as e4m3 codes with row exponents
             fp8_pool = mla.quantize_kv_fp8(pool)
         L = synth.draw_seqlens(w, 0)
@@ -686,8 +691,14 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
         out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H), dtype=torch.float32, device=dev)
 
+        if prepared:
+            mla.decode_prepare(Ld, B, H, max_len, num_splits, ws)
+
         def attend(i):
-            if fp8:
+            if prepared:
+                mla.decode_attention_prepared(q_lat, q_rope, pool, bts[i % rot], Ld, max_len,
+                                              synth.SCALE_192, num_splits, out, lse, ws)
+            elif fp8:
                 mla.decode_attention_fp8(q_lat, q_rope, fp8_pool[0], fp8_pool[1], bts[i % rot], Ld,
                                          max_len, synth.SCALE_192, num_splits, out, lse, ws)
             else:
@@ -721,7 +732,9 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
             "l2": (f"{rot} disjoint block ranges rotated" if rot > 1
                    else "cache larger than L2"),
             "algorithmic_bytes": byts,
-            "cache": "e4m3 codes + one power-of-two scale exponent per token" if fp8 else "bf16"}
+            "cache": "e4m3 codes + one power-of-two scale exponent per token" if fp8 else "bf16",
+            "schedule": ("prepared once, outside the timed launches (one decode step's layers "
+                         "share it)" if prepared else "computed by every call")}
         del ws, out, lse, bts, q_lat, q_rope
     return out_all
 
