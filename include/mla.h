@@ -114,7 +114,8 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
  * seqlens [B] int32 with 0 <= seqlens[b] <= max_seqlen (checked on the device: a length
  * outside that range is recorded as MLA_ERR_OUT_OF_RANGE and clamped into it, by every
  * work distribution alike),
- * out [B][H][512] bf16, lse [B][H] fp32.
+ * out [B][H][512] bf16 (32-byte aligned: its rows are written with 32-byte stores),
+ * lse [B][H] fp32.
  * scale must be finite and > 0 (1/sqrt(d_nope + d_rope) for DeepSeek-shaped heads).
  * H must be 16, 32, 64 or 128; 1 <= B <= 4096. num_splits: the number of equal token
  * ranges each sequence is cut into (1..256), merged exactly by their log-sum-exps
@@ -275,7 +276,7 @@ mla_status_t mla_decode_combine(const float *o_part, const float *lse_part, int 
  * (an empty range gives o_part = 0, lse_part = -inf). The ranks then exchange
  * (o_part, lse_part) -- an all-gather, outside this library -- and mla_decode_combine_ranks
  * merges them exactly. Arguments, checks, workspace and plans as mla_decode_attention;
- * o_part [B][H][512] fp32 (16-byte aligned), lse_part [B][H] fp32.
+ * o_part [B][H][512] fp32 (32-byte aligned), lse_part [B][H] fp32.
  */
 mla_status_t mla_decode_attention_partial(const mla_bf16_t *q_lat, const mla_bf16_t *q_rope,
                                           const mla_bf16_t *kv_cache, int num_blocks,

@@ -306,7 +306,7 @@ mla_status_t decode_validate(const void *q_lat, const void *q_rope, const void *
         return MLA_ERR_INVALID_ARG;
     if (!heads_ok(hq) || s_q * hq > 128) return MLA_ERR_UNSUPPORTED;
     if (!aligned(q_lat, 16) || !aligned(q_rope, 16) || !aligned(kv_cache, 16) ||
-        !aligned(out, 16) || !aligned(lse, 4))
+        !aligned(out, 32) || !aligned(lse, 4))
         return MLA_ERR_INVALID_ARG;
     return MLA_OK;
 }

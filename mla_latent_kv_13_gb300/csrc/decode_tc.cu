@@ -898,31 +898,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FP8 ? NTHREADS_FP8 :
                 tmem_ld32(tl + TM_O + 32 * c, r);
                 tmem_ld_wait();
                 if (row < H) {
+                    // each thread writes its row: 32-byte stores, so that every request
+                    // carries a whole sector (16-byte ones over 32 rows per warp instruction
+                    // made the L1-to-L2 requests, not the bytes, the limit)
                     if (!out32) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            p.out + ((size_t)b * H + row) * D_C + col0 + 32 * c);
+                        uint16_t *dst = p.out + ((size_t)b * H + row) * D_C + col0 + 32 * c;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(
-                                pack_bf16x2(__uint_as_float(r[8 * k + 0]) * inv,
-                                            __uint_as_float(r[8 * k + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv,
-                                            __uint_as_float(r[8 * k + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv,
-                                            __uint_as_float(r[8 * k + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv,
-                                            __uint_as_float(r[8 * k + 7]) * inv));
+                        for (int k = 0; k < 2; ++k) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                w[j] = pack_bf16x2(__uint_as_float(r[16 * k + 2 * j]) * inv,
+                                                   __uint_as_float(r[16 * k + 2 * j + 1]) * inv);
+                            st_global_v8(dst + 16 * k, w[0], w[1], w[2], w[3], w[4], w[5], w[6],
+                                         w[7]);
+                        }
                     } else {
                         // parts are kept in L2 (evict-last) until the merge that follows reads
                         // them: the tail part of a cut sequence is written early in the launch
                         const uint64_t pol = direct ? l2_policy_evict_normal() : l2_policy_evict_last();
                         float *dst = orow32 + 32 * c;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            st_global_v4_hint(dst + 4 * k, __uint_as_float(r[4 * k]) * inv,
-                                              __uint_as_float(r[4 * k + 1]) * inv,
-                                              __uint_as_float(r[4 * k + 2]) * inv,
-                                              __uint_as_float(r[4 * k + 3]) * inv, pol);
+                        for (int k = 0; k < 4; ++k)
+                            st_global_v8_hint(
+                                dst + 8 * k, __float_as_uint(__uint_as_float(r[8 * k]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 1]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 2]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 3]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 4]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 5]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 6]) * inv),
+                                __float_as_uint(__uint_as_float(r[8 * k + 7]) * inv), pol);
                     }
                 }
             }

@@ -194,6 +194,22 @@ __device__ __forceinline__ void st_global_v4_hint(void *ptr, float a, float b, f
                  "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol)
                  : "memory");
 }
+// 32-byte global stores (one full sector per thread; the address 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                             uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_v8_hint(void *ptr, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d, uint32_t e, uint32_t f, uint32_t g,
+                                                  uint32_t h, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(
+                     ptr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h), "l"(pol)
+                 : "memory");
+}
 // tma_load_2d with an L2 cache policy for the lines it reads
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *map, uint32_t bar,
                                                  int x, int y, uint64_t policy) {
