@@ -83,6 +83,30 @@ def test_decode_plan_reports_splits_and_launches(lib):
     assert lib.mla_decode_plan(4, 48, 64, 0, None, None) == 2
 
 
+def test_decode_output_alignment_checked_before_launch(lib):
+    """The attention output rows are written with 32-byte stores: an output pointer that is
+    16- but not 32-byte aligned is rejected on the host (nothing below is dereferenced or
+    launched: every call returns at its argument checks)."""
+    f = lib.mla_decode_attention
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    base = 1 << 20  # a 256-byte-aligned stand-in address
+    # two fixed splits need partial buffers that a 256-byte workspace cannot hold: a call that
+    # got past the alignment check would stop at the workspace check, still before any launch
+    args = lambda out: (base, base, base, 8, base, 2, base, 4, 128, 64, 0.07, 2, base,
+                        256, out, base, None)
+    assert f(*args(base)) == 3
+    assert f(*args(base + 16)) == 1
+    assert f(*args(base + 8)) == 1
+    g = lib.mla_decode_attention_partial
+    g.argtypes = f.argtypes
+    g.restype = ctypes.c_int
+    assert g(*args(base + 16)) == 1
+
+
 def test_prepare_validation_before_launch(lib):
     """mla_decode_prepare checks its arguments and the workspace size on the host; a fixed
     split needs no schedule, so the call returns at once. (Every call below returns before
