@@ -666,21 +666,29 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     if (launch_reduce_bf16(part, L.s1, 1, B, q_lora, cq, q_lora, 0, st) != cudaSuccess)
         return MLA_ERR_CUDA;
 
-    // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128])
-    g = GemmParams{};
-    g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
-    g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
-    g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
-    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+    if (B <= 128) {
+        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128]) and q_rope = RoPE(c_q W_QR^T)
+        // in one launch: both read c_q, and the rotation is the second product's epilogue
+        if (launch_gemm_tc_rope(cq, B, q_lora, w_uq, H * D_NOPE, qn, w_qr, H * D_ROPE, q_rope,
+                                pos, rope_theta, st, err) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    } else {
+        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128])
+        g = GemmParams{};
+        g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
+        g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
+        g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
 
-    // q_rope = RoPE(c_q W_QR^T)
-    g = GemmParams{};
-    g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
-    g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
-    g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
-    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
-    if (launch_qrope_finalize(part, L.s2, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
-        return MLA_ERR_CUDA;
+        // q_rope = RoPE(c_q W_QR^T)
+        g = GemmParams{};
+        g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
+        g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
+        g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_qrope_finalize(part, L.s2, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
 
     // q_lat[b, i] = q_nope[b, i] W_UK_i  (per-head product, W_UK_i stored [128][512])
     g = GemmParams{};

@@ -24,6 +24,8 @@
 // memory is sized to it, so products with little K per tile (the per-head absorptions)
 // run several CTAs per SM instead of one; products with many 256-wide tiles and short K
 // take two stages for the same reason.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -61,6 +63,12 @@ struct TcGemmArgs {
     uint16_t *c_bf16;
     long ldc, c_bstride;
     uint32_t *err;
+    // ROPE kernels: output tiles from column n_split on are a second product, with the
+    // weights of map_b2 and the output map_c2, and each pair of columns (2i, 2i+1) of a
+    // 64-column head rotated by the angle rope_pos[row] * rope.f[i] (decoupled RoPE)
+    int n_split;
+    const int32_t *rope_pos;
+    RopeFreqs rope;
 };
 
 // Store the box at (x, y) of a tensor map from this CTA's shared memory (bulk async-group;
@@ -91,11 +99,13 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
-template <bool NN, int BN>
+template <bool NN, int BN, bool ROPE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_c, TcGemmArgs g) {
+                   const __grid_constant__ CUtensorMap map_c,
+                   const __grid_constant__ CUtensorMap map_b2,
+                   const __grid_constant__ CUtensorMap map_c2, TcGemmArgs g) {
     constexpr int STAGE = Tile<BN>::STAGE;
     constexpr uint32_t TMEM_COLS = BN;
     constexpr uint32_t IDESC = idesc_bf16(BM, BN, false, NN);
@@ -106,6 +116,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+    // ROPE kernels: a tile of the second product reads map_b2 and writes map_c2 from its
+    // own column nb0
+    const bool second = ROPE && n0 >= g.n_split;
+    const int nb0 = second ? n0 - g.n_split : n0;
+    const CUtensorMap *const mbp = second ? &map_b2 : &map_b;
     const int batch = blockIdx.z / g.k_splits, split = blockIdx.z % g.k_splits;
     const int k_begin = split * g.k_per_split;
     const int k_end = min(g.K, k_begin + g.k_per_split);
@@ -131,8 +146,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&map_a);
-        tma_prefetch_map(&map_b);
-        if (g.tma_c) tma_prefetch_map(&map_c);
+        tma_prefetch_map(mbp);
+        if (g.tma_c) tma_prefetch_map(second ? &map_c2 : &map_c);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -151,7 +166,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int kb = 0; kb < min(nkb, ns); ++kb) {
                 const int k = k_begin + kb * BK;
                 if (!NN) {
-                    tma_prefetch_l2_2d(&map_b, batch * g.b_bx + k, batch * g.b_by + n0);
+                    tma_prefetch_l2_2d(mbp, batch * g.b_bx + k, batch * g.b_by + nb0);
                 } else {
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
@@ -168,7 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_arrive_expect_tx(full(s), STAGE);
                 tma_load_2d(sa, &map_a, full(s), batch * g.a_bx + k, m0);
                 if (!NN) {
-                    tma_load_2d(sbb, &map_b, full(s), batch * g.b_bx + k, batch * g.b_by + n0);
+                    tma_load_2d(sbb, mbp, full(s), batch * g.b_bx + k, batch * g.b_by + nb0);
                 } else {
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
@@ -210,6 +225,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int wq = warp & 3;
         const int m = m0 + wq * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        // ROPE: the row's 32 rotations, formed while the products run (positions come from
+        // the caller, so only after the dependency wait)
+        float rc[ROPE ? 32 : 1], rs[ROPE ? 32 : 1];
+        if constexpr (ROPE) {
+            if (second) {
+                grid_dependency_wait();
+                const int pm = m < g.M ? g.rope_pos[m] : 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) rope_cos_sin(pm, g.rope.f[i], rc[i], rs[i]);
+            }
+        }
         const bool ok =
             __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
         if (ok && g.tma_c == 2) {
@@ -243,28 +269,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // r * 128 bytes, its 16-byte chunks permuted by r % 8), written by one TMA store
             tc_fence_after();
             const int r = wq * 32 + lane;
+            if (second) {
+                if constexpr (ROPE) {
+                    // 64-column heads: chunk c holds the pairs 16 (c % 2) .. 16 (c % 2) + 15
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + 32 * c, v);
-                tmem_ld_wait();
-                const uint32_t rowp = sb + (c >> 1) * (BM * 128) + r * 128;
+                    for (int c2 = 0; c2 < BN / 64; ++c2) {
+                        const uint32_t rowp = sb + c2 * (BM * 128) + r * 128;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int ch = (c & 1) * 4 + k;
-                    st_shared_v4(rowp + ((ch ^ (r & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
-                                 pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
-                                 pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
-                                 pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t v[32];
+                            tmem_ld32(tl + 32 * (2 * c2 + hh), v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const int j = 4 * k + q;  // the pair's index in the chunk
+                                    const float x0 = __uint_as_float(v[2 * j]);
+                                    const float x1 = __uint_as_float(v[2 * j + 1]);
+                                    const float c_ = rc[16 * hh + j], s_ = rs[16 * hh + j];
+                                    w[q] = pack_bf16x2(x0 * c_ - x1 * s_, x0 * s_ + x1 * c_);
+                                }
+                                const int ch = hh * 4 + k;
+                                st_shared_v4(rowp + ((ch ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tl + 32 * c, v);
+                    tmem_ld_wait();
+                    const uint32_t rowp = sb + (c >> 1) * (BM * 128) + r * 128;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int ch = (c & 1) * 4 + k;
+                        st_shared_v4(rowp + ((ch ^ (r & 7)) << 4),
+                                     pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                                     pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                                     pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                                     pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
+                    }
                 }
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
             if (warp == 2 && lane == 0) {
-                for (int j = 0; j < BN / 64 && n0 + 64 * j < g.N; ++j)
-                    tma_store_2d(&map_c, sb + j * (BM * 128),
-                                 static_cast<int>(batch * g.c_bstride) + n0 + 64 * j, m0);
+                for (int j = 0; j < BN / 64 && n0 + 64 * j < g.N; ++j) {
+                    if (second)
+                        tma_store_2d(&map_c2, sb + j * (BM * 128), nb0 + 64 * j, m0);
+                    else
+                        tma_store_2d(&map_c, sb + j * (BM * 128),
+                                     static_cast<int>(batch * g.c_bstride) + n0 + 64 * j, m0);
+                }
                 bulk_commit();
                 bulk_wait_read_all();  // the boxes have left shared memory before exit
             }
@@ -366,9 +426,11 @@ bool map_3d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool NN, int BN>
+template <bool NN, int BN, bool ROPE = false>
 cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs g,
-                        const GemmParams &p, cudaStream_t stream) {
+                        const GemmParams &p, cudaStream_t stream,
+                        const CUtensorMap *mb2 = nullptr, const CUtensorMap *mc1 = nullptr,
+                        const CUtensorMap *mc2 = nullptr) {
     using T = Tile<BN>;
     dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM, p.batch * p.k_splits);
     const int kblocks = (p.k_per_split + BK - 1) / BK;
@@ -383,7 +445,10 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     // [M][ldc] matrix (x offsets multiples of 64 elements) and the ring holds the tile
     CUtensorMap mc = ma;
     g.tma_c = 0;
-    if (p.c_bf16 && !p.c_part && p.N % 64 == 0 && p.c_bstride % 64 == 0 && p.ldc % 8 == 0 &&
+    if (ROPE) {  // both outputs through the maps the caller made
+        mc = *mc1;
+        g.tma_c = 1;
+    } else if (p.c_bf16 && !p.c_part && p.N % 64 == 0 && p.c_bstride % 64 == 0 && p.ldc % 8 == 0 &&
         (reinterpret_cast<uintptr_t>(p.c_bf16) & 15) == 0 &&
         (long)(p.batch - 1) * p.c_bstride + p.N <= p.ldc && g.ns * T::STAGE >= BM * BN * 2 &&
         map_2d(&mc, p.c_bf16, (uint64_t)p.ldc, (uint64_t)p.M, (uint64_t)p.ldc, BM))
@@ -393,10 +458,18 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
              map_3d_f32(&mc, p.c_part, (uint64_t)p.N, (uint64_t)p.M,
                         (uint64_t)p.k_splits * p.batch))
         g.tma_c = 2;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN, ROPE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tc_kernel<NN, BN>, grid, dim3(NTHREADS), smem, stream, ma, mb, mc, g);
+    return launch_pdl(gemm_tc_kernel<NN, BN, ROPE>, grid, dim3(NTHREADS), smem, stream, ma, mb, mc,
+                      mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
+}
+
+RopeFreqs rope_freqs(float theta) {
+    RopeFreqs r;
+    for (int i = 0; i < D_ROPE / 2; ++i)
+        r.f[i] = std::pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(D_ROPE));
+    return r;
 }
 
 }  // namespace
@@ -445,6 +518,38 @@ cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, ui
                              : launch_tile<true, 128>(ma, mb, g, p, stream);
     return bn == 256 ? launch_tile<false, 256>(ma, mb, g, p, stream)
                      : launch_tile<false, 128>(ma, mb, g, p, stream);
+}
+
+// C1 = A B1^T and C2 = RoPE(A B2^T) in one launch: the output tiles of both products side by
+// side (TN, no k-split, 256 columns per tile), each 64-column head of C2 rotated pairwise by
+// pos[row] * theta^(-2i/64) in the epilogue. A [M][K], B1 [N1][K], B2 [N2][K], C1 [M][N1],
+// C2 [M][N2], all bf16; N1 and N2 multiples of 256, K of 64.
+cudaError_t launch_gemm_tc_rope(const uint16_t *A, int M, int K, const uint16_t *B1, int N1,
+                                uint16_t *C1, const uint16_t *B2, int N2, uint16_t *C2,
+                                const int32_t *pos, float theta, cudaStream_t stream,
+                                uint32_t *err) {
+    constexpr int BNR = 256;
+    if (N1 % BNR || N2 % BNR || K % BK || M > BM) return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.A = A; p.lda = K; p.B = B1; p.ldb = K;
+    p.M = M; p.N = N1 + N2; p.K = K; p.batch = 1;
+    p.k_splits = 1; p.k_per_split = K; p.c_bf16 = C1; p.ldc = N1;
+    TcGemmArgs g{};
+    g.M = M; g.N = N1 + N2; g.K = K; g.batch = 1;
+    g.k_splits = 1; g.k_per_split = K;
+    g.c_bf16 = C1; g.ldc = N1;
+    g.err = err;
+    g.n_split = N1;
+    g.rope_pos = pos;
+    g.rope = rope_freqs(theta);
+    CUtensorMap ma, mb1, mb2, mc1, mc2;
+    if (!map_2d(&ma, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, BM) ||
+        !map_2d(&mb1, B1, (uint64_t)K, (uint64_t)N1, (uint64_t)K, BNR) ||
+        !map_2d(&mb2, B2, (uint64_t)K, (uint64_t)N2, (uint64_t)K, BNR) ||
+        !map_2d(&mc1, C1, (uint64_t)N1, (uint64_t)M, (uint64_t)N1, BM) ||
+        !map_2d(&mc2, C2, (uint64_t)N2, (uint64_t)M, (uint64_t)N2, BM))
+        return cudaErrorInvalidValue;
+    return launch_tile<false, BNR, true>(ma, mb1, g, p, stream, &mb2, &mc1, &mc2);
 }
 
 }  // namespace mla

@@ -22,6 +22,12 @@ struct GemmParams {
 
 // tcgen05/TMA GEMM (one 128 x gemm_block_n(N, K) tile per CTA); err = workspace error word
 cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, uint32_t *err);
+// C1 = A B1^T and C2 = RoPE(A B2^T) (64-column heads rotated pairwise at pos[row]) in one
+// launch; bf16 everywhere, N1 and N2 multiples of 256, M <= 128
+cudaError_t launch_gemm_tc_rope(const uint16_t *A, int M, int K, const uint16_t *B1, int N1,
+                                uint16_t *C1, const uint16_t *B2, int N2, uint16_t *C2,
+                                const int32_t *pos, float theta, cudaStream_t stream,
+                                uint32_t *err);
 int gemm_block_n(int N, int K);  // output-tile width the GEMM uses (128 or 256)
 int gemm_block_n(int M, int N, int K);
 cudaError_t launch_reduce_bf16(const float *part, int S, int batch, int M, int N, uint16_t *C,
