@@ -291,3 +291,26 @@ def test_prepared_schedule_gives_the_same_bits(mla, B):
         assert np.array_equal(lse.cpu().numpy(), ref_lse.cpu().numpy())
     o = host_f64_from_bf16(out)
     assert np.all(o[L == 0] == 0) and np.all(np.isneginf(lse.cpu().numpy()[L == 0]))
+
+
+def test_balanced_schedule_without_cut_sequences(mla):
+    """152 equal sequences: every share of the balanced schedule holds exactly two, so no
+    sequence is cut and the merge kernel has no job (only its first CTA waits for the
+    attention kernel); the outputs still match the oracle, and a second call gives the same
+    bits."""
+    B, H, L = 152, 64, 640
+    d = _case(B, H, (L,) * B, seed=31)
+    assert mla.decode_plan(B, H, L, 0)[0] == 0
+    # with the 76 resident clusters of a GB300 the shares cut no sequence
+    assert mla.decode_schedule(np.full(B, L, dtype=np.int32), d["block_table"].shape[1], 76)[1] == 0
+    t = _to_dev(d)
+    out1, lse1, ws = mla.decode_attention(t["q_lat"], t["q_rope"], t["cache"], t["bt"],
+                                          t["seqlens"], L, d["scale"], 0)
+    assert mla.check_device_status(ws) == 0
+    out2, lse2, _ = mla.decode_attention(t["q_lat"], t["q_rope"], t["cache"], t["bt"],
+                                         t["seqlens"], L, d["scale"], 0, workspace=ws)
+    assert np.array_equal(host_bits(out1), host_bits(out2))
+    rows = [0, 1, 75, 76, 151]
+    ref, lref = _oracle(d, rows=rows)
+    assert_close_rows(host_f64_from_bf16(out1)[rows], ref)
+    assert_lse(lse1.cpu().numpy()[rows], lref)
