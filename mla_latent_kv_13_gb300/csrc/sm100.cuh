@@ -187,13 +187,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-// 16-byte global store with an L2 cache policy for the line it writes
-__device__ __forceinline__ void st_global_v4_hint(void *ptr, float a, float b, float c, float d,
-                                                  uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr),
-                 "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol)
-                 : "memory");
-}
 // 32-byte global stores (one full sector per thread; the address 32-byte aligned)
 __device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d, uint32_t e, uint32_t f, uint32_t g,
