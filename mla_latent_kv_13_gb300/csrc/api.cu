@@ -657,14 +657,22 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
 
     uint32_t *err = err_word(workspace);
 
-    // c_q = h W_DQ^T (bf16 intermediate)
+    // c_q = h W_DQ^T (bf16 intermediate): k-splits reduced inside their cluster when the
+    // device holds every tile's cluster at once, else partials and a finalize launch
     GemmParams g{};
     g.A = h; g.lda = d_model; g.B = w_dq; g.ldb = d_model;
     g.M = B; g.N = q_lora; g.K = d_model; g.batch = 1;
-    g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
-    if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
-    if (launch_reduce_bf16(part, L.s1, 1, B, q_lora, cq, q_lora, 0, st) != cudaSuccess)
-        return MLA_ERR_CUDA;
+    int per_c = 0;
+    const int s_c = gemm_cluster_plan(B, q_lora, d_model, &per_c);
+    if (s_c > 0) {
+        g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = cq; g.ldc = q_lora;
+        if (launch_gemm_tc_cluster(g, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+    } else {
+        g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_reduce_bf16(part, L.s1, 1, B, q_lora, cq, q_lora, 0, st) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
 
     if (B <= 128) {
         // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128]) and q_rope = RoPE(c_q W_QR^T)
@@ -751,10 +759,17 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     g.c_bf16 = ov; g.ldc = (long)H * D_V; g.c_bstride = D_V;
     if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
 
-    // y = o_v W_O^T
+    // y = o_v W_O^T (k-splits reduced inside their cluster when the device holds every
+    // tile's cluster at once, else partials and a finalize launch)
     g = GemmParams{};
     g.A = ov; g.lda = (long)H * D_V; g.B = w_o; g.ldb = (long)H * D_V;
     g.M = B; g.N = d_model; g.K = H * D_V; g.batch = 1;
+    int per_c = 0;
+    const int s_c = gemm_cluster_plan(B, d_model, H * D_V, &per_c);
+    if (s_c > 0) {
+        g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = y; g.ldc = d_model;
+        return cuda_status(launch_gemm_tc_cluster(g, st, err));
+    }
     g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
     if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
     return cuda_status(launch_reduce_bf16(part, L.s2, 1, B, d_model, y, d_model, 0, st));

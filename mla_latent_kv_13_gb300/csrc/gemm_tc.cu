@@ -9,9 +9,13 @@
 //   "NN": B stored [K][N] (W_UK, whose rows are per-head key dims).
 // Operands are addressed through 2-D tensor maps; a batch index (one per head for the
 // per-head products) shifts the A columns and the B rows by fixed amounts, so one map
-// serves every head. K is cut into k_splits ranges whose fp32 partials a finalize
-// kernel reduces: these products are weight-bandwidth bound (M = batch is small), and
-// the split keeps every SM streaming weights even when there are few output tiles.
+// serves every head. K is cut into k_splits ranges: these products are weight-bandwidth
+// bound (M = batch is small), and the split keeps every SM streaming weights even when
+// there are few output tiles. The ranges' fp32 partials are either written out for a
+// finalize kernel, or (CRED kernels) reduced inside the thread-block cluster that holds
+// all the k-splits of one output tile: each CTA stages its partial in its idle stage ring,
+// then sums a share of the tile's rows over every CTA's shared memory, in split order, and
+// writes them as bf16 -- no partials in global memory and no second launch.
 //
 // Roles (192 threads): warp 0 issues TMA (one lane), warp 1 owns TMEM and issues the
 // MMAs (the whole warp waits, one elected lane issues through predicated instructions),
@@ -93,13 +97,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// 16 bytes of fp32 from a shared::cluster address (this CTA's or a peer's shared memory)
+__device__ __forceinline__ float4 ld_cluster_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     uint64_t t0 = globaltimer_ns();
     while (!mbar_test(bar, parity))
         if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
-template <bool NN, int BN, bool ROPE>
+template <bool NN, int BN, bool ROPE, bool CRED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
@@ -127,7 +141,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nkb = (k_end - k_begin + BK - 1) / BK;
 
     const int ns = g.ns;
-    const int bar_off = ns * STAGE;
+    // CRED: the ring also holds the staged fp32 partial tile (BM x BN) once the products are done
+    const int bar_off = CRED ? max(ns * STAGE, BM * BN * 4) : ns * STAGE;
     const uint32_t bar = sb + bar_off;
     auto full = [&](int s) { return bar + 8u * s; };
     auto empty = [&](int s) { return bar + 8u * (ns + s); };
@@ -238,7 +253,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const bool ok =
             __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
-        if (ok && g.tma_c == 2) {
+        if constexpr (CRED) {
+            // this k-range's fp32 partial into the idle ring: row r at r * BN * 4 bytes, its
+            // 16-byte pieces permuted by r % 8 (8 consecutive rows, or 8 consecutive pieces of
+            // one row, then fall in distinct bank groups)
+            if (ok) {
+                tc_fence_after();
+                const int r = wq * 32 + lane;
+                const uint32_t rowp = sb + r * (BN * 4);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tl + 32 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        st_shared_v4(rowp + (((8 * c + k) ^ (r & 7)) << 4), v[4 * k], v[4 * k + 1],
+                                     v[4 * k + 2], v[4 * k + 3]);
+                }
+            }
+        } else if (ok && g.tma_c == 2) {
             // fp32 partials the same way: each 32-column chunk is one 128-byte-swizzled
             // 128 x 32 box of the [split x batch][M][N] partial array
             tc_fence_after();
@@ -368,6 +402,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     }
+    if constexpr (CRED) {
+        // The cluster is the k-splits of this output tile (cluster rank = split). Once every
+        // CTA has staged its partial, CTA r sums rows [r rp, r rp + rp) of the tile over the
+        // splits in order (the finalize kernel's order, so both paths give the same bits) and
+        // writes them bf16; the second barrier keeps every CTA's shared memory alive until
+        // the others have read it. Every thread reaches both barriers, whatever its waits gave.
+        __syncwarp();
+        cluster_sync();
+        const int S = g.k_splits;
+        const int mrows = min(BM, g.M - m0);
+        const int rp = (mrows + S - 1) / S;
+        const int r_begin = static_cast<int>(cluster_ctarank()) * rp;
+        const int r_end = min(mrows, r_begin + rp);
+        constexpr int U = BN / 4;  // 16-byte pieces of a staged row
+        uint32_t src[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) src[q] = q < S ? mapa(sb, static_cast<uint32_t>(q)) : 0u;
+        for (int e = tid; e < (r_end - r_begin) * U; e += NTHREADS) {
+            const int r = r_begin + e / U, j = e % U;
+            const int n = n0 + 4 * j;
+            if (n >= g.N) continue;
+            const uint32_t off = static_cast<uint32_t>(r * (BN * 4) + ((j ^ (r & 7)) << 4));
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < S) v[q] = ld_cluster_v4f(src[q] + off);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < S) {
+                    a0 += v[q].x;
+                    a1 += v[q].y;
+                    a2 += v[q].z;
+                    a3 += v[q].w;
+                }
+            *reinterpret_cast<uint2 *>(g.c_bf16 + (size_t)(m0 + r) * g.ldc + n) =
+                make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+        }
+        cluster_sync();
+    }
     if (tid == 0 && *abort_flag) flag_error(g.err, MLA_ERR_TIMEOUT, blockIdx.x);
     tc_fence_before();
     __syncthreads();
@@ -426,7 +500,13 @@ bool map_3d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool NN, int BN, bool ROPE = false>
+// shared memory of a CTA of gemm_tc_kernel<.., BN, .., CRED> with ns ring stages
+template <int BN, bool CRED> int tile_smem(int ns) {
+    const int ring = ns * Tile<BN>::STAGE;
+    return (CRED && ring < BM * BN * 4 ? BM * BN * 4 : ring) + SMEM_EXTRA;
+}
+
+template <bool NN, int BN, bool ROPE = false, bool CRED = false>
 cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs g,
                         const GemmParams &p, cudaStream_t stream,
                         const CUtensorMap *mb2 = nullptr, const CUtensorMap *mc1 = nullptr,
@@ -438,14 +518,16 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     // Many output tiles of a short product (the prefill up-projections: K = 512, thousands
     // of 128 x 256 tiles): two stages, so that two CTAs share an SM and one's epilogue
     // overlaps the other's loads and MMAs.
-    if (BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() && kblocks <= 16)
+    if (!CRED && BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() &&
+        kblocks <= 16)
         g.ns = g.ns < 2 ? g.ns : 2;
-    const int smem = g.ns * T::STAGE + SMEM_EXTRA;
+    const int smem = tile_smem<BN, CRED>(g.ns);
     // bf16 output through TMA stores when every batch's slice is a column range of one
     // [M][ldc] matrix (x offsets multiples of 64 elements) and the ring holds the tile
     CUtensorMap mc = ma;
     g.tma_c = 0;
-    if (ROPE) {  // both outputs through the maps the caller made
+    if (CRED) {  // the cluster's reduction writes C itself
+    } else if (ROPE) {  // both outputs through the maps the caller made
         mc = *mc1;
         g.tma_c = 1;
     } else if (p.c_bf16 && !p.c_part && p.N % 64 == 0 && p.c_bstride % 64 == 0 && p.ldc % 8 == 0 &&
@@ -458,11 +540,61 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
              map_3d_f32(&mc, p.c_part, (uint64_t)p.N, (uint64_t)p.M,
                         (uint64_t)p.k_splits * p.batch))
         g.tma_c = 2;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN, ROPE>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN, ROPE, CRED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tc_kernel<NN, BN, ROPE>, grid, dim3(NTHREADS), smem, stream, ma, mb, mc,
-                      mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
+    if (!CRED)
+        return launch_pdl(gemm_tc_kernel<NN, BN, ROPE, CRED>, grid, dim3(NTHREADS), smem, stream,
+                          ma, mb, mc, mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
+    // one cluster per output tile: its k-splits along z
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = static_cast<unsigned>(p.k_splits);
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, BN, ROPE, CRED>, ma, mb, mc,
+                              mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
+}
+
+// Clusters of `s` CTAs of gemm_tc_kernel<TN, BN, CRED> (s ring stages' worth of k-blocks
+// each at most) that the device holds at once; cached per (BN, s).
+template <int BN> int cluster_capacity(int s, int ns) {
+    static int cap[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    static int cap_ns[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    if (s < 2 || s > 8) return 0;
+    if (cap[s] > 0 && cap_ns[s] == ns) return cap[s];
+    auto kern = gemm_tc_kernel<false, BN, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<BN>::SMEM_TOTAL) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, s);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = tile_smem<BN, true>(ns);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(s);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 0) {
+        cudaGetLastError();  // a refused query leaves no sticky error behind
+        return 0;
+    }
+    cap[s] = n;
+    cap_ns[s] = ns;
+    return n;
 }
 
 RopeFreqs rope_freqs(float theta) {
@@ -484,6 +616,52 @@ int gemm_block_n(int M, int N, int K) {
     // short products (per-head W_UK, K = 128): half as many CTAs, A read half as often
     if (K <= 256 && N >= 512 && N % 256 == 0) return 256;
     return gemm_block_n(N, K);
+}
+
+// Cluster-reduced split-K for a TN product of one batch with bf16 output: the most k-splits
+// (2..8, at least two k-blocks each) whose clusters the device holds for every output tile
+// at once, with room to spare; 0 if no such split exists (the caller then writes partials
+// for a finalize kernel).
+int gemm_cluster_plan(int M, int N, int K, int *k_per_split) {
+    if (M < 1 || N < 4 || N % 4 || K < 2 * BK || K % BK) return 0;
+    const int bn = gemm_block_n(M, N, K);
+    const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM);
+    const int kblocks = K / BK;
+    for (int s = 8; s >= 2; --s) {
+        const int per = (kblocks + s - 1) / s;  // k-blocks per split
+        const int splits = (kblocks + per - 1) / per;
+        if (per < 2 || splits != s) continue;
+        const int nsmax = bn == 256 ? Tile<256>::NS : Tile<128>::NS;
+        const int ns = per < nsmax ? per : nsmax;  // the ring launch_tile gives it
+        const int cap = bn == 256 ? cluster_capacity<256>(s, ns) : cluster_capacity<128>(s, ns);
+        // a tenth of the clusters' room left free: clusters are placed only where a whole
+        // group of SMs is idle, and with every slot needed one SM still busy with the
+        // previous kernel sends a cluster into a second wave (5 splits of the 7168 x 16384
+        // output product, 28 clusters where the device holds 28, took 68 us; 4 splits 53)
+        if (tiles * 10 <= (long)cap * 9) {
+            *k_per_split = per * BK;
+            return s;
+        }
+    }
+    return 0;
+}
+
+cudaError_t launch_gemm_tc_cluster(const GemmParams &p, cudaStream_t stream, uint32_t *err) {
+    if (p.batch != 1 || !p.c_bf16 || p.c_part || p.k_splits < 2 || p.k_splits > 8 ||
+        p.N % 4 || p.ldc % 4 || (reinterpret_cast<uintptr_t>(p.c_bf16) & 7))
+        return cudaErrorInvalidValue;
+    TcGemmArgs g{};
+    g.M = p.M; g.N = p.N; g.K = p.K; g.batch = 1;
+    g.k_splits = p.k_splits; g.k_per_split = p.k_per_split;
+    g.c_bf16 = p.c_bf16; g.ldc = p.ldc;
+    g.err = err;
+    CUtensorMap ma, mb;
+    const int bn = gemm_block_n(p.M, p.N, p.K);
+    if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM) ||
+        !map_2d(&mb, p.B, (uint64_t)p.ldb, (uint64_t)p.N, (uint64_t)p.ldb, bn))
+        return cudaErrorInvalidValue;
+    return bn == 256 ? launch_tile<false, 256, false, true>(ma, mb, g, p, stream)
+                     : launch_tile<false, 128, false, true>(ma, mb, g, p, stream);
 }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column

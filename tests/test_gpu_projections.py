@@ -105,7 +105,11 @@ def _proj(B, dm, ql, H, seed):
                 pos=rng.integers(0, 9000, B).astype(np.int32))
 
 
+# W_DQ's k-splits reduced in their cluster: 8 splits over 4 tiles with ragged rows (100);
+# two row tiles (200), the second one 72 rows
 @pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
+                                           (100, 1024, 512, 32, None),
+                                           (200, 2048, 1536, 16, [0, 127, 128, 150, 199]),
                                            (128, 7168, 1536, 128, [0, 61, 127])])
 def test_absorb_q(mla, B, dm, ql, H, rows):
     p = _proj(B, dm, ql, H, 3)
@@ -119,7 +123,11 @@ def test_absorb_q(mla, B, dm, ql, H, rows):
     assert_close_rows(host_f64_from_bf16(q_rope)[rows], rr, "q_rope")
 
 
-@pytest.mark.parametrize("B,dm,H,rows", [(3, 256, 16, None), (128, 7168, 128, [1, 64, 100])])
+# W_O's k-splits reduced in their cluster: 128-column tiles with ragged rows (100), 256-column
+# tiles over two row tiles (200)
+@pytest.mark.parametrize("B,dm,H,rows", [(3, 256, 16, None), (100, 1024, 32, None),
+                                         (200, 7168, 64, [0, 127, 128, 199]),
+                                         (128, 7168, 128, [1, 64, 100])])
 def test_out_absorb(mla, B, dm, H, rows):
     p = _proj(B, dm, 64, H, 4)
     o_lat = bf16(np.random.default_rng(5).standard_normal((B, H, 512)) * 0.05)
