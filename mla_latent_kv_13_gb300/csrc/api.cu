@@ -175,6 +175,16 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
     g.A = h; g.lda = d_model; g.a_bstride = 0;
     g.B = w_dkr; g.ldb = d_model; g.b_bstride = 0;
     g.M = B; g.N = D_QK; g.K = d_model; g.batch = 1;
+    // the k-splits reduced inside their cluster, whose epilogue rotates k_rope and writes
+    // the rows into the cache, when the device holds every tile's cluster at once; else
+    // partials and a finalize launch
+    int per_c = 0;
+    const int s_c = gemm_cluster_plan(B, D_QK, d_model, &per_c);
+    if (s_c > 0) {
+        g.k_splits = s_c; g.k_per_split = per_c;
+        const ClusterAppend ap{pos, block_table, max_blocks, num_blocks, kv_cache, rope_theta};
+        return cuda_status(launch_gemm_tc_cluster(g, &ap, S(stream), err_word(workspace)));
+    }
     g.k_splits = splits; g.k_per_split = per;
     g.c_part = part;
     cudaError_t e = launch_gemm_tc(g, false, S(stream), err_word(workspace));
@@ -666,7 +676,7 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     const int s_c = gemm_cluster_plan(B, q_lora, d_model, &per_c);
     if (s_c > 0) {
         g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = cq; g.ldc = q_lora;
-        if (launch_gemm_tc_cluster(g, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_gemm_tc_cluster(g, nullptr, st, err) != cudaSuccess) return MLA_ERR_CUDA;
     } else {
         g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
         if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
@@ -768,7 +778,7 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     const int s_c = gemm_cluster_plan(B, d_model, H * D_V, &per_c);
     if (s_c > 0) {
         g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = y; g.ldc = d_model;
-        return cuda_status(launch_gemm_tc_cluster(g, st, err));
+        return cuda_status(launch_gemm_tc_cluster(g, nullptr, st, err));
     }
     g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
     if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;

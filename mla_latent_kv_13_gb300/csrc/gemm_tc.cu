@@ -72,7 +72,12 @@ struct TcGemmArgs {
     // 64-column head rotated by the angle rope_pos[row] * rope.f[i] (decoupled RoPE)
     int n_split;
     const int32_t *rope_pos;
-    RopeFreqs rope;
+    RopeFreqs rope;  // also the k_rope rotation of CRED = 2 kernels
+    // CRED = 2: positions, block table [M][ap_max_blocks] and the paged cache
+    // [ap_num_blocks * BLOCK][D_QK] the new rows go to
+    const int32_t *ap_pos, *ap_bt;
+    int ap_max_blocks, ap_num_blocks;
+    uint16_t *ap_cache;
 };
 
 // Store the box at (x, y) of a tensor map from this CTA's shared memory (bulk async-group;
@@ -113,7 +118,10 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > 200000000ull) return;
 }
 
-template <bool NN, int BN, bool ROPE, bool CRED>
+// CRED: 0 = no cluster reduction; 1 = reduced into bf16 C; 2 = reduced into the new latent
+// cache rows of append (row b of the product is sequence b's token at pos[b]: the k_rope
+// pairs rotated by that position, the row written into its block of the paged cache)
+template <bool NN, int BN, bool ROPE, int CRED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b,
@@ -142,7 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int ns = g.ns;
     // CRED: the ring also holds the staged fp32 partial tile (BM x BN) once the products are done
-    const int bar_off = CRED ? max(ns * STAGE, BM * BN * 4) : ns * STAGE;
+    const int bar_off = CRED != 0 ? max(ns * STAGE, BM * BN * 4) : ns * STAGE;
     const uint32_t bar = sb + bar_off;
     auto full = [&](int s) { return bar + 8u * s; };
     auto empty = [&](int s) { return bar + 8u * (ns + s); };
@@ -253,7 +261,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const bool ok =
             __all_sync(0xffffffffu, nkb > 0 && mbar_wait(done, 0, abort_flag, WAIT_NS));
-        if constexpr (CRED) {
+        if constexpr (CRED != 0) {
             // this k-range's fp32 partial into the idle ring: row r at r * BN * 4 bytes, its
             // 16-byte pieces permuted by r % 8 (8 consecutive rows, or 8 consecutive pieces of
             // one row, then fall in distinct bank groups)
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     }
-    if constexpr (CRED) {
+    if constexpr (CRED != 0) {
         // The cluster is the k-splits of this output tile (cluster rank = split). Once every
         // CTA has staged its partial, CTA r sums rows [r rp, r rp + rp) of the tile over the
         // splits in order (the finalize kernel's order, so both paths give the same bits) and
@@ -437,8 +445,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     a2 += v[q].z;
                     a3 += v[q].w;
                 }
-            *reinterpret_cast<uint2 *>(g.c_bf16 + (size_t)(m0 + r) * g.ldc + n) =
-                make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
+            uint16_t *dst;
+            if constexpr (CRED == 1) {
+                dst = g.c_bf16 + (size_t)(m0 + r) * g.ldc + n;
+            } else {
+                // a position or block outside the cache is an error: flagged once per row
+                // (first column piece of the first column tile) and the row dropped
+                const int b = m0 + r;
+                const int pp = g.ap_pos[b];
+                const int blk = pp >= 0 && pp < g.ap_max_blocks * BLOCK
+                                    ? g.ap_bt[(size_t)b * g.ap_max_blocks + pp / BLOCK]
+                                    : -1;
+                if (blk < 0 || blk >= g.ap_num_blocks) {
+                    if (j == 0 && n0 == 0) flag_error(g.err, MLA_ERR_OUT_OF_RANGE, b);
+                    continue;
+                }
+                if (n >= D_C) {
+                    rope_pair(a0, a1, pp, g.rope.f[(n - D_C) / 2]);
+                    rope_pair(a2, a3, pp, g.rope.f[(n - D_C) / 2 + 1]);
+                }
+                dst = g.ap_cache + ((size_t)blk * BLOCK + pp % BLOCK) * D_QK + n;
+            }
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
         }
         cluster_sync();
     }
@@ -501,12 +529,12 @@ bool map_3d_f32(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, 
 }
 
 // shared memory of a CTA of gemm_tc_kernel<.., BN, .., CRED> with ns ring stages
-template <int BN, bool CRED> int tile_smem(int ns) {
+template <int BN, int CRED> int tile_smem(int ns) {
     const int ring = ns * Tile<BN>::STAGE;
-    return (CRED && ring < BM * BN * 4 ? BM * BN * 4 : ring) + SMEM_EXTRA;
+    return (CRED != 0 && ring < BM * BN * 4 ? BM * BN * 4 : ring) + SMEM_EXTRA;
 }
 
-template <bool NN, int BN, bool ROPE = false, bool CRED = false>
+template <bool NN, int BN, bool ROPE = false, int CRED = 0>
 cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs g,
                         const GemmParams &p, cudaStream_t stream,
                         const CUtensorMap *mb2 = nullptr, const CUtensorMap *mc1 = nullptr,
@@ -518,7 +546,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     // Many output tiles of a short product (the prefill up-projections: K = 512, thousands
     // of 128 x 256 tiles): two stages, so that two CTAs share an SM and one's epilogue
     // overlaps the other's loads and MMAs.
-    if (!CRED && BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() &&
+    if (CRED == 0 && BN == 256 && (long)grid.x * grid.y * grid.z >= 4L * device_sm_count() &&
         kblocks <= 16)
         g.ns = g.ns < 2 ? g.ns : 2;
     const int smem = tile_smem<BN, CRED>(g.ns);
@@ -526,7 +554,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     // [M][ldc] matrix (x offsets multiples of 64 elements) and the ring holds the tile
     CUtensorMap mc = ma;
     g.tma_c = 0;
-    if (CRED) {  // the cluster's reduction writes C itself
+    if (CRED != 0) {  // the cluster's reduction writes the output itself
     } else if (ROPE) {  // both outputs through the maps the caller made
         mc = *mc1;
         g.tma_c = 1;
@@ -543,7 +571,7 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<NN, BN, ROPE, CRED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    if (!CRED)
+    if (CRED == 0)
         return launch_pdl(gemm_tc_kernel<NN, BN, ROPE, CRED>, grid, dim3(NTHREADS), smem, stream,
                           ma, mb, mc, mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
     // one cluster per output tile: its k-splits along z
@@ -572,14 +600,14 @@ template <int BN> int cluster_capacity(int s, int ns) {
     static int cap_ns[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     if (s < 2 || s > 8) return 0;
     if (cap[s] > 0 && cap_ns[s] == ns) return cap[s];
-    auto kern = gemm_tc_kernel<false, BN, false, true>;
+    auto kern = gemm_tc_kernel<false, BN, false, 1>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Tile<BN>::SMEM_TOTAL) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, s);
     cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = tile_smem<BN, true>(ns);
+    cfg.dynamicSmemBytes = tile_smem<BN, 1>(ns);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
@@ -646,9 +674,14 @@ int gemm_cluster_plan(int M, int N, int K, int *k_per_split) {
     return 0;
 }
 
-cudaError_t launch_gemm_tc_cluster(const GemmParams &p, cudaStream_t stream, uint32_t *err) {
-    if (p.batch != 1 || !p.c_bf16 || p.c_part || p.k_splits < 2 || p.k_splits > 8 ||
-        p.N % 4 || p.ldc % 4 || (reinterpret_cast<uintptr_t>(p.c_bf16) & 7))
+cudaError_t launch_gemm_tc_cluster(const GemmParams &p, const ClusterAppend *ap,
+                                   cudaStream_t stream, uint32_t *err) {
+    if (p.batch != 1 || p.c_part || p.k_splits < 2 || p.k_splits > 8 || p.N % 4)
+        return cudaErrorInvalidValue;
+    if (!ap && (!p.c_bf16 || p.ldc % 4 || (reinterpret_cast<uintptr_t>(p.c_bf16) & 7)))
+        return cudaErrorInvalidValue;
+    if (ap && (p.N != D_QK || !ap->pos || !ap->block_table || !ap->cache ||
+               (reinterpret_cast<uintptr_t>(ap->cache) & 7)))
         return cudaErrorInvalidValue;
     TcGemmArgs g{};
     g.M = p.M; g.N = p.N; g.K = p.K; g.batch = 1;
@@ -660,8 +693,15 @@ cudaError_t launch_gemm_tc_cluster(const GemmParams &p, cudaStream_t stream, uin
     if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM) ||
         !map_2d(&mb, p.B, (uint64_t)p.ldb, (uint64_t)p.N, (uint64_t)p.ldb, bn))
         return cudaErrorInvalidValue;
-    return bn == 256 ? launch_tile<false, 256, false, true>(ma, mb, g, p, stream)
-                     : launch_tile<false, 128, false, true>(ma, mb, g, p, stream);
+    if (ap) {
+        if (bn != 128) return cudaErrorInvalidValue;
+        g.ap_pos = ap->pos; g.ap_bt = ap->block_table; g.ap_max_blocks = ap->max_blocks;
+        g.ap_num_blocks = ap->num_blocks; g.ap_cache = ap->cache;
+        g.rope = rope_freqs(ap->theta);
+        return launch_tile<false, 128, false, 2>(ma, mb, g, p, stream);
+    }
+    return bn == 256 ? launch_tile<false, 256, false, 1>(ma, mb, g, p, stream)
+                     : launch_tile<false, 128, false, 1>(ma, mb, g, p, stream);
 }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column

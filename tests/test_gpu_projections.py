@@ -32,9 +32,11 @@ def _append_both(mla, h, w, pos, bt, cache):
     return host_bits(c_gpu), c_ref, st
 
 
-def test_append_exact_on_integer_inputs(mla):
+# d_model 128: split-K partials and a finalize launch; 512 and 1024: the k-splits reduced in
+# their cluster, rows written by its epilogue (1024 with 200 sequences: two row tiles)
+@pytest.mark.parametrize("B,dm", [(7, 128), (7, 512), (200, 1024)])
+def test_append_exact_on_integer_inputs(mla, B, dm):
     rng = np.random.default_rng(0)
-    B, dm = 7, 128
     h = bf16(rng.integers(-1, 2, (B, dm)))
     w = bf16(rng.integers(-1, 2, (576, dm)))
     bt = np.arange(B * 2, dtype=np.int32).reshape(B, 2)[:, ::-1].copy()
@@ -44,7 +46,7 @@ def test_append_exact_on_integer_inputs(mla):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("B,dm", [(5, 256), (128, 7168)])
+@pytest.mark.parametrize("B,dm", [(5, 256), (200, 1024), (128, 7168)])
 def test_append_real_inputs_within_fp32_summation_bound(mla, B, dm):
     rng = np.random.default_rng(1)
     h = bf16(rng.standard_normal((B, dm)))
@@ -79,9 +81,10 @@ def test_append_real_inputs_within_fp32_summation_bound(mla, B, dm):
     assert np.array_equal(got[mask], ref[mask])  # nothing else written
 
 
-def test_append_out_of_range_is_flagged_and_dropped(mla):
+@pytest.mark.parametrize("dm", [64, 256])  # finalize launch / cluster epilogue
+def test_append_out_of_range_is_flagged_and_dropped(mla, dm):
     rng = np.random.default_rng(2)
-    B, dm = 3, 64
+    B = 3
     h = bf16(rng.standard_normal((B, dm)))
     w = bf16(rng.standard_normal((576, dm)))
     bt = np.array([[0], [1], [99]], np.int32)      # sequence 2 points outside the pool
