@@ -740,12 +740,13 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
 
 
 def step_launches(step) -> int:
-    """Kernels one DecodeStep launches: append 2; absorb_q 4 (W_DQ, its split reduction, W_UQ
-    with W_QR and RoPE in one launch, W_UK; 6 above 128 sequences, where W_QR and RoPE are
-    separate launches); decode 1-3 (the library's own plan: + merge, + schedule); out 3."""
+    """Kernels one DecodeStep launches, by the library's own plans for these shapes on this
+    device: append 1-2, absorb_q 3-6, out_absorb 2-3 (a split-K product reduced inside its
+    clusters is one launch, else two), decode 1-3 (+ merge, + schedule)."""
     from mla_latent_kv_13_gb300 import mla
     _, decode = mla.decode_plan(step.B, step.H, step.max_seqlen, step.num_splits)
-    return 2 + (4 if step.B <= 128 else 6) + decode + 3
+    append, absorb, out = mla.projection_launches(step.B, step.dm, step.ql, step.H)
+    return append + absorb + decode + out
 
 
 DECODE_SOURCES = ("decode_tc.cu", "sm100.cuh", "common.cuh")

@@ -409,6 +409,21 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
                             const mla_bf16_t *w_o, int d_model, void *workspace, size_t ws_bytes,
                             mla_bf16_t *y, mla_stream_t stream);
 
+/*
+ * The kernels one call of each projection entry point launches for these shapes on the
+ * current device (no counterpart on the pages: a query of this library's launch plan).
+ * A split-K product whose k-splits fit the device as thread-block clusters (every output
+ * tile's cluster resident at once) reduces them inside the cluster, in one launch;
+ * otherwise it writes fp32 partials and a second launch sums them. *append = 1 or 2
+ * (mla_append_kv; mla_append_kv_fp8 always 2), *absorb_q = 3..6 (W_DQ 1 or 2; W_UQ, W_QR
+ * and the RoPE 1 for B <= 128, else 3; W_UK 1), *out_absorb = 2 or 3 (W_UV 1; W_O 1 or
+ * 2). With no visible device the partial-writing plan is reported. Any output pointer may
+ * be null. Same argument rules as the entry points (MLA_ERR_INVALID_ARG, or
+ * MLA_ERR_UNSUPPORTED for H).
+ */
+mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int *append,
+                                     int *absorb_q, int *out_absorb);
+
 /* ------------------------------------------------------- device status */
 
 /* Zero the workspace's error word (asynchronous on `stream`). */

@@ -785,6 +785,20 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     return cuda_status(launch_reduce_bf16(part, L.s2, 1, B, d_model, y, d_model, 0, st));
 }
 
+mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int *append,
+                                     int *absorb_q, int *out_absorb) {
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 || q_lora % 64)
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    int per = 0;
+    if (append) *append = gemm_cluster_plan(B, D_QK, d_model, &per) > 0 ? 1 : 2;
+    if (absorb_q)
+        *absorb_q = (gemm_cluster_plan(B, q_lora, d_model, &per) > 0 ? 1 : 2) +
+                    (B <= 128 ? 1 : 3) + 1;
+    if (out_absorb) *out_absorb = 1 + (gemm_cluster_plan(B, d_model, H * D_V, &per) > 0 ? 1 : 2);
+    return MLA_OK;
+}
+
 // -------------------------------------------------------------- status
 
 mla_status_t mla_clear_device_status(void *workspace, mla_stream_t stream) {

@@ -602,8 +602,10 @@ template <int BN> int cluster_capacity(int s, int ns) {
     if (cap[s] > 0 && cap_ns[s] == ns) return cap[s];
     auto kern = gemm_tc_kernel<false, BN, false, 1>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<BN>::SMEM_TOTAL) != cudaSuccess)
+                             Tile<BN>::SMEM_TOTAL) != cudaSuccess) {
+        cudaGetLastError();  // no device: nothing left behind for the next error check
         return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, s);
     cfg.blockDim = dim3(NTHREADS);

@@ -48,6 +48,8 @@ _SIGS = {
     "mla_append_kv": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _f, _vp, _sz, _vp], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _szp], _i),
     "mla_decode_plan": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
+    "mla_projection_launches": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i),
+                                 ctypes.POINTER(_i)], _i),
     "mla_decode_schedule": ([_vp, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
                             _i),
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
@@ -153,6 +155,17 @@ def decode_plan(B, H, max_seqlen, num_splits=0):
     if rc != 0:
         raise MLAError(rc, "mla_decode_plan")
     return s.value, n.value
+
+
+def projection_launches(B, d_model, q_lora, H):
+    """(append, absorb_q, out_absorb): the kernels one call of each launches for these
+    shapes on the current device."""
+    a, q, o = _i(0), _i(0), _i(0)
+    rc = _lib.mla_projection_launches(B, d_model, q_lora, H, ctypes.byref(a), ctypes.byref(q),
+                                      ctypes.byref(o))
+    if rc != 0:
+        raise MLAError(rc, "mla_projection_launches")
+    return a.value, q.value, o.value
 
 
 def decode_schedule(seqlens, max_blocks, clusters):

@@ -139,3 +139,12 @@ def test_out_absorb(mla, B, dm, H, rows):
     rows = list(range(B)) if rows is None else rows
     ref = oracle.out_absorb(synth.bf16_bits_to_f64(o_lat)[rows], p["w_uv"], p["w_o"])
     assert_close_rows(host_f64_from_bf16(y)[rows], ref, "y")
+
+
+def test_projection_launches_on_device(mla):
+    """On a full-size part (148 or more SMs) the headline shapes' split-K products all fit as
+    clusters: append, W_DQ and W_O each one launch (append 1, absorb_q 3, out_absorb 2)."""
+    import torch
+    if torch.cuda.get_device_properties(0).multi_processor_count < 148:
+        pytest.skip("a smaller part may plan partials")
+    assert mla.projection_launches(128, 7168, 1536, 128) == (1, 3, 2)
