@@ -178,12 +178,12 @@ mla_status_t mla_append_kv(const mla_bf16_t *h, int B, int d_model, const mla_bf
     // the k-splits reduced inside their cluster, whose epilogue rotates k_rope and writes
     // the rows into the cache, when the device holds every tile's cluster at once; else
     // partials and a finalize launch
-    int per_c = 0;
-    const int s_c = gemm_cluster_plan(B, D_QK, d_model, &per_c);
+    int per_c = 0, bn_c = 0;
+    const int s_c = gemm_cluster_plan(B, D_QK, d_model, &per_c, &bn_c);
     if (s_c > 0) {
         g.k_splits = s_c; g.k_per_split = per_c;
         const ClusterAppend ap{pos, block_table, max_blocks, num_blocks, kv_cache, rope_theta};
-        return cuda_status(launch_gemm_tc_cluster(g, &ap, S(stream), err_word(workspace)));
+        return cuda_status(launch_gemm_tc_cluster(g, bn_c, &ap, S(stream), err_word(workspace)));
     }
     g.k_splits = splits; g.k_per_split = per;
     g.c_part = part;
@@ -672,11 +672,11 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
     GemmParams g{};
     g.A = h; g.lda = d_model; g.B = w_dq; g.ldb = d_model;
     g.M = B; g.N = q_lora; g.K = d_model; g.batch = 1;
-    int per_c = 0;
-    const int s_c = gemm_cluster_plan(B, q_lora, d_model, &per_c);
+    int per_c = 0, bn_c = 0;
+    const int s_c = gemm_cluster_plan(B, q_lora, d_model, &per_c, &bn_c);
     if (s_c > 0) {
         g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = cq; g.ldc = q_lora;
-        if (launch_gemm_tc_cluster(g, nullptr, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_gemm_tc_cluster(g, bn_c, nullptr, st, err) != cudaSuccess) return MLA_ERR_CUDA;
     } else {
         g.k_splits = L.s1; g.k_per_split = L.per1; g.c_part = part;
         if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
@@ -774,11 +774,11 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
     g = GemmParams{};
     g.A = ov; g.lda = (long)H * D_V; g.B = w_o; g.ldb = (long)H * D_V;
     g.M = B; g.N = d_model; g.K = H * D_V; g.batch = 1;
-    int per_c = 0;
-    const int s_c = gemm_cluster_plan(B, d_model, H * D_V, &per_c);
+    int per_c = 0, bn_c = 0;
+    const int s_c = gemm_cluster_plan(B, d_model, H * D_V, &per_c, &bn_c);
     if (s_c > 0) {
         g.k_splits = s_c; g.k_per_split = per_c; g.c_bf16 = y; g.ldc = d_model;
-        return cuda_status(launch_gemm_tc_cluster(g, nullptr, st, err));
+        return cuda_status(launch_gemm_tc_cluster(g, bn_c, nullptr, st, err));
     }
     g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
     if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
@@ -791,11 +791,11 @@ mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int 
         return MLA_ERR_INVALID_ARG;
     if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
     int per = 0;
-    if (append) *append = gemm_cluster_plan(B, D_QK, d_model, &per) > 0 ? 1 : 2;
+    if (append) *append = gemm_cluster_plan(B, D_QK, d_model, &per, nullptr) > 0 ? 1 : 2;
     if (absorb_q)
-        *absorb_q = (gemm_cluster_plan(B, q_lora, d_model, &per) > 0 ? 1 : 2) +
+        *absorb_q = (gemm_cluster_plan(B, q_lora, d_model, &per, nullptr) > 0 ? 1 : 2) +
                     (B <= 128 ? 1 : 3) + 1;
-    if (out_absorb) *out_absorb = 1 + (gemm_cluster_plan(B, d_model, H * D_V, &per) > 0 ? 1 : 2);
+    if (out_absorb) *out_absorb = 1 + (gemm_cluster_plan(B, d_model, H * D_V, &per, nullptr) > 0 ? 1 : 2);
     return MLA_OK;
 }
 

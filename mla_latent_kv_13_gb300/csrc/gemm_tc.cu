@@ -48,9 +48,9 @@ constexpr int NTHREADS = 192;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
 template <int BN> struct Tile {
-    static constexpr int TILE_B = BN * BK * 2;           // 16 or 32 KB
+    static constexpr int TILE_B = BN * BK * 2;           // 16, 28 or 32 KB
     static constexpr int STAGE = TILE_A + TILE_B;
-    static constexpr int NS = BN == 128 ? 6 : 4;         // stages at most
+    static constexpr int NS = BN == 128 ? 6 : (BN == 224 ? 5 : 4);  // stages at most
     static constexpr int SMEM_TOTAL = NS * STAGE + SMEM_EXTRA;
     static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap map_b2,
                    const __grid_constant__ CUtensorMap map_c2, TcGemmArgs g) {
     constexpr int STAGE = Tile<BN>::STAGE;
-    constexpr uint32_t TMEM_COLS = BN;
+    constexpr uint32_t TMEM_COLS = BN <= 128 ? 128 : 256;  // a power of two
     constexpr uint32_t IDESC = idesc_bf16(BM, BN, false, NN);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -648,35 +648,53 @@ int gemm_block_n(int M, int N, int K) {
     return gemm_block_n(N, K);
 }
 
-// Cluster-reduced split-K for a TN product of one batch with bf16 output: the most k-splits
-// (2..8, at least two k-blocks each) whose clusters the device holds for every output tile
-// at once, with room to spare; 0 if no such split exists (the caller then writes partials
-// for a finalize kernel).
-int gemm_cluster_plan(int M, int N, int K, int *k_per_split) {
+// Cluster-reduced split-K for a TN product of one batch with bf16 output: the tile width and
+// the most k-splits (2..8, at least two k-blocks each) whose clusters the device holds for
+// every output tile at once, with room to spare, taking the width that runs the most CTAs;
+// 0 if no such split exists (the caller then writes partials for a finalize kernel).
+int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n) {
     if (M < 1 || N < 4 || N % 4 || K < 2 * BK || K % BK) return 0;
-    const int bn = gemm_block_n(M, N, K);
-    const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM);
     const int kblocks = K / BK;
-    for (int s = 8; s >= 2; --s) {
-        const int per = (kblocks + s - 1) / s;  // k-blocks per split
-        const int splits = (kblocks + per - 1) / per;
-        if (per < 2 || splits != s) continue;
-        const int nsmax = bn == 256 ? Tile<256>::NS : Tile<128>::NS;
-        const int ns = per < nsmax ? per : nsmax;  // the ring launch_tile gives it
-        const int cap = bn == 256 ? cluster_capacity<256>(s, ns) : cluster_capacity<128>(s, ns);
-        // a tenth of the clusters' room left free: clusters are placed only where a whole
-        // group of SMs is idle, and with every slot needed one SM still busy with the
-        // previous kernel sends a cluster into a second wave (5 splits of the 7168 x 16384
-        // output product, 28 clusters where the device holds 28, took 68 us; 4 splits 53)
-        if (tiles * 10 <= (long)cap * 9) {
-            *k_per_split = per * BK;
-            return s;
+    // tile widths: the product's own, and 224 in place of 256 when it divides N (more tiles
+    // for the same clusters: the 7168-wide output projection as 32 tiles instead of 28)
+    int widths[2] = {gemm_block_n(M, N, K), 0};
+    if (widths[0] == 256 && N % 224 == 0) widths[1] = 224;
+    int best_s = 0, best_per = 0, best_bn = 0;
+    long best_ctas = 0;
+    for (int w = 0; w < 2 && widths[w]; ++w) {
+        const int bn = widths[w];
+        const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM);
+        for (int s = 8; s >= 2; --s) {
+            const int per = (kblocks + s - 1) / s;  // k-blocks per split
+            const int splits = (kblocks + per - 1) / per;
+            if (per < 2 || splits != s) continue;
+            const int nsmax = bn == 128 ? Tile<128>::NS : (bn == 224 ? Tile<224>::NS : Tile<256>::NS);
+            const int ns = per < nsmax ? per : nsmax;  // the ring launch_tile gives it
+            const int cap = bn == 128   ? cluster_capacity<128>(s, ns)
+                            : bn == 224 ? cluster_capacity<224>(s, ns)
+                                        : cluster_capacity<256>(s, ns);
+            // a tenth of the clusters' room left free: clusters are placed only where a whole
+            // group of SMs is idle, and with every slot needed one SM still busy with the
+            // previous kernel sends a cluster into a second wave (5 splits of the 7168 x 16384
+            // output product, 28 clusters where the device holds 28, took 68 us; 4 splits 53)
+            if (tiles * 10 <= (long)cap * 9) {
+                if (tiles * s > best_ctas) {
+                    best_ctas = tiles * s;
+                    best_s = s;
+                    best_per = per;
+                    best_bn = bn;
+                }
+                break;  // fewer splits of this width only lose CTAs
+            }
         }
     }
-    return 0;
+    if (best_s == 0) return 0;
+    *k_per_split = best_per * BK;
+    if (block_n) *block_n = best_bn;
+    return best_s;
 }
 
-cudaError_t launch_gemm_tc_cluster(const GemmParams &p, const ClusterAppend *ap,
+cudaError_t launch_gemm_tc_cluster(const GemmParams &p, int bn, const ClusterAppend *ap,
                                    cudaStream_t stream, uint32_t *err) {
     if (p.batch != 1 || p.c_part || p.k_splits < 2 || p.k_splits > 8 || p.N % 4)
         return cudaErrorInvalidValue;
@@ -690,8 +708,8 @@ cudaError_t launch_gemm_tc_cluster(const GemmParams &p, const ClusterAppend *ap,
     g.k_splits = p.k_splits; g.k_per_split = p.k_per_split;
     g.c_bf16 = p.c_bf16; g.ldc = p.ldc;
     g.err = err;
+    if (bn != 128 && bn != 224 && bn != 256) return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
-    const int bn = gemm_block_n(p.M, p.N, p.K);
     if (!map_2d(&ma, p.A, (uint64_t)p.lda, (uint64_t)p.M, (uint64_t)p.lda, BM) ||
         !map_2d(&mb, p.B, (uint64_t)p.ldb, (uint64_t)p.N, (uint64_t)p.ldb, bn))
         return cudaErrorInvalidValue;
@@ -702,8 +720,9 @@ cudaError_t launch_gemm_tc_cluster(const GemmParams &p, const ClusterAppend *ap,
         g.rope = rope_freqs(ap->theta);
         return launch_tile<false, 128, false, 2>(ma, mb, g, p, stream);
     }
-    return bn == 256 ? launch_tile<false, 256, false, 1>(ma, mb, g, p, stream)
-                     : launch_tile<false, 128, false, 1>(ma, mb, g, p, stream);
+    return bn == 256   ? launch_tile<false, 256, false, 1>(ma, mb, g, p, stream)
+           : bn == 224 ? launch_tile<false, 224, false, 1>(ma, mb, g, p, stream)
+                       : launch_tile<false, 128, false, 1>(ma, mb, g, p, stream);
 }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column

@@ -25,7 +25,8 @@ cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, ui
 // Split-K whose k-splits of an output tile run as one thread-block cluster and reduce
 // through its shared memory into bf16 C (TN, batch 1): gemm_cluster_plan gives the splits
 // (and the K per split) for this shape on this device, 0 when none fits every tile in one
-// wave; launch_gemm_tc_cluster takes them in p.k_splits / p.k_per_split, p.c_part null.
+// wave, and the output-tile width (128, 224 or 256); launch_gemm_tc_cluster takes them in
+// p.k_splits / p.k_per_split and block_n, p.c_part null.
 // With `ap`, the product is append's h W_DKR^T (N = 576): row b is sequence b's new latent
 // row, its k_rope pairs rotated at pos[b], written into the paged cache (C unused).
 struct ClusterAppend {
@@ -34,8 +35,8 @@ struct ClusterAppend {
     uint16_t *cache;
     float theta;
 };
-int gemm_cluster_plan(int M, int N, int K, int *k_per_split);
-cudaError_t launch_gemm_tc_cluster(const GemmParams &p, const ClusterAppend *ap,
+int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n);
+cudaError_t launch_gemm_tc_cluster(const GemmParams &p, int block_n, const ClusterAppend *ap,
                                    cudaStream_t stream, uint32_t *err);
 // C1 = A B1^T and C2 = RoPE(A B2^T) (64-column heads rotated pairwise at pos[row]) in one
 // launch; bf16 everywhere, N1 and N2 multiples of 256, M <= 128
