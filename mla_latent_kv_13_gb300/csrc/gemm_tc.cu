@@ -48,9 +48,9 @@ constexpr int NTHREADS = 192;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
 template <int BN> struct Tile {
-    static constexpr int TILE_B = BN * BK * 2;           // 16, 28 or 32 KB
+    static constexpr int TILE_B = BN * BK * 2;           // 16 to 32 KB
     static constexpr int STAGE = TILE_A + TILE_B;
-    static constexpr int NS = BN == 128 ? 6 : (BN == 224 ? 5 : 4);  // stages at most
+    static constexpr int NS = BN == 128 ? 6 : (BN == 256 ? 4 : 5);  // stages at most
     static constexpr int SMEM_TOTAL = NS * STAGE + SMEM_EXTRA;
     static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
@@ -67,10 +67,10 @@ struct TcGemmArgs {
     uint16_t *c_bf16;
     long ldc, c_bstride;
     uint32_t *err;
-    // ROPE kernels: output tiles from column n_split on are a second product, with the
-    // weights of map_b2 and the output map_c2, and each pair of columns (2i, 2i+1) of a
-    // 64-column head rotated by the angle rope_pos[row] * rope.f[i] (decoupled RoPE)
-    int n_split;
+    // ROPE kernels: column tiles t1 and up are a second product, with the weights of map_b2
+    // and the output map_c2, and each pair of columns (2i, 2i+1) of a 64-column head rotated
+    // by the angle rope_pos[row] * rope.f[i] (decoupled RoPE); n1, n2 = the products' widths
+    int t1, n1, n2;
     const int32_t *rope_pos;
     RopeFreqs rope;  // also the k_rope rotation of CRED = 2 kernels
     // CRED = 2: positions, block table [M][ap_max_blocks] and the paged cache
@@ -139,9 +139,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
     // ROPE kernels: a tile of the second product reads map_b2 and writes map_c2 from its
-    // own column nb0
-    const bool second = ROPE && n0 >= g.n_split;
-    const int nb0 = second ? n0 - g.n_split : n0;
+    // own column nb0 (each product's last tile may be ragged)
+    const bool second = ROPE && static_cast<int>(blockIdx.x) >= g.t1;
+    const int nb0 = second ? (static_cast<int>(blockIdx.x) - g.t1) * BN : n0;
     const CUtensorMap *const mbp = second ? &map_b2 : &map_b;
     const int batch = blockIdx.z / g.k_splits, split = blockIdx.z % g.k_splits;
     const int k_begin = split * g.k_per_split;
@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
             if (warp == 2 && lane == 0) {
-                for (int j = 0; j < BN / 64 && n0 + 64 * j < g.N; ++j) {
+                const int nlim = ROPE ? (second ? g.n2 : g.n1) : g.N;
+                for (int j = 0; j < BN / 64 && nb0 + 64 * j < nlim; ++j) {
                     if (second)
                         tma_store_2d(&map_c2, sb + j * (BM * 128), nb0 + 64 * j, m0);
                     else
@@ -760,35 +761,48 @@ cudaError_t launch_gemm_tc(const GemmParams &p, bool nn, cudaStream_t stream, ui
 }
 
 // C1 = A B1^T and C2 = RoPE(A B2^T) in one launch: the output tiles of both products side by
-// side (TN, no k-split, 256 columns per tile), each 64-column head of C2 rotated pairwise by
-// pos[row] * theta^(-2i/64) in the epilogue. A [M][K], B1 [N1][K], B2 [N2][K], C1 [M][N1],
-// C2 [M][N2], all bf16; N1 and N2 multiples of 256, K of 64.
+// side (TN, no k-split), each 64-column head of C2 rotated pairwise by pos[row] *
+// theta^(-2i/64) in the epilogue. The tile width is the narrowest of 128, 192 and 256 whose
+// tiles fill at most one wave (at 128 heads: 192 columns, 86 + 43 = 129 CTAs, where 256 gave
+// 96), so that as many SMs as possible stream the weights. A [M][K], B1 [N1][K], B2 [N2][K],
+// C1 [M][N1], C2 [M][N2], all bf16; N1 and N2 multiples of 64, K of 64, M <= 128.
 cudaError_t launch_gemm_tc_rope(const uint16_t *A, int M, int K, const uint16_t *B1, int N1,
                                 uint16_t *C1, const uint16_t *B2, int N2, uint16_t *C2,
                                 const int32_t *pos, float theta, cudaStream_t stream,
                                 uint32_t *err) {
-    constexpr int BNR = 256;
-    if (N1 % BNR || N2 % BNR || K % BK || M > BM) return cudaErrorInvalidValue;
+    if (N1 % 64 || N2 % 64 || N1 < 64 || N2 < 64 || K % BK || M > BM) return cudaErrorInvalidValue;
+    const int widths[3] = {128, 192, 256};
+    int bn = 256;
+    for (int w = 0; w < 3; ++w) {
+        const int t = (N1 + widths[w] - 1) / widths[w] + (N2 + widths[w] - 1) / widths[w];
+        if (t <= device_sm_count()) {
+            bn = widths[w];
+            break;
+        }
+    }
+    const int t1 = (N1 + bn - 1) / bn, t2 = (N2 + bn - 1) / bn;
     GemmParams p{};
     p.A = A; p.lda = K; p.B = B1; p.ldb = K;
-    p.M = M; p.N = N1 + N2; p.K = K; p.batch = 1;
+    p.M = M; p.N = (t1 + t2) * bn; p.K = K; p.batch = 1;  // N: the grid's column tiles
     p.k_splits = 1; p.k_per_split = K; p.c_bf16 = C1; p.ldc = N1;
     TcGemmArgs g{};
     g.M = M; g.N = N1 + N2; g.K = K; g.batch = 1;
     g.k_splits = 1; g.k_per_split = K;
     g.c_bf16 = C1; g.ldc = N1;
     g.err = err;
-    g.n_split = N1;
+    g.t1 = t1; g.n1 = N1; g.n2 = N2;
     g.rope_pos = pos;
     g.rope = rope_freqs(theta);
     CUtensorMap ma, mb1, mb2, mc1, mc2;
     if (!map_2d(&ma, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, BM) ||
-        !map_2d(&mb1, B1, (uint64_t)K, (uint64_t)N1, (uint64_t)K, BNR) ||
-        !map_2d(&mb2, B2, (uint64_t)K, (uint64_t)N2, (uint64_t)K, BNR) ||
+        !map_2d(&mb1, B1, (uint64_t)K, (uint64_t)N1, (uint64_t)K, bn) ||
+        !map_2d(&mb2, B2, (uint64_t)K, (uint64_t)N2, (uint64_t)K, bn) ||
         !map_2d(&mc1, C1, (uint64_t)N1, (uint64_t)M, (uint64_t)N1, BM) ||
         !map_2d(&mc2, C2, (uint64_t)N2, (uint64_t)M, (uint64_t)N2, BM))
         return cudaErrorInvalidValue;
-    return launch_tile<false, BNR, true>(ma, mb1, g, p, stream, &mb2, &mc1, &mc2);
+    if (bn == 128) return launch_tile<false, 128, true>(ma, mb1, g, p, stream, &mb2, &mc1, &mc2);
+    if (bn == 192) return launch_tile<false, 192, true>(ma, mb1, g, p, stream, &mb2, &mc1, &mc2);
+    return launch_tile<false, 256, true>(ma, mb1, g, p, stream, &mb2, &mc1, &mc2);
 }
 
 }  // namespace mla

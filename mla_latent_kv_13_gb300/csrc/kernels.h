@@ -39,7 +39,7 @@ int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n);
 cudaError_t launch_gemm_tc_cluster(const GemmParams &p, int block_n, const ClusterAppend *ap,
                                    cudaStream_t stream, uint32_t *err);
 // C1 = A B1^T and C2 = RoPE(A B2^T) (64-column heads rotated pairwise at pos[row]) in one
-// launch; bf16 everywhere, N1 and N2 multiples of 256, M <= 128
+// launch; bf16 everywhere, N1 and N2 multiples of 64, M <= 128
 cudaError_t launch_gemm_tc_rope(const uint16_t *A, int M, int K, const uint16_t *B1, int N1,
                                 uint16_t *C1, const uint16_t *B2, int N2, uint16_t *C2,
                                 const int32_t *pos, float theta, cudaStream_t stream,

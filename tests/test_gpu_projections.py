@@ -110,8 +110,11 @@ def _proj(B, dm, ql, H, seed):
 
 # W_DQ's k-splits reduced in their cluster: 8 splits over 4 tiles with ragged rows (100);
 # two row tiles (200), the second one 72 rows
+# W_UQ + W_QR + RoPE in one launch: 128-column tiles at 16 and 32 heads, 192-column tiles
+# (ragged last tile of each product) at 128 heads
 @pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
                                            (100, 1024, 512, 32, None),
+                                           (5, 512, 256, 128, None),
                                            (200, 2048, 1536, 16, [0, 127, 128, 150, 199]),
                                            (128, 7168, 1536, 128, [0, 61, 127])])
 def test_absorb_q(mla, B, dm, ql, H, rows):
