@@ -337,25 +337,20 @@ def run_gpu(args, d, costs, metric, unit):
         raise RuntimeError("device error in the timed region")
 
     # ---- the attention launch inside the step, timed in a second pass with events around
-    # it (the same launches and streams as DecodeStep; kept out of the step's own timing,
-    # since an event between two launches stops the second one's early start)
+    # it (the same launches as DecodeStep; kept out of the step's own timing, since an event
+    # between two launches stops the second one's early start)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     w = step.w
     for i in range(args.steps):
-        step.ev_fork.record(stream)
-        step.side.wait_event(step.ev_fork)
-        mla.decode_prepare(L, B, H, max_len, step.num_splits, step.ws_att, step.side)
-        mla.append_kv(h, w["w_dkr"], pos, bt, cache, step.theta, step.ws_append, step.side)
-        step.ev_join.record(step.side)
-        mla.absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, step.theta,
-                     step.q_lat, step.q_rope, step.ws_q, stream)
-        stream.wait_event(step.ev_join)
+        mla.append_absorb_q(h, w["w_dkr"], pos, bt, cache, w["w_dq"], w["w_uq"], w["w_qr"],
+                            w["w_uk"], step.theta, step.q_lat, step.q_rope, step.ws_q, stream)
+        mla.decode_prepare(L, B, H, max_len, step.num_splits, step.ws_att, stream)
         ev[i][0].record(stream)
         mla.decode_attention_prepared(step.q_lat, step.q_rope, cache, bt, L, max_len, step.scale,
                                       step.num_splits, step.o_lat, step.lse, step.ws_att, stream)
         ev[i][1].record(stream)
-        mla.out_absorb(step.o_lat, w["w_uv"], w["w_o"], step.y, step.ws_out)
+        mla.out_absorb(step.o_lat, w["w_uv"], w["w_o"], step.y, step.ws_out, stream)
     torch.cuda.synchronize(dev)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     if step.check() != 0:
@@ -741,12 +736,13 @@ def time_attention_configs(pool, dev, launches: int, num_splits: int):
 
 def step_launches(step) -> int:
     """Kernels one DecodeStep launches, by the library's own plans for these shapes on this
-    device: append 1-2, absorb_q 3-6, out_absorb 2-3 (a split-K product reduced inside its
-    clusters is one launch, else two), decode 1-3 (+ merge, + schedule)."""
+    device: append_absorb_q 3-9 (W_DQ with W_DKR in one launch where their clusters fit),
+    decode 1-3 (+ merge, + schedule), out_absorb 2-3 (a split-K product reduced inside its
+    clusters is one launch, else two)."""
     from mla_latent_kv_13_gb300 import mla
     _, decode = mla.decode_plan(step.B, step.H, step.max_seqlen, step.num_splits)
-    append, absorb, out = mla.projection_launches(step.B, step.dm, step.ql, step.H)
-    return append + absorb + decode + out
+    _, _, out, both = mla.projection_launches(step.B, step.dm, step.ql, step.H)
+    return both + decode + out
 
 
 DECODE_SOURCES = ("decode_tc.cu", "sm100.cuh", "common.cuh")

@@ -398,6 +398,27 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
                           mla_bf16_t *q_rope, mla_stream_t stream);
 
 /*
+ * mla_append_kv and mla_absorb_q in one call (no counterpart on the pages: both
+ * down-projections of a decode step read the same hidden states h, [V2] 2.1). Results equal
+ * those of the two calls (the same arithmetic, up to the order of the fp32 split sums): the
+ * new latent rows written into the paged cache as mla_append_kv writes them, q_lat and q_rope
+ * as mla_absorb_q returns them. h W_DQ^T and h W_DKR^T run as one GEMM launch whose k-splits
+ * are reduced inside thread-block clusters; where no cluster split fits the device, the call
+ * runs the two entry points one after the other. Arguments as there (the append's first,
+ * then the query's; one rope_theta for both); the checks of both apply. Workspace:
+ * mla_append_absorb_q_workspace_size (the larger of the two calls' workspaces).
+ */
+mla_status_t mla_append_absorb_q_workspace_size(int B, int d_model, int q_lora, int H,
+                                                size_t *bytes);
+mla_status_t mla_append_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                                 const int32_t *pos, const int32_t *block_table, int max_blocks,
+                                 mla_bf16_t *kv_cache, int num_blocks, const mla_bf16_t *w_dq,
+                                 int q_lora, const mla_bf16_t *w_uq, const mla_bf16_t *w_qr,
+                                 const mla_bf16_t *w_uk, int H, float rope_theta, void *workspace,
+                                 size_t ws_bytes, mla_bf16_t *q_lat, mla_bf16_t *q_rope,
+                                 mla_stream_t stream);
+
+/*
  * [V2] 2.1 (W_UV absorbed into the output projection):
  *   o_v_i = W_UV_i . o_lat_i    (512 -> 128, head i)
  *   y     = [o_v_1 | ... | o_v_H] . W_O^T        (H*128 -> d_model)
@@ -417,12 +438,13 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
  * otherwise it writes fp32 partials and a second launch sums them. *append = 1 or 2
  * (mla_append_kv; mla_append_kv_fp8 always 2), *absorb_q = 3..6 (W_DQ 1 or 2; W_UQ, W_QR
  * and the RoPE 1 for B <= 128, else 3; W_UK 1), *out_absorb = 2 or 3 (W_UV 1; W_O 1 or
- * 2). With no visible device the partial-writing plan is reported. Any output pointer may
+ * 2), *append_absorb_q = 3 or 5 (W_DQ with W_DKR 1, then as absorb_q) or the sum of the
+ * two calls' counts. With no visible device the partial-writing plan is reported. Any output pointer may
  * be null. Same argument rules as the entry points (MLA_ERR_INVALID_ARG, or
  * MLA_ERR_UNSUPPORTED for H).
  */
 mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int *append,
-                                     int *absorb_q, int *out_absorb);
+                                     int *absorb_q, int *out_absorb, int *append_absorb_q);
 
 /* ------------------------------------------------------- device status */
 

@@ -633,6 +633,50 @@ AbsorbQLayout absorb_q_layout(int B, int d_model, int q_lora, int H) {
 }
 }  // namespace
 
+namespace {
+// absorb_q after c_q: q_nope and q_rope (one launch for up to 128 sequences), then the
+// per-head W_UK absorption into q_lat
+mla_status_t absorb_q_from_cq(const uint16_t *cq, int B, int q_lora, const mla_bf16_t *w_uq,
+                              const mla_bf16_t *w_qr, const mla_bf16_t *w_uk, int H,
+                              const int32_t *pos, float rope_theta, const AbsorbQLayout &L,
+                              float *part, uint16_t *qn, mla_bf16_t *q_lat, mla_bf16_t *q_rope,
+                              cudaStream_t st, uint32_t *err) {
+    if (B <= 128) {
+        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128]) and q_rope = RoPE(c_q W_QR^T)
+        // in one launch: both read c_q, and the rotation is the second product's epilogue
+        if (launch_gemm_tc_rope(cq, B, q_lora, w_uq, H * D_NOPE, qn, w_qr, H * D_ROPE, q_rope,
+                                pos, rope_theta, st, err) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    } else {
+        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128])
+        GemmParams g{};
+        g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
+        g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
+        g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+
+        // q_rope = RoPE(c_q W_QR^T)
+        g = GemmParams{};
+        g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
+        g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
+        g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
+        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+        if (launch_qrope_finalize(part, L.s2, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
+
+    // q_lat[b, i] = q_nope[b, i] W_UK_i  (per-head product, W_UK_i stored [128][512])
+    GemmParams g{};
+    g.A = qn; g.lda = H * D_NOPE; g.a_bstride = D_NOPE;
+    g.B = w_uk; g.ldb = D_C; g.b_bstride = (long)D_NOPE * D_C;
+    g.M = B; g.N = D_C; g.K = D_NOPE; g.batch = H;
+    g.k_splits = 1; g.k_per_split = D_NOPE;
+    g.c_bf16 = q_lat; g.ldc = (long)H * D_C; g.c_bstride = D_C;
+    return cuda_status(launch_gemm_tc(g, true, st, err));
+}
+
+}  // namespace
+
 mla_status_t mla_absorb_q_workspace_size(int B, int d_model, int q_lora, int H, size_t *bytes) {
     if (!bytes || B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 ||
         q_lora % 64)
@@ -684,38 +728,69 @@ mla_status_t mla_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf1
             return MLA_ERR_CUDA;
     }
 
-    if (B <= 128) {
-        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128]) and q_rope = RoPE(c_q W_QR^T)
-        // in one launch: both read c_q, and the rotation is the second product's epilogue
-        if (launch_gemm_tc_rope(cq, B, q_lora, w_uq, H * D_NOPE, qn, w_qr, H * D_ROPE, q_rope,
-                                pos, rope_theta, st, err) != cudaSuccess)
-            return MLA_ERR_CUDA;
-    } else {
-        // q_nope = c_q W_UQ^T (bf16 intermediate [B][H*128])
-        g = GemmParams{};
-        g.A = cq; g.lda = q_lora; g.B = w_uq; g.ldb = q_lora;
-        g.M = B; g.N = H * D_NOPE; g.K = q_lora; g.batch = 1;
-        g.k_splits = 1; g.k_per_split = q_lora; g.c_bf16 = qn; g.ldc = H * D_NOPE;
-        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
+    return absorb_q_from_cq(cq, B, q_lora, w_uq, w_qr, w_uk, H, pos, rope_theta, L, part, qn,
+                            q_lat, q_rope, st, err);
+}
 
-        // q_rope = RoPE(c_q W_QR^T)
-        g = GemmParams{};
-        g.A = cq; g.lda = q_lora; g.B = w_qr; g.ldb = q_lora;
-        g.M = B; g.N = H * D_ROPE; g.K = q_lora; g.batch = 1;
-        g.k_splits = L.s2; g.k_per_split = L.per2; g.c_part = part;
-        if (launch_gemm_tc(g, false, st, err) != cudaSuccess) return MLA_ERR_CUDA;
-        if (launch_qrope_finalize(part, L.s2, B, H, pos, rope_theta, q_rope, st) != cudaSuccess)
-            return MLA_ERR_CUDA;
+// ------------------------------------------------------ append + absorb_q
+
+mla_status_t mla_append_absorb_q_workspace_size(int B, int d_model, int q_lora, int H,
+                                                size_t *bytes) {
+    if (!bytes) return MLA_ERR_INVALID_ARG;
+    size_t a = 0, q = 0;
+    mla_status_t st = mla_append_kv_workspace_size(B, d_model, &a);
+    if (st != MLA_OK) return st;
+    if ((st = mla_absorb_q_workspace_size(B, d_model, q_lora, H, &q)) != MLA_OK) return st;
+    *bytes = a > q ? a : q;
+    return MLA_OK;
+}
+
+mla_status_t mla_append_absorb_q(const mla_bf16_t *h, int B, int d_model, const mla_bf16_t *w_dkr,
+                                 const int32_t *pos, const int32_t *block_table, int max_blocks,
+                                 mla_bf16_t *kv_cache, int num_blocks, const mla_bf16_t *w_dq,
+                                 int q_lora, const mla_bf16_t *w_uq, const mla_bf16_t *w_qr,
+                                 const mla_bf16_t *w_uk, int H, float rope_theta, void *workspace,
+                                 size_t ws_bytes, mla_bf16_t *q_lat, mla_bf16_t *q_rope,
+                                 mla_stream_t stream) {
+    if (!h || !w_dkr || !pos || !block_table || !kv_cache || !w_dq || !w_uq || !w_qr || !w_uk ||
+        !workspace || !q_lat || !q_rope)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 || q_lora % 64 ||
+        max_blocks < 1 || num_blocks < 1 || !(rope_theta > 0.f) || !isfinite(rope_theta))
+        return MLA_ERR_INVALID_ARG;
+    if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(h, 16) || !aligned(w_dkr, 16) || !aligned(kv_cache, 16) || !aligned(w_dq, 16) ||
+        !aligned(w_uq, 16) || !aligned(w_qr, 16) || !aligned(w_uk, 16) || !aligned(q_lat, 16) ||
+        !aligned(q_rope, 16) || !aligned(workspace, 256))
+        return MLA_ERR_INVALID_ARG;
+    size_t need = 0;
+    mla_append_absorb_q_workspace_size(B, d_model, q_lora, H, &need);
+    if (ws_bytes < need) return MLA_ERR_WORKSPACE;
+    AbsorbQLayout L = absorb_q_layout(B, d_model, q_lora, H);
+    char *w = static_cast<char *>(workspace);
+    float *part = reinterpret_cast<float *>(w + L.part);
+    uint16_t *cq = reinterpret_cast<uint16_t *>(w + L.cq);
+    uint16_t *qn = reinterpret_cast<uint16_t *>(w + L.qn);
+    cudaStream_t st = S(stream);
+    uint32_t *err = err_word(workspace);
+    // c_q = h W_DQ^T and the new cache rows from h W_DKR^T in one launch, their k-splits
+    // reduced inside their clusters; where no cluster split fits, the two calls one after
+    // the other (same stream, same workspace)
+    const ClusterAppend ap{pos, block_table, max_blocks, num_blocks, kv_cache, rope_theta};
+    const cudaError_t e = launch_gemm_tc_cluster_dq_append(h, B, d_model, w_dq, q_lora, cq, w_dkr,
+                                                           ap, st, err);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        mla_status_t r = mla_append_kv(h, B, d_model, w_dkr, pos, block_table, max_blocks,
+                                       kv_cache, num_blocks, rope_theta, workspace, ws_bytes,
+                                       stream);
+        if (r != MLA_OK) return r;
+        return mla_absorb_q(h, B, d_model, w_dq, q_lora, w_uq, w_qr, w_uk, H, pos, rope_theta,
+                            workspace, ws_bytes, q_lat, q_rope, stream);
     }
-
-    // q_lat[b, i] = q_nope[b, i] W_UK_i  (per-head product, W_UK_i stored [128][512])
-    g = GemmParams{};
-    g.A = qn; g.lda = H * D_NOPE; g.a_bstride = D_NOPE;
-    g.B = w_uk; g.ldb = D_C; g.b_bstride = (long)D_NOPE * D_C;
-    g.M = B; g.N = D_C; g.K = D_NOPE; g.batch = H;
-    g.k_splits = 1; g.k_per_split = D_NOPE;
-    g.c_bf16 = q_lat; g.ldc = (long)H * D_C; g.c_bstride = D_C;
-    return cuda_status(launch_gemm_tc(g, true, st, err));
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return absorb_q_from_cq(cq, B, q_lora, w_uq, w_qr, w_uk, H, pos, rope_theta, L, part, qn,
+                            q_lat, q_rope, st, err);
 }
 
 // ---------------------------------------------------------- out_absorb
@@ -786,7 +861,7 @@ mla_status_t mla_out_absorb(const mla_bf16_t *o_lat, int B, int H, const mla_bf1
 }
 
 mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int *append,
-                                     int *absorb_q, int *out_absorb) {
+                                     int *absorb_q, int *out_absorb, int *append_absorb_q) {
     if (B < 1 || B > 4096 || d_model < 64 || d_model % 64 || q_lora < 64 || q_lora % 64)
         return MLA_ERR_INVALID_ARG;
     if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
@@ -796,6 +871,15 @@ mla_status_t mla_projection_launches(int B, int d_model, int q_lora, int H, int 
         *absorb_q = (gemm_cluster_plan(B, q_lora, d_model, &per, nullptr) > 0 ? 1 : 2) +
                     (B <= 128 ? 1 : 3) + 1;
     if (out_absorb) *out_absorb = 1 + (gemm_cluster_plan(B, d_model, H * D_V, &per, nullptr) > 0 ? 1 : 2);
+    if (append_absorb_q) {
+        const int rest = (B <= 128 ? 1 : 3) + 1;  // q_nope / q_rope, then W_UK
+        if (gemm_cluster_fits_dq_append(B, d_model, q_lora))
+            *append_absorb_q = 1 + rest;
+        else
+            *append_absorb_q = (gemm_cluster_plan(B, D_QK, d_model, &per, nullptr) > 0 ? 1 : 2) +
+                               (gemm_cluster_plan(B, q_lora, d_model, &per, nullptr) > 0 ? 1 : 2) +
+                               rest;
+    }
     return MLA_OK;
 }
 

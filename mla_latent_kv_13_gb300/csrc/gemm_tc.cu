@@ -120,7 +120,9 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 
 // CRED: 0 = no cluster reduction; 1 = reduced into bf16 C; 2 = reduced into the new latent
 // cache rows of append (row b of the product is sequence b's token at pos[b]: the k_rope
-// pairs rotated by that position, the row written into its block of the paged cache)
+// pairs rotated by that position, the row written into its block of the paged cache);
+// 3 = two products of one activation, column tiles t1 and up the second (weights map_b2):
+// the first reduced into bf16 C, the second into append's cache rows
 template <bool NN, int BN, bool ROPE, int CRED>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -138,9 +140,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-    // ROPE kernels: a tile of the second product reads map_b2 and writes map_c2 from its
-    // own column nb0 (each product's last tile may be ragged)
-    const bool second = ROPE && static_cast<int>(blockIdx.x) >= g.t1;
+    // ROPE and CRED = 3 kernels: a tile of the second product reads map_b2 (ROPE: and writes
+    // map_c2) from its own column nb0 (each product's last tile may be ragged)
+    constexpr bool TWO = ROPE || CRED == 3;
+    const bool second = TWO && static_cast<int>(blockIdx.x) >= g.t1;
     const int nb0 = second ? (static_cast<int>(blockIdx.x) - g.t1) * BN : n0;
     const CUtensorMap *const mbp = second ? &map_b2 : &map_b;
     const int batch = blockIdx.z / g.k_splits, split = blockIdx.z % g.k_splits;
@@ -428,10 +431,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t src[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) src[q] = q < S ? mapa(sb, static_cast<uint32_t>(q)) : 0u;
+        const int nlim = CRED == 3 ? (second ? g.n2 : g.n1) : g.N;
         for (int e = tid; e < (r_end - r_begin) * U; e += NTHREADS) {
             const int r = r_begin + e / U, j = e % U;
-            const int n = n0 + 4 * j;
-            if (n >= g.N) continue;
+            const int n = nb0 + 4 * j;
+            if (n >= nlim) continue;
             const uint32_t off = static_cast<uint32_t>(r * (BN * 4) + ((j ^ (r & 7)) << 4));
             float4 v[8];
 #pragma unroll
@@ -447,7 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     a3 += v[q].w;
                 }
             uint16_t *dst;
-            if constexpr (CRED == 1) {
+            if (CRED == 1 || (CRED == 3 && !second)) {
                 dst = g.c_bf16 + (size_t)(m0 + r) * g.ldc + n;
             } else {
                 // a position or block outside the cache is an error: flagged once per row
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                     ? g.ap_bt[(size_t)b * g.ap_max_blocks + pp / BLOCK]
                                     : -1;
                 if (blk < 0 || blk >= g.ap_num_blocks) {
-                    if (j == 0 && n0 == 0) flag_error(g.err, MLA_ERR_OUT_OF_RANGE, b);
+                    if (j == 0 && nb0 == 0) flag_error(g.err, MLA_ERR_OUT_OF_RANGE, b);
                     continue;
                 }
                 if (n >= D_C) {
@@ -653,6 +657,32 @@ int gemm_block_n(int M, int N, int K) {
 // the most k-splits (2..8, at least two k-blocks each) whose clusters the device holds for
 // every output tile at once, with room to spare, taking the width that runs the most CTAs;
 // 0 if no such split exists (the caller then writes partials for a finalize kernel).
+namespace {
+// The most k-splits (2..8, at least two k-blocks each, every split non-empty) whose clusters
+// of `tiles` output tiles of width bn the device holds at once with room to spare; 0 if none.
+int cluster_splits(long tiles, int bn, int kblocks, int *per_out) {
+    for (int s = 8; s >= 2; --s) {
+        const int per = (kblocks + s - 1) / s;  // k-blocks per split
+        const int splits = (kblocks + per - 1) / per;
+        if (per < 2 || splits != s) continue;
+        const int nsmax = bn == 128 ? Tile<128>::NS : (bn == 224 ? Tile<224>::NS : Tile<256>::NS);
+        const int ns = per < nsmax ? per : nsmax;  // the ring launch_tile gives it
+        const int cap = bn == 128   ? cluster_capacity<128>(s, ns)
+                        : bn == 224 ? cluster_capacity<224>(s, ns)
+                                    : cluster_capacity<256>(s, ns);
+        // a tenth of the clusters' room left free: clusters are placed only where a whole
+        // group of SMs is idle, and with every slot needed one SM still busy with the
+        // previous kernel sends a cluster into a second wave (5 splits of the 7168 x 16384
+        // output product, 28 clusters where the device holds 28, took 68 us; 4 splits 53)
+        if (tiles * 10 <= (long)cap * 9) {
+            *per_out = per;
+            return s;
+        }
+    }
+    return 0;
+}
+}  // namespace
+
 int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n) {
     if (M < 1 || N < 4 || N % 4 || K < 2 * BK || K % BK) return 0;
     const int kblocks = K / BK;
@@ -665,28 +695,13 @@ int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n) {
     for (int w = 0; w < 2 && widths[w]; ++w) {
         const int bn = widths[w];
         const long tiles = (long)((N + bn - 1) / bn) * ((M + BM - 1) / BM);
-        for (int s = 8; s >= 2; --s) {
-            const int per = (kblocks + s - 1) / s;  // k-blocks per split
-            const int splits = (kblocks + per - 1) / per;
-            if (per < 2 || splits != s) continue;
-            const int nsmax = bn == 128 ? Tile<128>::NS : (bn == 224 ? Tile<224>::NS : Tile<256>::NS);
-            const int ns = per < nsmax ? per : nsmax;  // the ring launch_tile gives it
-            const int cap = bn == 128   ? cluster_capacity<128>(s, ns)
-                            : bn == 224 ? cluster_capacity<224>(s, ns)
-                                        : cluster_capacity<256>(s, ns);
-            // a tenth of the clusters' room left free: clusters are placed only where a whole
-            // group of SMs is idle, and with every slot needed one SM still busy with the
-            // previous kernel sends a cluster into a second wave (5 splits of the 7168 x 16384
-            // output product, 28 clusters where the device holds 28, took 68 us; 4 splits 53)
-            if (tiles * 10 <= (long)cap * 9) {
-                if (tiles * s > best_ctas) {
-                    best_ctas = tiles * s;
-                    best_s = s;
-                    best_per = per;
-                    best_bn = bn;
-                }
-                break;  // fewer splits of this width only lose CTAs
-            }
+        int per = 0;
+        const int s = cluster_splits(tiles, bn, kblocks, &per);
+        if (s > 0 && tiles * s > best_ctas) {  // the width that runs the most CTAs
+            best_ctas = tiles * s;
+            best_s = s;
+            best_per = per;
+            best_bn = bn;
         }
     }
     if (best_s == 0) return 0;
@@ -724,6 +739,54 @@ cudaError_t launch_gemm_tc_cluster(const GemmParams &p, int bn, const ClusterApp
     return bn == 256   ? launch_tile<false, 256, false, 1>(ma, mb, g, p, stream)
            : bn == 224 ? launch_tile<false, 224, false, 1>(ma, mb, g, p, stream)
                        : launch_tile<false, 128, false, 1>(ma, mb, g, p, stream);
+}
+
+bool gemm_cluster_fits_dq_append(int M, int N1, int K) {
+    if (M < 1 || N1 < 4 || N1 % 4 || K < 2 * BK || K % BK) return false;
+    const long tiles = (long)((N1 + 127) / 128 + (D_QK + 127) / 128) * ((M + BM - 1) / BM);
+    int per = 0;
+    return cluster_splits(tiles, 128, K / BK, &per) > 0;
+}
+
+// C1 = A B1^T (bf16, row pitch N1) and append's cache rows from A B2^T (N2 = 576), with both
+// products' k-splits reduced inside their clusters, in one launch (128-column tiles, each
+// product with its own tile range): the two down-projections of a decode step read the same
+// hidden states. Returns cudaErrorNotSupported when no cluster split fits the device (the
+// caller then runs the products separately).
+cudaError_t launch_gemm_tc_cluster_dq_append(const uint16_t *A, int M, int K, const uint16_t *B1,
+                                            int N1, uint16_t *C1, const uint16_t *B2,
+                                            const ClusterAppend &ap, cudaStream_t stream,
+                                            uint32_t *err) {
+    constexpr int bn = 128;
+    const int N2 = D_QK;
+    if (M < 1 || N1 < 4 || N1 % 4 || K < 2 * BK || K % BK || !ap.pos || !ap.block_table ||
+        !ap.cache || (reinterpret_cast<uintptr_t>(ap.cache) & 7) ||
+        (reinterpret_cast<uintptr_t>(C1) & 7))
+        return cudaErrorInvalidValue;
+    const int t1 = (N1 + bn - 1) / bn, t2 = (N2 + bn - 1) / bn;
+    const long tiles = (long)(t1 + t2) * ((M + BM - 1) / BM);
+    int per = 0;
+    const int s = cluster_splits(tiles, bn, K / BK, &per);
+    if (s == 0) return cudaErrorNotSupported;
+    GemmParams p{};
+    p.A = A; p.lda = K; p.B = B1; p.ldb = K;
+    p.M = M; p.N = (t1 + t2) * bn; p.K = K; p.batch = 1;  // N: the grid's column tiles
+    p.k_splits = s; p.k_per_split = per * BK; p.c_bf16 = C1; p.ldc = N1;
+    TcGemmArgs g{};
+    g.M = M; g.N = N1 + N2; g.K = K; g.batch = 1;
+    g.k_splits = s; g.k_per_split = per * BK;
+    g.c_bf16 = C1; g.ldc = N1;
+    g.err = err;
+    g.t1 = t1; g.n1 = N1; g.n2 = N2;
+    g.ap_pos = ap.pos; g.ap_bt = ap.block_table; g.ap_max_blocks = ap.max_blocks;
+    g.ap_num_blocks = ap.num_blocks; g.ap_cache = ap.cache;
+    g.rope = rope_freqs(ap.theta);
+    CUtensorMap ma, mb1, mb2;
+    if (!map_2d(&ma, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, BM) ||
+        !map_2d(&mb1, B1, (uint64_t)K, (uint64_t)N1, (uint64_t)K, bn) ||
+        !map_2d(&mb2, B2, (uint64_t)K, (uint64_t)N2, (uint64_t)K, bn))
+        return cudaErrorInvalidValue;
+    return launch_tile<false, bn, false, 3>(ma, mb1, g, p, stream, &mb2);
 }
 
 // Shapes: A is the [rows_a][lda] matrix holding every batch's [M][K] slice at column

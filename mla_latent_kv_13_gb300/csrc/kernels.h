@@ -36,6 +36,14 @@ struct ClusterAppend {
     float theta;
 };
 int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n);
+// whether launch_gemm_tc_cluster_dq_append finds a cluster split for these shapes
+bool gemm_cluster_fits_dq_append(int M, int N1, int K);
+// c_q = A W_DQ^T (bf16 [M][N1]) and append's rows from A W_DKR^T in one cluster-reduced
+// launch; cudaErrorNotSupported when no cluster split fits (run them separately then).
+cudaError_t launch_gemm_tc_cluster_dq_append(const uint16_t *A, int M, int K, const uint16_t *B1,
+                                            int N1, uint16_t *C1, const uint16_t *B2,
+                                            const ClusterAppend &ap, cudaStream_t stream,
+                                            uint32_t *err);
 cudaError_t launch_gemm_tc_cluster(const GemmParams &p, int block_n, const ClusterAppend *ap,
                                    cudaStream_t stream, uint32_t *err);
 // C1 = A B1^T and C2 = RoPE(A B2^T) (64-column heads rotated pairwise at pos[row]) in one

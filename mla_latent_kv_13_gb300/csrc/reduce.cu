@@ -171,54 +171,69 @@ __device__ int block_exclusive_scan4(const int *v, int n, int *out, int *warp_to
 // split of the total weight cuts between clusters -> nparts, part_begin; and the merge jobs:
 // the sequence cut at the end of cluster c's range (its first tile in that range) is job c,
 // jobs[c] = (b, first part, parts), else (-1, 0, 0). Reads only seqlens, so it may run once
-// for several attention calls over the same lengths.
+// for several attention calls over the same lengths. Everything is computed in shared memory
+// before the dependency wait, which comes only before the first store: the lengths are the
+// caller's input, so the kernel may run beside its predecessor (the last query projection of
+// a decode step), while its outputs may still be read by the previous attention call's merge.
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(
     const int32_t *seqlens, int B, int max_len, int P, int32_t *tile_start, int32_t *wpos,
     int32_t *part_begin, int32_t *nparts, int4 *jobs, uint32_t *err) {
-    __shared__ int v[4096], ex[4096], warp_tot[33];
+    // dynamic shared memory, four arrays of B: v = tiles per sequence, later parts per
+    // sequence; ts = the tiles' exclusive scan (tile_start); wp = the weights' exclusive
+    // scan, then the weighted positions (wpos); pb = the parts' exclusive scan (part_begin)
+    extern __shared__ int sched_smem[];
+    int *const v = sched_smem, *const ts = v + B, *const wp = ts + B, *const pb = wp + B;
+    __shared__ int warp_tot[33];
+    __shared__ int bad;
     grid_launch_dependents();
-    grid_dependency_wait();
-    for (int c = threadIdx.x; c < P; c += blockDim.x) jobs[c] = make_int4(-1, 0, 0, 0);
+    if (threadIdx.x == 0) bad = -1;
+    __syncthreads();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         int L = seqlens[b];
         if (L < 0 || L > max_len) {  // the attention kernel clamps the same way
-            flag_error(err, MLA_ERR_OUT_OF_RANGE, b);
+            atomicMax(&bad, b);
             L = L < 0 ? 0 : max_len;
         }
         v[b] = (L + BLOCK - 1) / BLOCK;
     }
     __syncthreads();
-    const int T = block_exclusive_scan4(v, B, ex, warp_tot);
-    for (int b = threadIdx.x; b < B; b += blockDim.x) tile_start[b] = ex[b];
-    if (threadIdx.x == 0) tile_start[B] = T;
+    const int T = block_exclusive_scan4(v, B, ts, warp_tot);
+    for (int b = threadIdx.x; b < B; b += blockDim.x) wp[b] = v[b] > 0 ? v[b] + SEG_COST : 0;
     __syncthreads();
-    for (int b = threadIdx.x; b < B; b += blockDim.x) ex[b] = v[b] > 0 ? v[b] + SEG_COST : 0;
-    __syncthreads();
-    const int W = block_exclusive_scan4(ex, B, ex, warp_tot);  // in place
+    const int W = block_exclusive_scan4(wp, B, wp, warp_tot);  // in place
     // never more ranges than weight positions, so that every range is non-empty and a
     // sequence cut between clusters c0..c1 gets exactly one part from each of them
     const int Pe = W < P ? W : P;
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        const int w0 = ex[b] + (v[b] > 0 ? SEG_COST : 0);
-        wpos[b] = w0;
+        const int w0 = wp[b] + (v[b] > 0 ? SEG_COST : 0);
         int np = 0;
         if (v[b] > 0) {
             const int c0 = cluster_of_tile(w0, W, Pe);
             const int c1 = cluster_of_tile(w0 + v[b] - 1, W, Pe);
             np = c1 > c0 ? c1 - c0 + 1 : 0;
         }
-        nparts[b] = np;
+        wp[b] = w0;
+        v[b] = np;  // the tile counts are in ts from here on
     }
-    if (threadIdx.x == 0) wpos[B] = W;
     __syncthreads();
-    for (int b = threadIdx.x; b < B; b += blockDim.x) v[b] = nparts[b];
-    __syncthreads();
-    block_exclusive_scan4(v, B, ex, warp_tot);
+    block_exclusive_scan4(v, B, pb, warp_tot);
+    // every output below may still be read by the attention call before this one
+    grid_dependency_wait();
+    if (threadIdx.x == 0 && bad >= 0) flag_error(err, MLA_ERR_OUT_OF_RANGE, bad);
+    for (int c = threadIdx.x; c < P; c += blockDim.x) jobs[c] = make_int4(-1, 0, 0, 0);
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        part_begin[b] = ex[b];
-        if (v[b] > 0)  // after the initialisation above (block_exclusive_scan4 synchronises)
-            jobs[cluster_of_tile(wpos[b], W, Pe)] = make_int4(b, ex[b], v[b], 0);
+        tile_start[b] = ts[b];
+        wpos[b] = wp[b];
+        nparts[b] = v[b];
+        part_begin[b] = pb[b];
     }
+    if (threadIdx.x == 0) {
+        tile_start[B] = T;
+        wpos[B] = W;
+    }
+    __syncthreads();  // the job list is cleared before the jobs go in
+    for (int b = threadIdx.x; b < B; b += blockDim.x)
+        if (v[b] > 0) jobs[cluster_of_tile(wp[b], W, Pe)] = make_int4(b, pb[b], v[b], 0);
 }
 
 constexpr int EMPTY_CTAS = 32;  // rows of CTAs of the merge kernel writing empty sequences
@@ -275,7 +290,11 @@ cudaError_t launch_decode_schedule(const int32_t *seqlens, int B, int max_len, i
                                    int32_t *tile_start, int32_t *wpos, int32_t *part_begin,
                                    int32_t *nparts, int4 *jobs, uint32_t *err,
                                    cudaStream_t stream) {
-    return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), 0, stream, seqlens, B,
+    const size_t smem = 4 * sizeof(int) * (size_t)B;  // B <= 4096: at most 64 KB
+    cudaError_t e = cudaFuncSetAttribute(decode_schedule_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * 4 * 4096);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_schedule_kernel, dim3(1), dim3(1024), smem, stream, seqlens, B,
                       max_len, P, tile_start, wpos, part_begin, nparts, jobs, err);
 }
 

@@ -49,7 +49,7 @@ _SIGS = {
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _szp], _i),
     "mla_decode_plan": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
     "mla_projection_launches": ([_i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i),
-                                 ctypes.POINTER(_i)], _i),
+                                 ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
     "mla_decode_schedule": ([_vp, _i, _i, _i, _vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
                             _i),
     "mla_decode_attention": ([_vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _f, _i, _vp, _sz,
@@ -74,6 +74,9 @@ _SIGS = {
     "mla_absorb_q_workspace_size": ([_i, _i, _i, _i, _szp], _i),
     "mla_absorb_q": ([_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _f, _vp, _sz, _vp, _vp,
                       _vp], _i),
+    "mla_append_absorb_q_workspace_size": ([_i, _i, _i, _i, _szp], _i),
+    "mla_append_absorb_q": ([_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp,
+                             _i, _f, _vp, _sz, _vp, _vp, _vp], _i),
     "mla_out_absorb_workspace_size": ([_i, _i, _i, _szp], _i),
     "mla_out_absorb": ([_vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp, _vp], _i),
     "mla_clear_device_status": ([_vp, _vp], _i),
@@ -158,14 +161,14 @@ def decode_plan(B, H, max_seqlen, num_splits=0):
 
 
 def projection_launches(B, d_model, q_lora, H):
-    """(append, absorb_q, out_absorb): the kernels one call of each launches for these
-    shapes on the current device."""
-    a, q, o = _i(0), _i(0), _i(0)
+    """(append, absorb_q, out_absorb, append_absorb_q): the kernels one call of each
+    launches for these shapes on the current device."""
+    a, q, o, aq = _i(0), _i(0), _i(0), _i(0)
     rc = _lib.mla_projection_launches(B, d_model, q_lora, H, ctypes.byref(a), ctypes.byref(q),
-                                      ctypes.byref(o))
+                                      ctypes.byref(o), ctypes.byref(aq))
     if rc != 0:
         raise MLAError(rc, "mla_projection_launches")
-    return a.value, q.value, o.value
+    return a.value, q.value, o.value, aq.value
 
 
 def decode_schedule(seqlens, max_blocks, clusters):
@@ -191,6 +194,10 @@ def decode_schedule(seqlens, max_blocks, clusters):
 
 def absorb_q_workspace_size(B, d_model, q_lora, H):
     return _size("mla_absorb_q_workspace_size", B, d_model, q_lora, H)
+
+
+def append_absorb_q_workspace_size(B, d_model, q_lora, H):
+    return _size("mla_append_absorb_q_workspace_size", B, d_model, q_lora, H)
 
 
 def out_absorb_workspace_size(B, H, d_model):
@@ -443,6 +450,30 @@ def absorb_q(h, w_dq, w_uq, w_qr, w_uk, pos, rope_theta=10000.0, q_lat=None, q_r
     return q_lat, q_rope, workspace
 
 
+def append_absorb_q(h, w_dkr, pos, block_table, kv_cache, w_dq, w_uq, w_qr, w_uk,
+                    rope_theta=10000.0, q_lat=None, q_rope=None, workspace=None, stream=None):
+    """append_kv and absorb_q in one call (both read h): the new rows go into kv_cache,
+    returns (q_lat, q_rope, workspace)."""
+    B, dm = h.shape
+    ql = w_dq.shape[0]
+    H = w_uk.shape[0]
+    dev = h.device
+    if q_lat is None:
+        q_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
+    if q_rope is None:
+        q_rope = torch.empty((B, H, D_ROPE), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(append_absorb_q_workspace_size(B, dm, ql, H), stream=stream)
+    rc = _lib.mla_append_absorb_q(_ptr(_bits(h)), B, dm, _ptr(_bits(w_dkr)), _ptr(pos),
+                                  _ptr(block_table), block_table.shape[1], _ptr(_bits(kv_cache)),
+                                  kv_cache.shape[0], _ptr(_bits(w_dq)), ql, _ptr(_bits(w_uq)),
+                                  _ptr(_bits(w_qr)), _ptr(_bits(w_uk)), H, float(rope_theta),
+                                  _ptr(workspace), workspace.numel(), _ptr(q_lat), _ptr(q_rope),
+                                  _stream(stream))
+    _ok(rc, "mla_append_absorb_q")
+    return q_lat, q_rope, workspace
+
+
 def out_absorb(o_lat, w_uv, w_o, y=None, workspace=None, stream=None):
     B, H, _ = o_lat.shape
     dm = w_o.shape[0]
@@ -518,8 +549,7 @@ class DecodeStep:
         self.theta = rope_theta
         self.scale = (1.0 / (D_NOPE + D_ROPE) ** 0.5) if scale is None else scale
         dev = weights["w_dkr"].device
-        self.ws_append = alloc_workspace(append_kv_workspace_size(B, self.dm))
-        self.ws_q = alloc_workspace(absorb_q_workspace_size(B, self.dm, self.ql, H))
+        self.ws_q = alloc_workspace(append_absorb_q_workspace_size(B, self.dm, self.ql, H))
         self.ws_att = alloc_workspace(decode_workspace_size(B, H, max_seqlen, num_splits))
         self.ws_out = alloc_workspace(out_absorb_workspace_size(B, H, self.dm))
         self.q_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
@@ -527,29 +557,21 @@ class DecodeStep:
         self.o_lat = torch.empty((B, H, D_C), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, H), dtype=torch.float32, device=dev)
         self.y = torch.empty((B, self.dm), dtype=torch.bfloat16, device=dev)
-        # append_kv and absorb_q read only h and pos, the attention schedule only the
-        # lengths: the append and the schedule run on a side stream, forked from and joined
-        # back into the caller's stream by events
-        self.side = torch.cuda.Stream(device=dev)
-        self.ev_fork = torch.cuda.Event()
-        self.ev_join = torch.cuda.Event()
 
     def __call__(self, h, pos, seqlens_after, block_table, kv_cache, stream=None, out=None):
         """One step; the result y [B, d_model] bf16 goes to `out` if given, else to the
-        step's own buffer (returned either way)."""
+        step's own buffer (returned either way). One stream: the new cache rows and the
+        absorbed query (one call: both read h), the attention schedule (it reads only the
+        lengths, so it runs beside the last query projection), the attention, the output
+        projections."""
         w = self.w
         y = self.y if out is None else out
         main = torch.cuda.current_stream() if stream is None else stream
-        self.ev_fork.record(main)
-        self.side.wait_event(self.ev_fork)
+        append_absorb_q(h, w["w_dkr"], pos, block_table, kv_cache, w["w_dq"], w["w_uq"],
+                        w["w_qr"], w["w_uk"], self.theta, self.q_lat, self.q_rope, self.ws_q,
+                        main)
         decode_prepare(seqlens_after, self.B, self.H, self.max_seqlen, self.num_splits,
-                       self.ws_att, self.side)
-        append_kv(h, w["w_dkr"], pos, block_table, kv_cache, self.theta, self.ws_append,
-                  self.side)
-        self.ev_join.record(self.side)
-        absorb_q(h, w["w_dq"], w["w_uq"], w["w_qr"], w["w_uk"], pos, self.theta, self.q_lat,
-                 self.q_rope, self.ws_q, main)
-        main.wait_event(self.ev_join)  # attention reads the row the append wrote
+                       self.ws_att, main)
         decode_attention_prepared(self.q_lat, self.q_rope, kv_cache, block_table, seqlens_after,
                                   self.max_seqlen, self.scale, self.num_splits, self.o_lat,
                                   self.lse, self.ws_att, main)
@@ -557,6 +579,5 @@ class DecodeStep:
         return y
 
     def check(self, stream=None) -> int:
-        codes = [check_device_status(ws, stream) for ws in
-                 (self.ws_append, self.ws_q, self.ws_att, self.ws_out)]
+        codes = [check_device_status(ws, stream) for ws in (self.ws_q, self.ws_att, self.ws_out)]
         return next((c for c in codes if c), 0)

@@ -86,19 +86,20 @@ def test_decode_plan_reports_splits_and_launches(lib):
 def test_projection_launches_validation_and_partial_plan(lib):
     """Launch counts of the projection calls: argument rules, and with no visible device the
     plan that writes split-K partials for a finalize launch (append 2, absorb_q 4 or 6 with W_QR
-    and RoPE separate above 128 sequences, out_absorb 3)."""
+    and RoPE separate above 128 sequences, out_absorb 3, the combined call both calls' sum)."""
     import torch
     from mla_latent_kv_13_gb300 import mla
-    assert lib.mla_projection_launches(0, 7168, 1536, 128, None, None, None) == 1
-    assert lib.mla_projection_launches(128, 7000, 1536, 128, None, None, None) == 1
-    assert lib.mla_projection_launches(128, 7168, 1500, 128, None, None, None) == 1
-    assert lib.mla_projection_launches(128, 7168, 1536, 48, None, None, None) == 2
-    a, q, o = mla.projection_launches(128, 7168, 1536, 128)
-    assert a in (1, 2) and q in (3, 4) and o in (2, 3)
+    assert lib.mla_projection_launches(0, 7168, 1536, 128, None, None, None, None) == 1
+    assert lib.mla_projection_launches(128, 7000, 1536, 128, None, None, None, None) == 1
+    assert lib.mla_projection_launches(128, 7168, 1500, 128, None, None, None, None) == 1
+    assert lib.mla_projection_launches(128, 7168, 1536, 48, None, None, None, None) == 2
+    a, q, o, aq = mla.projection_launches(128, 7168, 1536, 128)
+    assert a in (1, 2) and q in (3, 4) and o in (2, 3) and aq in (3, 4, 5, 6)
     assert mla.projection_launches(200, 7168, 1536, 128)[1] in (5, 6)
     if not torch.cuda.is_available():
-        assert mla.projection_launches(128, 7168, 1536, 128) == (2, 4, 3)
-        assert mla.projection_launches(200, 7168, 1536, 128) == (2, 6, 3)
+        # no device: partials everywhere, the combined call runs the two calls
+        assert mla.projection_launches(128, 7168, 1536, 128) == (2, 4, 3, 6)
+        assert mla.projection_launches(200, 7168, 1536, 128) == (2, 6, 3, 8)
 
 
 def test_decode_output_alignment_checked_before_launch(lib):

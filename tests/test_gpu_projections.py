@@ -57,6 +57,11 @@ def test_append_real_inputs_within_fp32_summation_bound(mla, B, dm):
     cache = np.zeros((nb, 64, 576), np.uint16)
     got, ref, st = _append_both(mla, h, w, pos, bt, cache)
     assert st == 0
+    _check_appended_rows(got, ref, h, w, pos, bt, dm)
+
+
+def _check_appended_rows(got, ref, h, w, pos, bt, dm):
+    B = h.shape[0]
     diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
     # bf16 bit patterns of same-sign values differ by the number of ulps between them
     assert (diff > 0).mean() < 0.01
@@ -146,8 +151,67 @@ def test_out_absorb(mla, B, dm, H, rows):
 
 def test_projection_launches_on_device(mla):
     """On a full-size part (148 or more SMs) the headline shapes' split-K products all fit as
-    clusters: append, W_DQ and W_O each one launch (append 1, absorb_q 3, out_absorb 2)."""
+    clusters: append, W_DQ and W_O each one launch (append 1, absorb_q 3, out_absorb 2), and
+    W_DQ with W_DKR one launch in the combined call (3)."""
     import torch
     if torch.cuda.get_device_properties(0).multi_processor_count < 148:
         pytest.skip("a smaller part may plan partials")
-    assert mla.projection_launches(128, 7168, 1536, 128) == (1, 3, 2)
+    assert mla.projection_launches(128, 7168, 1536, 128) == (1, 3, 2, 3)
+
+
+
+# append_kv and absorb_q in one call: W_DQ and W_DKR in one cluster-reduced launch (8 or 6
+# splits over both products' tiles; 200 sequences: two row tiles)
+@pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
+                                           (100, 1024, 512, 32, None),
+                                           (200, 2048, 1536, 16, [0, 127, 128, 199]),
+                                           (128, 7168, 1536, 128, [0, 61, 127])])
+def test_append_absorb_q(mla, B, dm, ql, H, rows):
+    p = _proj(B, dm, ql, H, 6)
+    rng = np.random.default_rng(7)
+    w_dkr = bf16(rng.standard_normal((576, dm)) * 0.02)
+    nb = 3 * B
+    bt = rng.permutation(nb).astype(np.int32).reshape(B, 3)
+    pos = rng.integers(0, 192, B).astype(np.int32)
+    cache = np.zeros((nb, 64, 576), np.uint16)
+    c_gpu = dev_bf16(cache)
+    q_lat, q_rope, ws = mla.append_absorb_q(dev_bf16(p["h"]), dev_bf16(w_dkr), dev_i32(pos),
+                                            dev_i32(bt), c_gpu, dev_bf16(p["w_dq"]),
+                                            dev_bf16(p["w_uq"]), dev_bf16(p["w_qr"]),
+                                            dev_bf16(p["w_uk"]))
+    assert mla.check_device_status(ws) == 0
+    c_ref = cache.copy()
+    oracle.append_kv(p["h"], w_dkr, pos, bt, c_ref, allow_range=True)
+    _check_appended_rows(host_bits(c_gpu), c_ref, p["h"], w_dkr, pos, bt, dm)
+    rows = list(range(B)) if rows is None else rows
+    # the query side takes the append's positions
+    rl, rr = oracle.absorb_q(p["h"][rows], p["w_dq"], p["w_uq"], p["w_qr"], p["w_uk"], pos[rows])
+    assert_close_rows(host_f64_from_bf16(q_lat)[rows], rl, "q_lat")
+    assert_close_rows(host_f64_from_bf16(q_rope)[rows], rr, "q_rope")
+
+
+def test_append_absorb_q_out_of_range_is_flagged_and_dropped(mla):
+    """A row outside the cache is flagged and dropped by the combined launch's append side;
+    the query side is computed for every row."""
+    rng = np.random.default_rng(8)
+    B, dm, ql, H = 3, 256, 128, 16
+    p = _proj(B, dm, ql, H, 9)
+    w_dkr = bf16(rng.standard_normal((576, dm)))
+    bt = np.array([[0], [1], [99]], np.int32)
+    pos = np.array([3, 64, 0], np.int32)
+    cache = np.zeros((3, 64, 576), np.uint16)
+    c_gpu = dev_bf16(cache)
+    q_lat, q_rope, ws = mla.append_absorb_q(dev_bf16(p["h"]), dev_bf16(w_dkr), dev_i32(pos),
+                                            dev_i32(bt), c_gpu, dev_bf16(p["w_dq"]),
+                                            dev_bf16(p["w_uq"]), dev_bf16(p["w_qr"]),
+                                            dev_bf16(p["w_uk"]))
+    assert mla.check_device_status(ws) == 4
+    c_ref = cache.copy()
+    oracle.append_kv(p["h"], w_dkr, pos, bt, c_ref, allow_range=True)
+    got = host_bits(c_gpu)
+    written = np.zeros(got.shape[:2], bool)
+    written[0, 3] = True
+    assert np.array_equal(got[~written], c_ref[~written])  # only sequence 0 was written
+    rl, rr = oracle.absorb_q(p["h"], p["w_dq"], p["w_uq"], p["w_qr"], p["w_uk"], pos)
+    assert_close_rows(host_f64_from_bf16(q_lat), rl, "q_lat")
+    assert_close_rows(host_f64_from_bf16(q_rope), rr, "q_rope")
