@@ -166,12 +166,17 @@ mla_status_t mla_decode_attention(const mla_bf16_t *q_lat, const mla_bf16_t *q_r
 /*
  * The balanced schedule of mla_decode_attention computed ahead of the call (no counterpart
  * on the pages: it depends only on the sequence lengths, so a decode step computes it once
- * for every layer, and may compute it on another stream, next to the query projections).
+ * for every layer, on the attention's stream or another one).
  * Writes the schedule into the workspace: the same workspace layout, the same arguments
  * (B, H, max_seqlen, num_splits) as the attention calls that use it; does nothing when the
  * plan for them is a fixed split. seqlens [B] device int32 as in mla_decode_attention
  * (lengths outside [0, max_seqlen] are recorded and clamped here). The workspace's first
  * 256 bytes (the error word) must be zero as for mla_decode_attention.
+ * The schedule kernel reads seqlens before it waits for its predecessor in the stream (it
+ * stores nothing until then), so it runs beside that kernel: seqlens must not be written by
+ * a kernel that lets its successors start before it completes (programmatic dependent
+ * launch); no kernel of this library writes it, and a kernel without that opt-in completes
+ * before this one starts. The same holds for mla_decode_attention's own schedule launch.
  * MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED / MLA_ERR_WORKSPACE as mla_decode_attention.
  */
 mla_status_t mla_decode_prepare(const int32_t *seqlens, int B, int H, int max_seqlen,
