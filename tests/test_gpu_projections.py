@@ -120,6 +120,9 @@ def _proj(B, dm, ql, H, seed):
 @pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
                                            (100, 1024, 512, 32, None),
                                            (5, 512, 256, 128, None),
+                                           # 256 row x column tiles: no cluster split fits,
+                                           # W_DQ writes partials for a reduction launch
+                                           (4096, 256, 1024, 16, [0, 2047, 4095]),
                                            (200, 2048, 1536, 16, [0, 127, 128, 150, 199]),
                                            (128, 7168, 1536, 128, [0, 61, 127])])
 def test_absorb_q(mla, B, dm, ql, H, rows):
@@ -137,6 +140,7 @@ def test_absorb_q(mla, B, dm, ql, H, rows):
 # W_O's k-splits reduced in their cluster: 128-column tiles with ragged rows (100), 256-column
 # tiles over two row tiles (200)
 @pytest.mark.parametrize("B,dm,H,rows", [(3, 256, 16, None), (100, 1024, 32, None),
+                                         (4096, 512, 16, [0, 1000, 4095]),  # W_O: partials
                                          (200, 7168, 64, [0, 127, 128, 199]),
                                          (128, 7168, 128, [1, 64, 100])])
 def test_out_absorb(mla, B, dm, H, rows):
@@ -157,6 +161,11 @@ def test_projection_launches_on_device(mla):
     if torch.cuda.get_device_properties(0).multi_processor_count < 148:
         pytest.skip("a smaller part may plan partials")
     assert mla.projection_launches(128, 7168, 1536, 128) == (1, 3, 2, 3)
+    # the large-batch parity cases above take the partial-writing paths
+    assert mla.projection_launches(4096, 256, 1024, 16)[1] == 6  # W_DQ 2, W_UQ/W_QR/RoPE 3, W_UK 1
+    assert mla.projection_launches(4096, 512, 128, 16)[2] == 3   # W_UV 1, W_O 2
+    a, _, _, both = mla.projection_launches(2000, 256, 128, 16)
+    assert a == 2 and both == 7  # the two calls: append 2, absorb_q 1 + 3 + 1
 
 
 
@@ -165,7 +174,10 @@ def test_projection_launches_on_device(mla):
 @pytest.mark.parametrize("B,dm,ql,H,rows", [(3, 256, 128, 16, None),
                                            (100, 1024, 512, 32, None),
                                            (200, 2048, 1536, 16, [0, 127, 128, 199]),
-                                           (128, 7168, 1536, 128, [0, 61, 127])])
+                                           (128, 7168, 1536, 128, [0, 61, 127]),
+                                           # 96 tiles: no cluster split fits, the two calls
+                                           # run one after the other
+                                           (2000, 256, 128, 16, [0, 999, 1999])])
 def test_append_absorb_q(mla, B, dm, ql, H, rows):
     p = _proj(B, dm, ql, H, 6)
     rng = np.random.default_rng(7)
