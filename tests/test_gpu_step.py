@@ -44,3 +44,40 @@ def test_full_step_sampled():
                                       d["seqlens_after"][rows], d["scale"])
     y_ref = oracle.out_absorb(o_lat, d["w_uv"], d["w_o"])
     assert_close_rows(y_gpu[rows], y_ref, "y")
+
+
+def test_small_ragged_step_every_row():
+    """DecodeStep at 64 heads, d_model 1024, q_lora 512 on 20 sequences of ragged lengths
+    (one whose only row is the appended one, block edges at 64 and 65, up to 1000): the
+    combined append + query call, the schedule, attention and the output projections, every
+    row against the oracle's composition."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_13_gb300 import mla
+    lens = (1, 2, 63, 64, 65, 66, 127, 128, 129, 200, 300, 333, 400, 512, 513, 640, 700, 800,
+            999, 1000)
+    w = synth.Workload("step_small", len(lens), 64, lens, None, shuffled=True, full_step=True,
+                       d_model=1024, q_lora=512)
+    d = synth.make_step_inputs(w, seed=3)
+    names = ["w_dkr", "w_dq", "w_uq", "w_qr", "w_uk", "w_uv", "w_o"]
+    wt = {k: dev_bf16(d[k]) for k in names}
+    cache = dev_bf16(d["kv_cache"])
+    bt = dev_i32(d["block_table"])
+    step = mla.DecodeStep(wt, d["B"], d["H"], int(d["seqlens_after"].max()))
+    y = step(dev_bf16(d["h"]), dev_i32(d["pos"]), dev_i32(d["seqlens_after"]), bt, cache)
+    assert step.check() == 0
+    y_gpu = host_f64_from_bf16(y)
+
+    ref_cache = d["kv_cache"].copy()
+    oracle.append_kv(d["h"], d["w_dkr"], d["pos"], d["block_table"], ref_cache)
+    for b in range(d["B"]):  # the appended rows (<= 1 bf16 ulp)
+        p = int(d["pos"][b])
+        blk = int(d["block_table"][b, p // 64])
+        got = host_bits(cache[blk, p % 64])
+        diff = np.abs(got.astype(np.int32) - ref_cache[blk, p % 64].astype(np.int32))
+        assert diff.max() <= 1
+    q_lat, q_rope = oracle.absorb_q(d["h"], d["w_dq"], d["w_uq"], d["w_qr"], d["w_uk"], d["pos"])
+    o_lat, _ = oracle.decode_absorbed(q_lat, q_rope, ref_cache, d["block_table"],
+                                      d["seqlens_after"], d["scale"])
+    y_ref = oracle.out_absorb(o_lat, d["w_uv"], d["w_o"])
+    assert_close_rows(y_gpu, y_ref, "y")
