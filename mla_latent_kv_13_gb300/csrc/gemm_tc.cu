@@ -598,8 +598,9 @@ cudaError_t launch_tile(const CUtensorMap &ma, const CUtensorMap &mb, TcGemmArgs
                               mb2 ? *mb2 : mb, mc2 ? *mc2 : mc, g);
 }
 
-// Clusters of `s` CTAs of gemm_tc_kernel<TN, BN, CRED> (s ring stages' worth of k-blocks
-// each at most) that the device holds at once; cached per (BN, s).
+// Clusters of `s` CTAs of a cluster-reduced gemm_tc_kernel at width BN with `ns` ring stages
+// that the device holds at once (cudaOccupancyMaxActiveClusters); cached per (BN, s) for the
+// last ring asked about.
 template <int BN> int cluster_capacity(int s, int ns) {
     static int cap[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     static int cap_ns[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
@@ -653,10 +654,6 @@ int gemm_block_n(int M, int N, int K) {
     return gemm_block_n(N, K);
 }
 
-// Cluster-reduced split-K for a TN product of one batch with bf16 output: the tile width and
-// the most k-splits (2..8, at least two k-blocks each) whose clusters the device holds for
-// every output tile at once, with room to spare, taking the width that runs the most CTAs;
-// 0 if no such split exists (the caller then writes partials for a finalize kernel).
 namespace {
 // The most k-splits (2..8, at least two k-blocks each, every split non-empty) whose clusters
 // of `tiles` output tiles of width bn the device holds at once with room to spare; 0 if none.
@@ -683,6 +680,10 @@ int cluster_splits(long tiles, int bn, int kblocks, int *per_out) {
 }
 }  // namespace
 
+// Cluster-reduced split-K for a TN product of one batch with bf16 output: the tile width and
+// the most k-splits (2..8, at least two k-blocks each) whose clusters the device holds for
+// every output tile at once, with room to spare, taking the width that runs the most CTAs;
+// 0 if no such split exists (the caller then writes partials for a finalize kernel).
 int gemm_cluster_plan(int M, int N, int K, int *k_per_split, int *block_n) {
     if (M < 1 || N < 4 || N % 4 || K < 2 * BK || K % BK) return 0;
     const int kblocks = K / BK;
