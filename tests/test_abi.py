@@ -148,6 +148,41 @@ def test_prepare_validation_before_launch(lib):
     assert f(sl, 4, 128, 64, 1, ws, 256, None) == 0
 
 
+def test_append_absorb_q_validation_before_launch(lib):
+    """mla_append_absorb_q checks the arguments of both calls it stands for, and its workspace
+    is the larger of theirs; every call below returns before anything is launched."""
+    from mla_latent_kv_13_gb300 import mla
+    f = lib.mla_append_absorb_q
+    vp, i, fl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    f.argtypes = [vp, i, i, vp, vp, vp, i, vp, i, vp, i, vp, vp, vp, i, fl, vp, sz, vp, vp, vp]
+    f.restype = ctypes.c_int
+    p = 1 << 20  # a 256-byte-aligned stand-in address, never dereferenced
+    need = mla.append_absorb_q_workspace_size(128, 7168, 1536, 128)
+    assert need >= max(mla.append_kv_workspace_size(128, 7168),
+                       mla.absorb_q_workspace_size(128, 7168, 1536, 128))
+    ok = [p, 128, 7168, p, p, p, 64, p, 1024, p, 1536, p, p, p, 128, 10000.0, p, need, p, p, None]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["h", "B", "dm", "w_dkr", "pos", "bt", "maxb", "cache", "nblk", "w_dq", "ql",
+                 "w_uq", "w_qr", "w_uk", "H", "theta", "ws", "ws_bytes", "q_lat", "q_rope"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(h=None) == 1
+    assert call(cache=None) == 1
+    assert call(B=0) == 1
+    assert call(dm=7000) == 1
+    assert call(ql=1500) == 1
+    assert call(maxb=0) == 1
+    assert call(theta=0.0) == 1
+    assert call(H=48) == 2
+    assert call(cache=p + 8) == 1     # the cache must be 16-byte aligned
+    assert call(ws=p + 16) == 1       # the workspace 256-byte aligned
+    assert call(ws_bytes=need - 1) == 3
+
+
 def test_multi_query_validation_before_launch(lib):
     from mla_latent_kv_13_gb300 import mla
     # s_q * H rows must fit the 128 TMEM lanes; H itself a supported head count
