@@ -46,11 +46,13 @@ def test_full_step_sampled():
     assert_close_rows(y_gpu[rows], y_ref, "y")
 
 
-def test_small_ragged_step_every_row():
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_small_ragged_step_every_row(num_splits):
     """DecodeStep at 64 heads, d_model 1024, q_lora 512 on 20 sequences of ragged lengths
     (one whose only row is the appended one, block edges at 64 and 65, up to 1000): the
-    combined append + query call, the schedule, attention and the output projections, every
-    row against the oracle's composition."""
+    combined append + query call, the schedule (or a fixed split: none, or three ranges
+    merged), attention and the output projections, every row against the oracle's
+    composition."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from mla_latent_kv_13_gb300 import mla
@@ -63,7 +65,8 @@ def test_small_ragged_step_every_row():
     wt = {k: dev_bf16(d[k]) for k in names}
     cache = dev_bf16(d["kv_cache"])
     bt = dev_i32(d["block_table"])
-    step = mla.DecodeStep(wt, d["B"], d["H"], int(d["seqlens_after"].max()))
+    step = mla.DecodeStep(wt, d["B"], d["H"], int(d["seqlens_after"].max()),
+                          num_splits=num_splits)
     y = step(dev_bf16(d["h"]), dev_i32(d["pos"]), dev_i32(d["seqlens_after"]), bt, cache)
     assert step.check() == 0
     y_gpu = host_f64_from_bf16(y)
